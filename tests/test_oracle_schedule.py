@@ -1,0 +1,96 @@
+"""Pins of the oracle's prefix scheduler (DSpark paper section 3.2.2, and the
+Chinese translation page's Algorithm 1) against brute force."""
+import numpy as np
+import pytest
+
+import oracle
+from tests._sched import exhaustive_best, greedy_order, theta_of
+
+
+def _convex_profile(rng, n):
+    a, b, c = rng.uniform(1, 5), rng.uniform(0.01, 1.0), rng.uniform(0, 0.2)
+    N = np.arange(n, dtype=np.float64)
+    return a + b * N + c * N * N
+
+
+def _confidences(rng, R, g):
+    c = rng.uniform(0, 1, (R, g)).astype(np.float32)
+    c[rng.uniform(size=(R, g)) < 0.15] = 1.0   # ties inside a request
+    c[rng.uniform(size=(R, g)) < 0.08] = 0.0   # excluded candidates
+    return c
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_early_stop_is_optimal_for_convex_step_time(seed):
+    """For increasing convex T(N) Theta is unimodal along the greedy path, so the
+    causal early-stopping scheduler reaches the brute-force maximum."""
+    rng = np.random.default_rng(seed)
+    R, g = int(rng.integers(1, 4)), int(rng.integers(1, 5))
+    conf = _confidences(rng, R, g)
+    T = _convex_profile(rng, R * (g + 1) + 1)
+    s = oracle.schedule(conf, T, early_stop=True)
+    best, _ = exhaustive_best(conf, T)
+    assert abs(s["theta_best"] - best) <= 1e-12 * best
+    assert abs(theta_of(s["verify_len"], conf, T) - s["theta_best"]) <= 1e-12 * best
+    assert s["n_admitted"] == int(s["verify_len"].sum())
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_global_search_is_optimal_for_any_step_time(seed):
+    """Without the break (section 5.2) the best greedy prefix is the brute-force
+    optimum for any T(N): for a fixed batch size the top survival values are
+    optimal and are prefix-closed."""
+    rng = np.random.default_rng(100 + seed)
+    R, g = int(rng.integers(1, 4)), int(rng.integers(1, 5))
+    conf = _confidences(rng, R, g)
+    T = rng.uniform(1.0, 3.0, R * (g + 1) + 1)        # jagged profile
+    s = oracle.schedule(conf, T, early_stop=False)
+    best, _ = exhaustive_best(conf, T)
+    assert abs(s["theta_best"] - best) <= 1e-12 * best
+    assert abs(theta_of(s["verify_len"], conf, T) - best) <= 1e-12 * best
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_early_stop_is_first_drop_on_jagged_profile(seed):
+    """With a jagged T the causal scheduler stops at the first non-improvement
+    along the globally sorted admission path."""
+    rng = np.random.default_rng(200 + seed)
+    R, g = int(rng.integers(1, 5)), int(rng.integers(1, 6))
+    conf = _confidences(rng, R, g)
+    T = rng.uniform(1.0, 3.0, R * (g + 1) + 1)
+    s = oracle.schedule(conf, T, early_stop=True)
+    order = greedy_order(conf)
+    ell = np.zeros(R, int)
+    prev = theta_of(ell, conf, T)
+    n_star = 0
+    for n, (r, j, _) in enumerate(order, 1):
+        ell[r] = j
+        th = theta_of(ell, conf, T)
+        if not th > prev:
+            break
+        prev, n_star = th, n
+    assert s["n_admitted"] == n_star
+    assert abs(s["theta_best"] - prev) <= 1e-12 * prev
+    expect = np.zeros(R, int)
+    for r, j, _ in order[:n_star]:
+        expect[r] = max(expect[r], j)
+    np.testing.assert_array_equal(s["verify_len"], expect)
+
+
+def test_scheduled_workload_is_sane():
+    from speculative_decoding_verification_41_gb300 import workloads
+    R, g = 512, 16
+    conf = workloads.make_confidences(R, g, seed=7)
+    T = workloads.step_time_profile(R * (g + 1) + 1)
+    s = oracle.schedule(conf, T, early_stop=True)
+    ell = s["verify_len"]
+    assert ell.min() >= 0 and ell.max() <= g
+    assert s["n_admitted"] == ell.sum() and s["n_admitted"] > 0
+    # the admitted candidates are exactly the top n* survival values
+    a = np.cumprod(conf.astype(np.float64), axis=1)
+    chosen = np.concatenate([a[r, :ell[r]] for r in range(R)])
+    rest = np.concatenate([a[r, ell[r]:] for r in range(R)])
+    assert chosen.min() >= rest.max()
+    # flat profile: every candidate is admitted
+    s2 = oracle.schedule(conf, np.full(R * (g + 1) + 1, 4.0), early_stop=True)
+    assert np.all(s2["verify_len"] == g)
