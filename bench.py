@@ -1,0 +1,403 @@
+"""Benchmark of the DSpark verification hot path on GB300.
+
+A step is one pass of the whole path over one batch: the prefix scheduler
+(dspark_schedule) on per-position confidences, then batched verification
+(dspark_verify) of the lengths it chose, over B=256 requests, gamma=16 draft
+positions, V=129,280 bf16 logits, temperature 0.7 (the headline workload). The
+step-time profile is flat, so the scheduler admits every candidate and all 16
+positions of every request are verified, as that workload specifies.
+
+Metric: verified draft positions per second (sum of verify lengths / step time).
+Inputs are resident in HBM before timing; the logits (2.18 GB) exceed L2, so no
+flush is needed between steps. `e2e` repeats the step through the same C-ABI
+calls from pinned host buffers, host->device copies and the device->host read
+of the results inside the timed region.
+
+--impl reference times the CPU oracle (the plain fp64 C implementation under
+oracle/) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "b256_g16_v129280_bf16"
+METRIC = "verified draft positions/sec (B=256, gamma=16, V=129280, bf16)"
+UNIT = "positions/s"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--cpu-sample", type=int, default=256, help="requests in the oracle's sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--batch", type=int, default=None,
+                   help="requests per step (default: the headline 256); a smaller batch of the "
+                        "same recipe serves the ncu capture case")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU, independent replicas)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def max_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+def cpu_sample_inputs(n_req: int, seed: int = 7):
+    """A bounded sample of the headline workload, generated on the host with the
+    same recipe (n_req requests)."""
+    from speculative_decoding_verification_41_gb300 import workloads
+    cfg = workloads.CONFIGS[WORKLOAD]
+    return workloads.make_verify(n_req, cfg["gamma"], cfg["V"], cfg["dtype"], cfg["temperature"],
+                                 rho=cfg["rho"], verify_len="full", ragged=False, seed=seed,
+                                 device="cpu")
+
+
+def run_oracle_sample(vi, nthreads: int):
+    import oracle
+    tl = vi.target_logits.view(torch.int16).numpy().view(np.uint16)
+    dl = vi.draft_logits.view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    oracle.verify(tl, dl, vi.draft_tokens.numpy(), vi.verify_len.numpy(), vi.uniforms.numpy(),
+                  vi.temperature, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    cores = oracle.max_threads()
+    n_req = max(1, min(args.cpu_sample, 256))
+    vi = cpu_sample_inputs(n_req)
+    positions = int(vi.verify_len.sum())
+    for _ in range(args.warmup):
+        run_oracle_sample(vi, cores)
+    times = [run_oracle_sample(vi, cores) for _ in range(args.steps)]
+    per = statistics.median(times)
+    value = positions / per
+    sample = (f"{n_req} of 256 requests of {WORKLOAD} per step (all {vi.gamma} positions, "
+              f"host-generated with the same recipe), fp64 oracle, OpenMP over requests")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_requests": n_req},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample, "cpu": cpu_model()},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# native arm
+# ---------------------------------------------------------------------------
+def native_arm(args):
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(ws, "nccl")
+    from speculative_decoding_verification_41_gb300 import binding, workloads
+    from speculative_decoding_verification_41_gb300 import build as cuda_build
+    if rank == 0 or not os.path.exists(cuda_build.LIB_PATH):
+        cuda_build.build()
+    barrier(dist, dev)
+    binding.load()
+
+    if args.batch is None:
+        vi = workloads.make_config(WORKLOAD, device=dev)
+    else:
+        cfg = workloads.CONFIGS[WORKLOAD]
+        vi = workloads.make_verify(args.batch, cfg["gamma"], cfg["V"], cfg["dtype"],
+                                   cfg["temperature"], rho=cfg["rho"], verify_len="full",
+                                   seed=7, device=dev, name=f"{WORKLOAD}_b{args.batch}")
+    sched = workloads.make_schedule(vi.B, vi.gamma, seed=7 + rank, device=dev, flat_profile=True)
+    vbuf = binding.VerifyBuffers(vi.B, vi.gamma, vi.V, dev)
+    sbuf = binding.ScheduleBuffers(vi.B, vi.gamma, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        s = binding.dspark_schedule(sched.confidences, sched.step_time_ms, buffers=sbuf)
+        binding.dspark_verify(vi.target_logits, vi.draft_logits, vi.draft_tokens, s["verify_len"],
+                              vi.uniforms, vi.temperature, buffers=vbuf)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(sbuf.device_status.item()) != 0 or int(vbuf.device_status.item()) != 0:
+        raise SystemExit("device status not OK during warm-up")
+    ell = sbuf.verify_len.cpu().numpy()
+    positions = int(ell.sum())
+    logit_bytes = vi.logit_bytes(ell)
+
+    # timed region: per-call events on the launching stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        s = binding.dspark_schedule(sched.confidences, sched.step_time_ms, buffers=sbuf)
+        ev[i][1].record(stream)
+        binding.dspark_verify(vi.target_logits, vi.draft_logits, vi.draft_tokens,
+                              s["verify_len"], vi.uniforms, vi.temperature, buffers=vbuf)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(dist, total_ms, dev)
+    sched_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    verify_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_per_step = total_ms / args.steps
+    value = positions * ws * args.steps / (total_ms * 1e-3)
+
+    # end to end: pinned host buffers -> device, both calls, results back
+    e2e = None
+    if args.e2e_steps > 0:
+        host = {k: getattr(vi, k).cpu().pin_memory() for k in
+                ("target_logits", "draft_logits", "draft_tokens", "uniforms")}
+        host_conf = sched.confidences.cpu().pin_memory()
+        host_prof = sched.step_time_ms.cpu().pin_memory()
+        dbuf = {k: torch.empty_like(getattr(vi, k)) for k in host}
+        dconf = torch.empty_like(sched.confidences)
+        dprof = torch.empty_like(sched.step_time_ms)
+        out_acc = torch.empty(vi.B, dtype=torch.int32).pin_memory()
+        out_em = torch.empty(vi.B, vi.gamma + 1, dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
+            host_conf.numel() * 4 + host_prof.numel() * 8
+        d2h = out_acc.numel() * 4 + out_em.numel() * 4
+
+        def e2e_step():
+            for k, t in host.items():
+                dbuf[k].copy_(t, non_blocking=True)
+            dconf.copy_(host_conf, non_blocking=True)
+            dprof.copy_(host_prof, non_blocking=True)
+            s = binding.dspark_schedule(dconf, dprof, buffers=sbuf)
+            o = binding.dspark_verify(dbuf["target_logits"], dbuf["draft_logits"],
+                                      dbuf["draft_tokens"], s["verify_len"], dbuf["uniforms"],
+                                      vi.temperature, buffers=vbuf)
+            out_acc.copy_(o["accepted_len"], non_blocking=True)
+            out_em.copy_(o["emitted_tokens"], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(dist, dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(dist, a.elapsed_time(b), dev)
+        e2e = {"value": positions * ws * args.e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms / args.e2e_steps}
+        del host, dbuf
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        cores = oracle.max_threads()
+        n_req = max(1, min(args.cpu_sample, 256))
+        svi = cpu_sample_inputs(n_req)
+        ts = [run_oracle_sample(svi, cores) for _ in range(3)]
+        t = statistics.median(ts)
+        cpu = {"value": int(svi.verify_len.sum()) / t, "unit": UNIT, "cores": cores,
+               "kind": "oracle",
+               "sample": f"{n_req} of 256 requests of {WORKLOAD} (host-generated, same recipe), "
+                         f"median of 3 passes, {t:.2f} s wall each, OpenMP over requests",
+               "cpu": cpu_model()}
+
+    if rank != 0:
+        return
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or 6800.0
+    v_med = statistics.median(verify_ms)
+    achieved = logit_bytes / (v_med * 1e-3) / 1e9
+    traffic = measured_traffic(logit_bytes)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": vi.B, "gamma": vi.gamma, "V": vi.V,
+                   "temperature": vi.temperature, "positions_per_step": positions,
+                   "logit_bytes_per_step": logit_bytes,
+                   "l2": "inputs (2.18 GB) larger than L2, no flush",
+                   "step": "dspark_schedule (flat profile) + dspark_verify"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "dspark_verify call (median CUDA-event time of the call)",
+                     "peak_source": peak_src},
+        "timing_ms": {"verify_median": v_med, "verify_p10": float(np.percentile(verify_ms, 10)),
+                      "verify_p90": float(np.percentile(verify_ms, 90)),
+                      "schedule_median": statistics.median(sched_ms)},
+        "gpu_launches": args.steps * 5,  # per step: k_schedule, k_plan, k_rowstats, k_verify, k_resample
+        "near_ties": int(vbuf.near_tie_count.item()),
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# DRAM traffic of the streaming kernel from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), scaled per logit byte; valid only for the kernel source it
+# was taken on (profiles/k_rowstats_tma_b32_g16_v129280_bf16.md).
+TRAFFIC_CAPTURE = {"sources_sha256": None, "dram_bytes": None, "logit_bytes": None}
+
+
+def kernel_sources_sha256() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_41_gb300", "csrc")
+    for f in ("dspark_verify.cu", "dspark_common.cuh"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()
+
+
+def measured_traffic(logit_bytes: int):
+    cap = TRAFFIC_CAPTURE
+    if not cap["sources_sha256"] or cap["sources_sha256"] != kernel_sources_sha256():
+        return None
+    return cap["dram_bytes"] / cap["logit_bytes"] * logit_bytes
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        native_arm(args)
+
+
+if __name__ == "__main__":
+    main()

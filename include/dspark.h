@@ -1,0 +1,191 @@
+/*
+ * dspark.h -- C-ABI of libdspark: batched speculative verification and the
+ * hardware-aware prefix scheduler of DSpark, on one GB300 GPU (sm_103a).
+ *
+ * Method: "DSpark: Confidence-Scheduled Speculative Decoding with
+ * Semi-Autoregressive Generation" (DeepSeek-AI / Peking University).
+ *   - dspark_verify: section 2.1 "Speculative Decoding" (accept x_k with
+ *     probability min(1, p_t^k(x_k) / p_d^k(x_k)), left to right, the first
+ *     rejection discards the rest of the block), section 1 (append one bonus
+ *     token), Appendix 8 (with nothing admitted the target samples a fresh token
+ *     from p_t). The residual distribution after a rejection,
+ *     max(0, p_t - p_d) renormalised, is the standard rule of the speculative
+ *     sampling papers the DSpark paper cites as [1] and [2].
+ *   - dspark_schedule: section 3.2.2 "Hardware-Aware Prefix Scheduler" and
+ *     Algorithm 1 of the Chinese translation page (prefix survival products,
+ *     global descending sort, greedy admission, early stop at the first
+ *     Theta <= Theta_best).
+ *
+ * Conventions for both calls:
+ *   - Every pointer is a DEVICE pointer to memory owned by the caller, unless
+ *     stated otherwise. The library allocates nothing, never synchronises the
+ *     host with the device, and enqueues all its work on `stream`.
+ *   - The return value reports errors detectable on the host before any launch
+ *     (DSPARK_ERR_INVALID_ARG, DSPARK_ERR_WORKSPACE) and launch failures
+ *     (DSPARK_ERR_CUDA). Nothing is enqueued when a host check fails.
+ *   - Errors in the data (a token outside [0, V), a verify length outside
+ *     [0, gamma], a uniform outside [0, 1), inconsistent row offsets, a
+ *     confidence outside [0, 1] or NaN, non-finite row statistics) are found on
+ *     the device and written to *device_status (DSPARK_ERR_BAD_DATA); the first
+ *     error recorded wins. The caller reads it after its own synchronisation.
+ *     Outputs for the affected requests are then unspecified but every write
+ *     stays inside the output buffers. A bounded wait that gives up writes
+ *     DSPARK_ERR_TIMEOUT. The library never traps or asserts on the device.
+ *   - The first call on each device sets kernel attributes (dynamic shared
+ *     memory limits); make one call before capturing a CUDA graph.
+ *   - Calls that share a workspace must not overlap on the GPU.
+ */
+#ifndef DSPARK_H
+#define DSPARK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t / CUstream */
+
+typedef enum {
+  DSPARK_OK = 0,
+  DSPARK_ERR_INVALID_ARG = 1,
+  DSPARK_ERR_CUDA = 2,
+  DSPARK_ERR_WORKSPACE = 3,
+  DSPARK_ERR_TIMEOUT = 4,
+  DSPARK_ERR_BAD_DATA = 5
+} dspark_status;
+
+typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
+
+#define DSPARK_MAX_GAMMA 32
+/* Bytes of one row that form one work unit (one partial statistic) of the
+   row-statistics pass. */
+#define DSPARK_TILE_BYTES 16384
+/* Tokens per segment of the inverse-CDF (resample) pass. */
+#define DSPARK_RESAMPLE_SEG 2048
+/* Near-tie windows: |u - ratio| < 1e-6 for a ratio test, |u*Z - C| < 1e-6*Z
+   for an inverse-CDF cut, |Theta(n) - Theta(n-1)| <= 1e-9*Theta(n-1) for a
+   scheduler comparison. Decisions inside a window are counted in
+   *near_tie_count; outside every window the results are exact functions of
+   the inputs. */
+#define DSPARK_TIE_EPS 1e-6
+#define DSPARK_SCHED_TIE_REL 1e-9
+
+#define DSPARK_ALIGN256(x) ((((size_t)(x)) + 255u) & ~(size_t)255u)
+#define DSPARK_CEILDIV(a, b) ((((size_t)(a)) + ((size_t)(b)) - 1u) / ((size_t)(b)))
+/* Work units per logit row (sized for 4-byte logits, the larger count). */
+#define DSPARK_TILES_PER_ROW(V) DSPARK_CEILDIV((V), DSPARK_TILE_BYTES / 4)
+#define DSPARK_SEGS_PER_ROW(V) DSPARK_CEILDIV((V), DSPARK_RESAMPLE_SEG)
+#define DSPARK_MAX_ROWS(B, gamma) ((size_t)(B) * (2u * (size_t)(gamma) + 1u))
+
+/* Workspace of dspark_verify, in bytes (256-byte aligned regions):
+   header, per-request row starts, row list, per-tile row statistics,
+   per-request resample descriptors, per-segment residual sums, tickets. */
+#define DSPARK_VERIFY_WS_BYTES(B, gamma, V)                                   \
+  ((size_t)256 + DSPARK_ALIGN256(((size_t)(B) + 1u) * 4u) +                   \
+   DSPARK_ALIGN256(DSPARK_MAX_ROWS(B, gamma) * 8u) +                          \
+   DSPARK_ALIGN256(DSPARK_MAX_ROWS(B, gamma) * DSPARK_TILES_PER_ROW(V) * 16u) + \
+   DSPARK_ALIGN256((size_t)(B) * 64u) +                                       \
+   DSPARK_ALIGN256((size_t)(B) * DSPARK_SEGS_PER_ROW(V) * 8u) +               \
+   DSPARK_ALIGN256((size_t)(B) * 4u))
+
+/* Workspace of dspark_schedule, in bytes: two (key, index) buffers for the
+   sort, per-request lengths and a header. */
+#define DSPARK_SCHEDULE_WS_BYTES(R, gamma)                                    \
+  ((size_t)256 + 2u * DSPARK_ALIGN256((size_t)(R) * (size_t)(gamma) * 8u) +     \
+   2u * DSPARK_ALIGN256((size_t)(R) * (size_t)(gamma) * 4u) +                   \
+   DSPARK_ALIGN256((size_t)(R) * 4u))
+
+/*
+ * dspark_verify -- one batched verification step (DSpark paper, section 2.1).
+ *
+ * For every request r with verify length l_r = verify_len[r] (0 <= l_r <=
+ * gamma), position k = 1..l_r is tested with the temperature-scaled softmax of
+ * target row k and draft row k at the draft token x_k = draft_tokens[r][k-1]:
+ *   p(v) = exp(z_v/T - M) / sum_w exp(z_w/T - M),  M = max_w z_w/T,
+ *   accept x_k  iff  uniforms[r][k-1] < p_t^k(x_k) / p_d^k(x_k),
+ * scanning left to right; the first rejection ends the block. With m tests
+ * passed: if m < l_r the token after the block is drawn from
+ * q = max(0, p_t^{m+1} - p_d^{m+1}) / Z, otherwise from p_t^{l_r+1} (the bonus
+ * distribution; with l_r = 0 a fresh token from p_t^1), as the smallest token
+ * id y whose running sum exceeds uniforms[r][gamma] * Z (Z = 1 for p_t).
+ *
+ * Arguments
+ *   target_logits  [rows_t][V] row-major, dtype; request r's row k-1 holds
+ *                  target position k (k = 1..l_r+1). Dense layout
+ *                  (target_row_off == NULL): rows_t = B*(gamma+1), request r
+ *                  starts at row r*(gamma+1). Ragged: starts at
+ *                  target_row_off[r]; needs target_row_off[r+1] -
+ *                  target_row_off[r] >= l_r + 1 and the buffer holds
+ *                  target_row_off[B] rows.
+ *   draft_logits   [rows_d][V]; request r's row k-1 holds draft position k
+ *                  (k = 1..l_r). Dense: r*gamma; ragged: draft_row_off[r],
+ *                  with draft_row_off[r+1] - draft_row_off[r] >= l_r.
+ *   draft_tokens   [B][gamma] int32; only the first l_r of a request are read.
+ *   verify_len     [B] int32.
+ *   uniforms       [B][gamma+1] float32 in [0, 1): gamma ratio tests, then the
+ *                  resample uniform.
+ *   temperature    T > 0 and finite; divides target and draft logits alike.
+ *   dtype          DSPARK_BF16 or DSPARK_F32 (both logit buffers).
+ *   B >= 0, 1 <= gamma <= DSPARK_MAX_GAMMA, V >= 1.
+ *   target_row_off, draft_row_off  [B+1] int64, both NULL (dense) or both set.
+ *   accepted_len   out [B] int32: m.
+ *   emitted_tokens out [B][gamma+1] int32: x_1..x_m, y, then -1.
+ *   probs_out      out [B][gamma][2] float32 or NULL: (p_t^k(x_k), p_d^k(x_k))
+ *                  for k <= l_r (computed for every verified position), -1 after.
+ *   near_tie_count out [1] uint32 or NULL: decisions inside a near-tie window.
+ *   device_status  out [1] int32 (required): DSPARK_OK or a data error.
+ *   workspace      device scratch of at least DSPARK_VERIFY_WS_BYTES(B, gamma,
+ *                  V) bytes, 256-byte aligned; no initial contents needed.
+ *   stream         CUDA stream (NULL = legacy default stream).
+ * Logit buffers must be 16-byte aligned for the TMA path; with rows whose byte
+ * length is not a multiple of 16 a slower load path is used.
+ */
+int dspark_verify(const void* target_logits, const void* draft_logits,
+                  const int32_t* draft_tokens, const int32_t* verify_len,
+                  const float* uniforms, float temperature, int32_t dtype,
+                  int32_t B, int32_t gamma, int32_t V,
+                  const int64_t* target_row_off, const int64_t* draft_row_off,
+                  int32_t* accepted_len, int32_t* emitted_tokens,
+                  float* probs_out, uint32_t* near_tie_count,
+                  int32_t* device_status, void* workspace,
+                  size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * dspark_schedule -- hardware-aware prefix scheduler (DSpark paper, section
+ * 3.2.2; Algorithm 1 of the Chinese translation page).
+ *
+ * a_{r,j} = prod_{i<=j} c_{r,i} (multiplied left to right in double); the
+ * candidates (r, j) with a_{r,j} > 0 are sorted by a descending (equal values
+ * keep the flattened order r*gamma + j - 1) and admitted one by one from
+ * B = R, tau = R, Theta_best = R / T(R): each admission sets l_r = j,
+ * B += 1, tau += a_{r,j}, Theta = tau / T(B) (that is tau * SPS(B) with
+ * SPS = 1/T); the loop stops at the first Theta <= Theta_best.
+ *
+ * Arguments
+ *   confidences   [R][gamma] float32, each in [0, 1].
+ *   step_time_ms  [n_profile] float64: the profiled step time T(N) of a
+ *                 target forward over N tokens, N = 0..n_profile-1; entries
+ *                 for N in [R, R*(gamma+1)] must be > 0.
+ *   n_profile     >= R*(gamma+1) + 1.
+ *   R >= 1, 1 <= gamma <= DSPARK_MAX_GAMMA.
+ *   verify_len    out [R] int32: the chosen l_r.
+ *   theta_best    out [1] float64 or NULL.
+ *   near_tie_count out [1] uint32 or NULL: evaluated comparisons inside the
+ *                 1e-9 relative window.
+ *   device_status out [1] int32 (required).
+ *   workspace     at least DSPARK_SCHEDULE_WS_BYTES(R, gamma) bytes.
+ */
+int dspark_schedule(const float* confidences, const double* step_time_ms,
+                    int64_t n_profile, int32_t R, int32_t gamma,
+                    int32_t* verify_len, double* theta_best,
+                    uint32_t* near_tie_count, int32_t* device_status,
+                    void* workspace, size_t workspace_bytes,
+                    struct CUstream_st* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H */

@@ -1,0 +1,230 @@
+"""Thin Python binding of libdspark (ctypes). Argument marshalling only: every
+step of verification and scheduling runs in the CUDA kernels of libdspark.so;
+there is no CPU path. Torch supplies device memory and the current stream.
+
+The two calls mirror include/dspark.h:
+  dspark_verify(...)   -- batched speculative verification (DSpark paper, section 2.1)
+  dspark_schedule(...) -- hardware-aware prefix scheduler (section 3.2.2, Algorithm 1)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from typing import Optional
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+HEADER = os.path.join(ROOT, "include", "dspark.h")
+LIB_PATH = os.path.join(PKG, "libdspark.so")
+
+STATUS_NAMES = {0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_CUDA",
+                3: "DSPARK_ERR_WORKSPACE", 4: "DSPARK_ERR_TIMEOUT", 5: "DSPARK_ERR_BAD_DATA"}
+DSPARK_F32, DSPARK_BF16 = 0, 1
+EXPORTED = ("dspark_verify", "dspark_schedule")
+
+
+class DsparkError(RuntimeError):
+    def __init__(self, where: str, code: int):
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+def _header_consts() -> dict:
+    txt = open(HEADER).read()
+    out = {}
+    for name in ("DSPARK_TILE_BYTES", "DSPARK_RESAMPLE_SEG", "DSPARK_MAX_GAMMA"):
+        out[name] = int(re.search(rf"#define {name} (\d+)", txt).group(1))
+    return out
+
+
+_CONSTS = _header_consts()
+MAX_GAMMA = _CONSTS["DSPARK_MAX_GAMMA"]
+
+
+def _a256(x: int) -> int:
+    return (x + 255) & ~255
+
+
+def _cdiv(a: int, b: int) -> int:
+    return (a + b - 1) // b
+
+
+def verify_workspace_bytes(B: int, gamma: int, V: int) -> int:
+    """Python statement of DSPARK_VERIFY_WS_BYTES (include/dspark.h)."""
+    rows = B * (2 * gamma + 1)
+    tiles = _cdiv(V, _CONSTS["DSPARK_TILE_BYTES"] // 4)
+    segs = _cdiv(V, _CONSTS["DSPARK_RESAMPLE_SEG"])
+    return (256 + _a256((B + 1) * 4) + _a256(rows * 8) + _a256(rows * tiles * 16)
+            + _a256(B * 64) + _a256(B * segs * 8) + _a256(B * 4))
+
+
+def schedule_workspace_bytes(R: int, gamma: int) -> int:
+    """Python statement of DSPARK_SCHEDULE_WS_BYTES (include/dspark.h)."""
+    n = R * gamma
+    return 256 + 2 * _a256(n * 8) + 2 * _a256(n * 4) + _a256(R * 4)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load libdspark.so. Raises if it has not been built: there is no fallback."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libdspark.so is not built ({p}); run "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(p)
+        vp, i32, i64, f32, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                 ctypes.c_size_t)
+        lib.dspark_verify.restype = ctypes.c_int
+        lib.dspark_verify.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp, vp, vp,
+                                      vp, vp, vp, vp, sz, vp]
+        lib.dspark_schedule.restype = ctypes.c_int
+        lib.dspark_schedule.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _require_cuda(name: str, t: torch.Tensor, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libdspark has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+class VerifyBuffers:
+    """Outputs and workspace of dspark_verify for a fixed (B, gamma, V), so that
+    repeated calls (and CUDA-graph capture) allocate nothing."""
+
+    def __init__(self, B: int, gamma: int, V: int, device, with_probs: bool = True):
+        self.B, self.gamma, self.V = B, gamma, V
+        dev = torch.device(device)
+        self.accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+        self.emitted_tokens = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
+        self.probs = torch.empty(B, gamma, 2, dtype=torch.float32, device=dev) if with_probs else None
+        self.near_tie_count = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.device_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.workspace = torch.empty(verify_workspace_bytes(B, gamma, V), dtype=torch.uint8, device=dev)
+        assert self.workspace.data_ptr() % 256 == 0
+
+
+def dspark_verify(target_logits: torch.Tensor, draft_logits: torch.Tensor,
+                  draft_tokens: torch.Tensor, verify_len: torch.Tensor, uniforms: torch.Tensor,
+                  temperature: float, target_row_off: Optional[torch.Tensor] = None,
+                  draft_row_off: Optional[torch.Tensor] = None, *, with_probs: bool = True,
+                  buffers: Optional[VerifyBuffers] = None, stream=None, check: bool = False) -> dict:
+    """Batched speculative verification through libdspark (see include/dspark.h).
+
+    Returns a dict of device tensors: accepted_len [B] int32, emitted_tokens
+    [B, gamma+1] int32, probs [B, gamma, 2] float32 (or None), near_tie_count
+    [1], device_status [1]. With check=True the call synchronises and raises on
+    a non-OK device status."""
+    dev = target_logits.device
+    if target_logits.dtype == torch.bfloat16:
+        dtype = DSPARK_BF16
+    elif target_logits.dtype == torch.float32:
+        dtype = DSPARK_F32
+    else:
+        raise ValueError(f"logits must be bfloat16 or float32, got {target_logits.dtype}")
+    _require_cuda("target_logits", target_logits)
+    _require_cuda("draft_logits", draft_logits, target_logits.dtype, dev)
+    _require_cuda("draft_tokens", draft_tokens, torch.int32, dev)
+    _require_cuda("verify_len", verify_len, torch.int32, dev)
+    _require_cuda("uniforms", uniforms, torch.float32, dev)
+    if (target_row_off is None) != (draft_row_off is None):
+        raise ValueError("pass both row-offset tensors or neither")
+    if target_row_off is not None:
+        _require_cuda("target_row_off", target_row_off, torch.int64, dev)
+        _require_cuda("draft_row_off", draft_row_off, torch.int64, dev)
+    B, gamma = draft_tokens.shape
+    V = target_logits.shape[-1]
+    if draft_logits.shape[-1] != V:
+        raise ValueError("target and draft vocabularies differ")
+    if uniforms.shape != (B, gamma + 1) or verify_len.shape != (B,):
+        raise ValueError("uniforms must be [B, gamma+1] and verify_len [B]")
+    buf = buffers or VerifyBuffers(B, gamma, V, dev, with_probs)
+    if (buf.B, buf.gamma, buf.V) != (B, gamma, V):
+        raise ValueError("buffers were made for another shape")
+    lib = load()
+    with torch.cuda.device(dev):
+        rc = lib.dspark_verify(
+            _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(verify_len),
+            _ptr(uniforms), float(temperature), dtype, B, gamma, V, _ptr(target_row_off),
+            _ptr(draft_row_off), _ptr(buf.accepted_len), _ptr(buf.emitted_tokens),
+            _ptr(buf.probs if with_probs else None), _ptr(buf.near_tie_count),
+            _ptr(buf.device_status), _ptr(buf.workspace), buf.workspace.numel(),
+            _stream_handle(stream))
+    if rc != 0:
+        raise DsparkError("dspark_verify", rc)
+    out = {"accepted_len": buf.accepted_len, "emitted_tokens": buf.emitted_tokens,
+           "probs": buf.probs if with_probs else None, "near_tie_count": buf.near_tie_count,
+           "device_status": buf.device_status}
+    if check:
+        torch.cuda.synchronize(dev)
+        st = int(buf.device_status.item())
+        if st != 0:
+            raise DsparkError("dspark_verify (device)", st)
+    return out
+
+
+class ScheduleBuffers:
+    def __init__(self, R: int, gamma: int, device):
+        dev = torch.device(device)
+        self.R, self.gamma = R, gamma
+        self.verify_len = torch.empty(R, dtype=torch.int32, device=dev)
+        self.theta_best = torch.empty(1, dtype=torch.float64, device=dev)
+        self.near_tie_count = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.device_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.workspace = torch.empty(schedule_workspace_bytes(R, gamma), dtype=torch.uint8, device=dev)
+
+
+def dspark_schedule(confidences: torch.Tensor, step_time_ms: torch.Tensor, *,
+                    buffers: Optional[ScheduleBuffers] = None, stream=None,
+                    check: bool = False) -> dict:
+    """Hardware-aware prefix scheduler through libdspark (see include/dspark.h).
+    Returns verify_len [R] int32, theta_best [1] float64, near_tie_count [1],
+    device_status [1] (device tensors)."""
+    dev = confidences.device
+    _require_cuda("confidences", confidences, torch.float32)
+    _require_cuda("step_time_ms", step_time_ms, torch.float64, dev)
+    R, gamma = confidences.shape
+    buf = buffers or ScheduleBuffers(R, gamma, dev)
+    lib = load()
+    with torch.cuda.device(dev):
+        rc = lib.dspark_schedule(_ptr(confidences), _ptr(step_time_ms), step_time_ms.numel(), R,
+                                 gamma, _ptr(buf.verify_len), _ptr(buf.theta_best),
+                                 _ptr(buf.near_tie_count), _ptr(buf.device_status),
+                                 _ptr(buf.workspace), buf.workspace.numel(), _stream_handle(stream))
+    if rc != 0:
+        raise DsparkError("dspark_schedule", rc)
+    out = {"verify_len": buf.verify_len, "theta_best": buf.theta_best,
+           "near_tie_count": buf.near_tie_count, "device_status": buf.device_status}
+    if check:
+        torch.cuda.synchronize(dev)
+        st = int(buf.device_status.item())
+        if st != 0:
+            raise DsparkError("dspark_schedule (device)", st)
+    return out

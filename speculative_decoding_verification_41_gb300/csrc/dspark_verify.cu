@@ -1,0 +1,983 @@
+// dspark_verify.cu -- batched speculative verification on GB300 (sm_103a).
+//
+// Method: "DSpark: Confidence-Scheduled Speculative Decoding with
+// Semi-Autoregressive Generation", section 2.1 (ratio test min(1, p_t/p_d) at
+// every draft position, scanned left to right, the first rejection ends the
+// block), section 1 (one bonus token), Appendix 8 (a fresh token from p_t when
+// nothing is admitted). The residual max(0, p_t - p_d) after a rejection is the
+// standard rule of the speculative sampling papers cited there as [1], [2].
+//
+// Pipeline (four launches on the caller's stream, no host synchronisation):
+//   k_plan      one CTA: validates verify lengths and row offsets, lays out the
+//               rows to read (l_r + 1 target rows and l_r draft rows per
+//               request) and resets counters.
+//   k_rowstats  the streaming pass, HBM-bound. Persistent grid of 16 warps per
+//               SM; every warp is an independent streamer with its own ring of
+//               shared-memory stages fed by 4 KB 1-D bulk copies (TMA). A work
+//               unit is 16 KB of one row. Each lane keeps an integer exponent
+//               reference K (about ceil(max z * c), c = log2(e)/T, raised only
+//               when its data outgrow it, by exact power-of-two rescaling) and
+//               accumulates 2^(z*c - K) -- two FMAs and one ex2 per logit -- as
+//               pairwise sums with Kahan compensation across chunks. Lanes merge
+//               by exact powers of two and a TwoSum reduction; the unit's
+//               statistics (sum as a float pair, K) go to the workspace. No
+//               double-precision instruction runs per logit: GB300's FP64 rate
+//               is a small fraction of its FP32 rate.
+//   k_verify    one warp per request: merges the unit statistics of its rows
+//               (compensated float), evaluates the ratio p_t^k(x_k)/p_d^k(x_k)
+//               in float and redoes it in double only when the uniform lies
+//               within 2e-6 of it, finds the first rejection with a warp ballot
+//               and writes accepted lengths, tokens and probabilities.
+//   k_resample  per (request, 8 segments of 2048 tokens): sums of the residual
+//               (or target) weights per segment; the last CTA of each request
+//               scans the segment sums, re-reads the one segment holding the
+//               cut and scans it to pick the token.
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "dspark_common.cuh"
+
+namespace dspark {
+
+constexpr int kChunkBytes = 4096;               // one bulk copy
+constexpr int kUnitBytes = DSPARK_TILE_BYTES;   // one work unit (one row statistic)
+constexpr int kSeg = DSPARK_RESAMPLE_SEG;
+static_assert(kUnitBytes % kChunkBytes == 0, "unit = whole chunks");
+
+struct TileStat {  // statistics of one (row, unit): sum_v 2^(z_v*c - K) = s_hi + s_lo
+  float s_hi;
+  float s_lo;
+  int32_t K;       // INT_MIN when the unit holds only masked (-inf) logits
+  int32_t bad;     // non-zero if a non-finite maximum was met
+};
+static_assert(sizeof(TileStat) == 16, "TileStat layout");
+
+struct ResampleDesc {
+  int64_t t_row;  // global row of the target distribution sampled from
+  int64_t d_row;  // global draft row (residual mode)
+  int32_t K_t;    // exponent reference of the target row
+  float D_hi;     // residual: log2(p_t/p_d)(v) = (z_t - z_d)*c - D, D = D_hi + D_lo
+  float D_lo;
+  float u;        // resample uniform
+  int32_t mode;   // 0 nothing to do, 1 residual, 2 target distribution
+  int32_t m;      // accepted count: position of the sampled token
+  int32_t pad[6];
+};
+static_assert(sizeof(ResampleDesc) == 64, "ResampleDesc layout");
+
+enum { kModeNone = 0, kModeResidual = 1, kModeTarget = 2 };
+
+struct WsHeader {
+  int32_t total_rows;
+  uint32_t ties_scratch;  // near-tie counter used when the caller passes none
+  int32_t pad[62];
+};
+
+struct VerifyWs {
+  WsHeader* hdr;
+  int32_t* req_row_start;  // [B+1]: first row-list entry of each request
+  int64_t* row_list;       // [rows]: (global row << 1) | is_draft
+  TileStat* tiles;         // [rows * n_units]
+  ResampleDesc* desc;      // [B]
+  double* seg_sum;         // [B * n_seg]
+  uint32_t* tickets;       // [B]
+};
+
+struct ExpParams {
+  double c_d;  // log2(e) / T
+  float c_hi;  // largest float <= c_d
+  float c_lo;  // c_d - c_hi (> 0)
+};
+
+// ---------------------------------------------------------------------------
+// compensated float helpers
+// ---------------------------------------------------------------------------
+// (hi, lo) <- (hi, lo) + (bh, bl), error-free transformation of the high parts
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float bh, float bl) {
+  const float s = hi + bh;
+  const float bp = s - hi;
+  const float err = (hi - (s - bp)) + (bh - bp);
+  hi = s;
+  lo = lo + bl + err;
+}
+
+__device__ __forceinline__ void warp_two_sum(float& hi, float& lo) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xFFFFFFFFu, hi, o);
+    const float ol = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+    two_sum_acc(hi, lo, oh, ol);
+  }
+}
+
+// x * 2^d for d <= 0 (exact while the result stays normal)
+__device__ __forceinline__ float scale_pow2(float x, int d) { return d < -200 ? 0.f : ldexpf(x, d); }
+
+// 2^(z*c - K), with z*c formed from c_hi + c_lo so that the rounding of c does
+// not bias the sum; -inf logits give 0.
+__device__ __forceinline__ float exp_term(float z, float nK, const ExpParams& ep) {
+  return ex2_approx(fmaf(z, ep.c_lo, fmaf(z, ep.c_hi, nK)));
+}
+
+// ---------------------------------------------------------------------------
+// k_plan
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verify_len,
+                                               const int64_t* __restrict__ toff,
+                                               const int64_t* __restrict__ doff, int B,
+                                               int gamma, VerifyWs ws, uint32_t* ties,
+                                               int32_t* status) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    *status = DSPARK_OK;
+    *ties = 0;
+    carry = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < B; base += 1024) {
+    const int r = base + tid;
+    int cnt = 0;
+    if (r < B) {
+      const int ell = verify_len[r];
+      bool ok = ell >= 0 && ell <= gamma;
+      if (ok && toff) {
+        // rows of a valid request stay inside [0, toff[B]) and [0, doff[B]), the row
+        // counts of the buffers, whatever the offsets of other requests hold
+        const long long t0 = toff[r], t1 = toff[r + 1], d0 = doff[r], d1 = doff[r + 1];
+        ok = t0 >= 0 && d0 >= 0 && t1 - t0 >= ell + 1 && d1 - d0 >= ell && t1 <= toff[B] &&
+             d1 <= doff[B];
+      }
+      if (ok)
+        cnt = 2 * ell + 1;
+      else
+        set_status(status, DSPARK_ERR_BAD_DATA);
+      ws.tickets[r] = 0;
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_tot[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, w, o);
+        if (lane >= o) w += v;
+      }
+      warp_tot[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = carry + (warp ? warp_tot[warp - 1] : 0) + incl - cnt;
+    if (r < B) ws.req_row_start[r] = before;
+    __syncthreads();
+    if (tid == 0) carry += warp_tot[31];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    ws.req_row_start[B] = carry;
+    ws.hdr->total_rows = carry;
+  }
+  __syncthreads();
+  for (int r = tid; r < B; r += 1024) {
+    const int start = ws.req_row_start[r], end = ws.req_row_start[r + 1];
+    if (end == start) continue;  // invalid request: nothing to read
+    const int ell = (end - start - 1) / 2;
+    const long long tb = toff ? toff[r] : (long long)r * (gamma + 1);
+    const long long db = doff ? doff[r] : (long long)r * gamma;
+    for (int i = 0; i <= ell; ++i) ws.row_list[start + i] = (tb + i) << 1;
+    for (int i = 0; i < ell; ++i) ws.row_list[start + ell + 1 + i] = ((db + i) << 1) | 1;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// k_rowstats: unit statistics
+// ---------------------------------------------------------------------------
+// Per-lane running state of one unit.
+struct LaneAcc {
+  int32_t K = INT_MIN;  // exponent reference (INT_MIN: nothing seen yet)
+  float s = 0.f;        // Kahan sum of 2^(z*c - K)
+  float comp = 0.f;     // Kahan compensation (value = s - comp)
+  bool bad = false;
+};
+
+// Raise the lane's reference if a chunk maximum outgrows it by more than 2^64
+// (first chunk: set it). Returns -K as float for the FMA chain.
+__device__ __forceinline__ float lane_reference(LaneAcc& a, float lane_max, const ExpParams& ep) {
+  if (lane_max > -INFINITY) {
+    const float mc = lane_max * ep.c_hi;
+    if (!(fabsf(mc) < 1.0e9f)) {  // +inf / NaN / absurd logits
+      a.bad = true;
+    } else if (a.K == INT_MIN || mc > static_cast<float>(a.K) + 64.f) {
+      const int Kn = static_cast<int>(ceilf(mc));
+      if (a.K != INT_MIN) {
+        a.s = scale_pow2(a.s, a.K - Kn);
+        a.comp = scale_pow2(a.comp, a.K - Kn);
+      }
+      a.K = Kn;
+    }
+  }
+  return a.K == INT_MIN ? 0.f : -static_cast<float>(a.K);
+}
+
+__device__ __forceinline__ void kahan_add(LaneAcc& a, float x) {
+  const float y = x - a.comp;
+  const float t = a.s + y;
+  a.comp = (t - a.s) - y;
+  a.s = t;
+}
+
+// One 4 KB chunk held in registers (VPL 16-byte vectors per lane).
+template <typename Tin, int VPL>
+__device__ __forceinline__ void chunk_accumulate(const uint4 (&v)[VPL], LaneAcc& a,
+                                                 const ExpParams& ep) {
+  float lane_max;
+  if constexpr (sizeof(Tin) == 2) {
+    __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&v[0].x);
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v[j]);
+      m2 = __hmax2(m2, __hmax2(__hmax2(p[0], p[1]), __hmax2(p[2], p[3])));
+    }
+    lane_max = fmaxf(__low2float(m2), __high2float(m2));
+  } else {
+    lane_max = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+      lane_max = fmaxf(lane_max, fmaxf(fmaxf(__uint_as_float(v[j].x), __uint_as_float(v[j].y)),
+                                       fmaxf(__uint_as_float(v[j].z), __uint_as_float(v[j].w))));
+  }
+  if (!(lane_max > -INFINITY)) {
+    if (lane_max != lane_max) a.bad = true;  // NaN
+    return;
+  }
+  const float nK = lane_reference(a, lane_max, ep);
+  float part[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    if constexpr (sizeof(Tin) == 2) {
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      float e[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        e[2 * q] = exp_term(bf16_lo(w[q]), nK, ep);
+        e[2 * q + 1] = exp_term(bf16_hi(w[q]), nK, ep);
+      }
+      part[j] = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+    } else {
+      const float e0 = exp_term(__uint_as_float(v[j].x), nK, ep);
+      const float e1 = exp_term(__uint_as_float(v[j].y), nK, ep);
+      const float e2 = exp_term(__uint_as_float(v[j].z), nK, ep);
+      const float e3 = exp_term(__uint_as_float(v[j].w), nK, ep);
+      part[j] = (e0 + e1) + (e2 + e3);
+    }
+  }
+#pragma unroll
+  for (int w = 1; w < VPL; w <<= 1)
+#pragma unroll
+    for (int j = 0; j + w < VPL; j += 2 * w) part[j] += part[j + w];
+  kahan_add(a, part[0]);
+}
+
+// End of a unit: merge the lanes (exact power-of-two alignment, TwoSum) and
+// write the statistics.
+__device__ __forceinline__ void unit_finish(const LaneAcc& a, TileStat* out, int lane,
+                                            int32_t* status) {
+  const int Kw = __reduce_max_sync(0xFFFFFFFFu, a.K);
+  const bool bad = __any_sync(0xFFFFFFFFu, a.bad);
+  float hi = 0.f, lo = 0.f;
+  if (a.K != INT_MIN) {
+    hi = scale_pow2(a.s, a.K - Kw);
+    lo = -scale_pow2(a.comp, a.K - Kw);
+  }
+  warp_two_sum(hi, lo);
+  if (lane == 0) {
+    TileStat ts;
+    const float s = hi + lo;  // renormalise the pair
+    ts.s_hi = s;
+    ts.s_lo = lo - (s - hi);
+    ts.K = Kw;
+    ts.bad = bad ? 1 : 0;
+    if (bad) set_status(status, DSPARK_ERR_BAD_DATA);
+    *out = ts;
+  }
+}
+
+// Streaming pass through the TMA engine. Row byte length and both buffers
+// must be 16-byte aligned. Shared memory: W warps x STAGES x 4 KB + barriers.
+template <typename Tin, int W, int STAGES>
+__global__ void __launch_bounds__(W * 32, 1)
+    k_rowstats_tma(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int V, int n_units,
+                   VerifyWs ws, ExpParams ep, int32_t* status) {
+  constexpr int VPL = kChunkBytes / 16 / 32;  // 16-byte vectors per lane per chunk
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* buf = smem + static_cast<size_t>(warp) * STAGES * kChunkBytes;
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(W) * STAGES * kChunkBytes) +
+      warp * STAGES;
+  if (lane == 0) {
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  const long long U = static_cast<long long>(ws.hdr->total_rows) * n_units;
+  const long long gw = static_cast<long long>(blockIdx.x) * W + warp;
+  const long long GW = static_cast<long long>(gridDim.x) * W;
+  const long long row_bytes = static_cast<long long>(V) * sizeof(Tin);
+
+  auto unit_bytes = [&](long long u) -> int {
+    const long long part = u % n_units;
+    const long long left = row_bytes - part * kUnitBytes;
+    return static_cast<int>(left < kUnitBytes ? left : kUnitBytes);
+  };
+
+  // producer cursor (lane 0): next chunk to copy
+  long long pu = gw;
+  int pc = 0;
+  const char* pbase = nullptr;
+  auto issue_next = [&](int s) {  // lane 0 only; pu < U
+    const int ub = unit_bytes(pu);
+    if (pc == 0) {
+      const long long row = pu / n_units;
+      const long long e = ws.row_list[row];
+      pbase = reinterpret_cast<const char*>((e & 1) ? dl : tl) + (e >> 1) * row_bytes +
+              (pu - row * n_units) * static_cast<long long>(kUnitBytes);
+    }
+    const int left = ub - pc * kChunkBytes;
+    const uint32_t bytes = static_cast<uint32_t>(left < kChunkBytes ? left : kChunkBytes);
+    mbar_arrive_expect_tx(&bars[s], bytes);
+    bulk_g2s(buf + s * kChunkBytes, pbase + static_cast<long long>(pc) * kChunkBytes, bytes,
+             &bars[s]);
+    if ((++pc) * kChunkBytes >= ub) {
+      pc = 0;
+      pu += GW;
+    }
+  };
+  if (lane == 0)
+    for (int s = 0; s < STAGES && pu < U; ++s) issue_next(s);
+
+  int stage = 0;
+  uint32_t phase = 0;
+  uint4 neg_inf;
+  neg_inf.x = neg_inf.y = neg_inf.z = neg_inf.w = (sizeof(Tin) == 2) ? 0xFF80FF80u : 0xFF800000u;
+  for (long long u = gw; u < U; u += GW) {
+    const int ub = unit_bytes(u);
+    const int nc = (ub + kChunkBytes - 1) / kChunkBytes;
+    LaneAcc acc;
+    for (int c = 0; c < nc; ++c) {
+      // every lane waits (each gets the barrier's acquire); the give-up decision is warp-uniform
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[stage], phase))) {
+        if (lane == 0) set_status(status, DSPARK_ERR_TIMEOUT);
+        for (int s = 0; s < STAGES; ++s) (void)mbar_wait(&bars[s], phase ^ (s < stage ? 1u : 0u));
+        return;
+      }
+      const int bytes = min(kChunkBytes, ub - c * kChunkBytes);
+      uint4 v[VPL];
+      const uint4* sp = reinterpret_cast<const uint4*>(buf + stage * kChunkBytes);
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        const int idx = j * 32 + lane;
+        v[j] = (idx * 16 < bytes) ? sp[idx] : neg_inf;
+      }
+      __syncwarp();
+      if (lane == 0 && pu < U) {
+        fence_proxy_async();
+        issue_next(stage);
+      }
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      chunk_accumulate<Tin, VPL>(v, acc, ep);
+    }
+    unit_finish(acc, ws.tiles + u, lane, status);
+  }
+}
+
+// Fallback streaming pass with plain loads, for rows whose byte length or
+// buffers are not 16-byte aligned.
+template <typename Tin>
+__global__ void __launch_bounds__(256) k_rowstats_plain(const Tin* __restrict__ tl,
+                                                        const Tin* __restrict__ dl, int V,
+                                                        int n_units, VerifyWs ws, ExpParams ep,
+                                                        int32_t* status) {
+  constexpr int kUnitElems = kUnitBytes / sizeof(Tin);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long U = static_cast<long long>(ws.hdr->total_rows) * n_units;
+  const long long GW = static_cast<long long>(gridDim.x) * 8;
+  for (long long u = static_cast<long long>(blockIdx.x) * 8 + warp; u < U; u += GW) {
+    const long long row = u / n_units;
+    const int part = static_cast<int>(u - row * n_units);
+    const long long e = ws.row_list[row];
+    const Tin* src = ((e & 1) ? dl : tl) + (e >> 1) * static_cast<long long>(V) +
+                     static_cast<long long>(part) * kUnitElems;
+    const int n = min(kUnitElems, V - part * kUnitElems);
+    float mx = -INFINITY;
+    for (int i = lane; i < n; i += 32) mx = fmaxf(mx, to_float<Tin>(src[i]));
+    LaneAcc acc;
+    const float nK = lane_reference(acc, mx, ep);
+    if (mx != mx) acc.bad = true;
+    if (acc.K != INT_MIN) {
+      for (int i = lane; i < n; i += 32) kahan_add(acc, exp_term(to_float<Tin>(src[i]), nK, ep));
+    }
+    unit_finish(acc, ws.tiles + u, lane, status);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// k_verify: ratio tests and the first-reject scan
+// ---------------------------------------------------------------------------
+struct RowStat {
+  float S_hi, S_lo;  // sum_v 2^(z_v*c - K)
+  int32_t K;
+  bool ok;
+};
+
+__device__ RowStat merge_row(const TileStat* __restrict__ t, int n_units) {
+  RowStat r;
+  r.K = INT_MIN;
+  r.ok = true;
+  for (int i = 0; i < n_units; ++i) {
+    const TileStat ts = t[i];
+    if (ts.bad) r.ok = false;
+    if (ts.K != INT_MIN && ts.K > r.K) r.K = ts.K;
+  }
+  float hi = 0.f, lo = 0.f;
+  for (int i = 0; i < n_units; ++i) {
+    const TileStat ts = t[i];
+    if (ts.K == INT_MIN) continue;
+    const int d = ts.K - r.K;
+    two_sum_acc(hi, lo, scale_pow2(ts.s_hi, d), scale_pow2(ts.s_lo, d));
+  }
+  const float s = hi + lo;
+  r.S_hi = s;
+  r.S_lo = lo - (s - hi);
+  r.ok = r.ok && r.K != INT_MIN && s > 0.f && isfinite(s);
+  return r;
+}
+
+// 2^a for a double exponent: split into an integer and a fraction in
+// [-0.5, 0.5] so that the float exponential only sees a small argument
+// (relative error ~1 ulp whatever the size of a). A few double operations per
+// call; used per tested position, never per logit.
+__device__ __forceinline__ float exp2_split(double a) {
+  if (!(a > -1.0e4)) return 0.f;
+  const double n = rint(a);
+  return ldexpf(exp2f(static_cast<float>(a - n)), static_cast<int>(fmin(n, 1.0e4)));
+}
+
+// log2(p(x)) + log2(S) + K = z*c, so p(x) = 2^(z*c - K) / S.
+__device__ __forceinline__ float prob_f32(float z, const RowStat& s, const ExpParams& ep) {
+  return exp2_split(static_cast<double>(z) * ep.c_d - static_cast<double>(s.K)) /
+         (s.S_hi + s.S_lo);
+}
+
+__device__ __forceinline__ double prob_f64(float z, const RowStat& s, const ExpParams& ep) {
+  const double a = static_cast<double>(z) * ep.c_d - static_cast<double>(s.K);
+  return exp2(a) / (static_cast<double>(s.S_hi) + static_cast<double>(s.S_lo));
+}
+
+template <typename Tin>
+__global__ void __launch_bounds__(64) k_verify(
+    const Tin* __restrict__ tl, const Tin* __restrict__ dl, const int32_t* __restrict__ tokens,
+    const float* __restrict__ uniforms, int B, int gamma, int V, int n_units, ExpParams ep,
+    VerifyWs ws, int32_t* __restrict__ accepted_len, int32_t* __restrict__ emitted,
+    float* __restrict__ probs_out, uint32_t* ties, int32_t* status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 2 + warp;
+  if (r >= B) return;
+  const int start = ws.req_row_start[r], end = ws.req_row_start[r + 1];
+  int32_t* em = emitted + static_cast<long long>(r) * (gamma + 1);
+  float* pr = probs_out ? probs_out + static_cast<long long>(r) * gamma * 2 : nullptr;
+  if (end == start) {  // invalid request (reported by k_plan): defined, in-bounds outputs
+    for (int k = lane; k <= gamma; k += 32) em[k] = -1;
+    if (pr)
+      for (int k = lane; k < gamma; k += 32) pr[2 * k] = pr[2 * k + 1] = -1.f;
+    if (lane == 0) {
+      accepted_len[r] = 0;
+      ws.desc[r].mode = kModeNone;
+    }
+    return;
+  }
+  const int ell = (end - start - 1) / 2;
+  const int k = lane + 1;  // the position this lane tests
+  const bool has = k <= ell;
+  float pt = 0.f, pd = 1.f;
+  bool accept = false, tie = false;
+  int32_t x = 0;
+  RowStat st{}, sd{};
+  if (has) {
+    st = merge_row(ws.tiles + static_cast<long long>(start + k - 1) * n_units, n_units);
+    sd = merge_row(ws.tiles + static_cast<long long>(start + ell + k) * n_units, n_units);
+    x = tokens[static_cast<long long>(r) * gamma + k - 1];
+    const float u = uniforms[static_cast<long long>(r) * (gamma + 1) + k - 1];
+    if (x < 0 || x >= V || !(u >= 0.f && u < 1.f) || !st.ok || !sd.ok) {
+      set_status(status, DSPARK_ERR_BAD_DATA);
+      x = min(max(x, 0), V - 1);
+    }
+    const long long trow = ws.row_list[start + k - 1] >> 1;
+    const long long drow = ws.row_list[start + ell + k] >> 1;
+    const float zt = to_float<Tin>(tl[trow * V + x]);
+    const float zd = to_float<Tin>(dl[drow * V + x]);
+    pt = prob_f32(zt, st, ep);
+    pd = prob_f32(zd, sd, ep);
+    // ratio = 2^((z_t - z_d)*c - (K_t - K_d)) * S_d / S_t (relative error a few 1e-7)
+    const double a = (static_cast<double>(zt) - static_cast<double>(zd)) * ep.c_d -
+                     static_cast<double>(st.K - sd.K);
+    const float ratio32 = exp2_split(a) * ((sd.S_hi + sd.S_lo) / (st.S_hi + st.S_lo));
+    if (fabsf(u - ratio32) > 2e-6f && isfinite(ratio32)) {
+      accept = u < ratio32;
+    } else {  // close call: decide and flag in double precision
+      const double pt64 = prob_f64(zt, st, ep), pd64 = prob_f64(zd, sd, ep);
+      const double ratio = pd64 > 0.0 ? pt64 / pd64 : INFINITY;
+      accept = static_cast<double>(u) < ratio;
+      tie = fabs(static_cast<double>(u) - ratio) < DSPARK_TIE_EPS || !(pd64 > 0.0);
+    }
+  }
+  const unsigned rej = __ballot_sync(0xFFFFFFFFu, has && !accept);
+  const int m = rej ? __ffs(rej) - 1 : ell;
+  const unsigned n_ties = __popc(__ballot_sync(0xFFFFFFFFu, tie && k <= m + 1));
+  if (lane == 0 && n_ties) atomicAdd(ties, n_ties);
+
+  if (pr && lane < gamma) {
+    pr[2 * lane] = has ? pt : -1.f;
+    pr[2 * lane + 1] = has ? pd : -1.f;
+  }
+  if (lane < m)
+    em[lane] = x;
+  else if (lane > m && lane <= gamma)
+    em[lane] = -1;
+  if (lane == 0 && gamma == 32 && m < 32) em[32] = -1;
+
+  // descriptor of the token to sample after the block
+  const int src = m < ell ? m : 0;
+  const float St_hi = __shfl_sync(0xFFFFFFFFu, st.S_hi, src);
+  const float St_lo = __shfl_sync(0xFFFFFFFFu, st.S_lo, src);
+  const float Sd_hi = __shfl_sync(0xFFFFFFFFu, sd.S_hi, src);
+  const float Sd_lo = __shfl_sync(0xFFFFFFFFu, sd.S_lo, src);
+  const int Kt = __shfl_sync(0xFFFFFFFFu, st.K, src);
+  const int Kd = __shfl_sync(0xFFFFFFFFu, sd.K, src);
+  if (lane == 0) {
+    accepted_len[r] = m;
+    ResampleDesc d;
+    d.u = uniforms[static_cast<long long>(r) * (gamma + 1) + gamma];
+    if (!(d.u >= 0.f && d.u < 1.f)) {
+      set_status(status, DSPARK_ERR_BAD_DATA);
+      d.u = 0.f;
+    }
+    d.m = m;
+    for (int i = 0; i < 6; ++i) d.pad[i] = 0;
+    if (m < ell) {
+      d.mode = kModeResidual;
+      d.t_row = ws.row_list[start + m] >> 1;
+      d.d_row = ws.row_list[start + ell + 1 + m] >> 1;
+      d.K_t = Kt;
+      // one lane, a handful of double operations per request
+      const double D = static_cast<double>(Kt - Kd) +
+                       log2((static_cast<double>(St_hi) + St_lo) /
+                            (static_cast<double>(Sd_hi) + Sd_lo));
+      d.D_hi = static_cast<float>(D);
+      d.D_lo = static_cast<float>(D - static_cast<double>(d.D_hi));
+    } else {
+      const RowStat sb = merge_row(ws.tiles + static_cast<long long>(start + ell) * n_units,
+                                   n_units);
+      if (!sb.ok) set_status(status, DSPARK_ERR_BAD_DATA);
+      d.mode = kModeTarget;
+      d.t_row = ws.row_list[start + ell] >> 1;
+      d.d_row = 0;
+      d.K_t = sb.K == INT_MIN ? 0 : sb.K;
+      d.D_hi = d.D_lo = 0.f;
+    }
+    ws.desc[r] = d;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// k_resample: inverse-CDF draw from the residual or the target distribution
+// ---------------------------------------------------------------------------
+// Weight of token v, up to a factor common to the whole row:
+//   target mode:   e_t(v) = 2^(z_t*c - K_t)                   (proportional to p_t)
+//   residual mode: e_t(v) * (1 - p_d/p_t)^+                   (proportional to max(0, p_t - p_d))
+// with p_d/p_t = 2^(-d2), d2 = (z_t - z_d)*c - D. Where a token carries much
+// mass and p_d is close to p_t, the factor is -expm1(-d2 ln 2) so that it keeps
+// full relative precision; elsewhere 1 - 2^(-d2) is accurate enough.
+__device__ __forceinline__ float resample_weight(float zt, float zd, int mode, float nK,
+                                                 float D_hi, float D_lo, const ExpParams& ep) {
+  const float e = exp_term(zt, nK, ep);
+  if (mode != kModeResidual) return e;
+  const float dz = zt - zd;
+  const float d2 = fmaf(dz, ep.c_hi, -D_hi) + fmaf(dz, ep.c_lo, -D_lo);
+  if (!(d2 > 0.f)) return 0.f;
+  const float f = (d2 < 4.f && e > 0.00390625f) ? -expm1f(-d2 * 0.6931471805599453f)
+                                                : 1.f - ex2_approx(-d2);
+  return e * f;
+}
+
+template <typename Tin, bool VEC>
+__device__ void segment_sum(const Tin* __restrict__ zt, const Tin* __restrict__ zd, int a, int b,
+                            int mode, float nK, float D_hi, float D_lo, const ExpParams& ep,
+                            int lane, float& out_hi, float& out_lo) {
+  LaneAcc acc;
+  if constexpr (VEC) {
+    constexpr int E = 16 / sizeof(Tin);
+    const uint4* vt = reinterpret_cast<const uint4*>(zt);
+    const uint4* vd = reinterpret_cast<const uint4*>(zd);
+    for (int vi = a / E + lane; vi < b / E; vi += 32) {
+      const uint4 qt = __ldg(vt + vi);
+      uint4 qd = qt;
+      if (mode == kModeResidual) qd = __ldg(vd + vi);
+      const Tin* et = reinterpret_cast<const Tin*>(&qt);
+      const Tin* ed = reinterpret_cast<const Tin*>(&qd);
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < E; ++i)
+        s += resample_weight(to_float<Tin>(et[i]), to_float<Tin>(ed[i]), mode, nK, D_hi, D_lo, ep);
+      kahan_add(acc, s);
+    }
+  } else {
+    for (int i = a + lane; i < b; i += 32) {
+      const float z1 = to_float<Tin>(zt[i]);
+      const float z2 = mode == kModeResidual ? to_float<Tin>(zd[i]) : z1;
+      kahan_add(acc, resample_weight(z1, z2, mode, nK, D_hi, D_lo, ep));
+    }
+  }
+  float hi = acc.s, lo = -acc.comp;
+  warp_two_sum(hi, lo);
+  out_hi = hi;
+  out_lo = lo;
+}
+
+template <typename Tin, bool VEC>
+__global__ void __launch_bounds__(256) k_resample(const Tin* __restrict__ tl,
+                                                  const Tin* __restrict__ dl, int V, int n_seg,
+                                                  int gamma, ExpParams ep, VerifyWs ws,
+                                                  int32_t* __restrict__ emitted, uint32_t* ties,
+                                                  int32_t* status) {
+  const int r = blockIdx.y;
+  const ResampleDesc d = ws.desc[r];
+  if (d.mode == kModeNone) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const Tin* zt = tl + d.t_row * static_cast<long long>(V);
+  const Tin* zd = d.mode == kModeResidual ? dl + d.d_row * static_cast<long long>(V) : zt;
+  const float nK = -static_cast<float>(d.K_t);
+  double* seg = ws.seg_sum + static_cast<long long>(r) * n_seg;
+  {
+    const int s = blockIdx.x * 8 + warp;
+    if (s < n_seg) {
+      float hi, lo;
+      segment_sum<Tin, VEC>(zt, zd, s * kSeg, min(V, (s + 1) * kSeg), d.mode, nK, d.D_hi, d.D_lo,
+                            ep, lane, hi, lo);
+      if (lane == 0) seg[s] = static_cast<double>(hi) + static_cast<double>(lo);
+    }
+  }
+  __shared__ int is_last;
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    is_last = atomicAdd(&ws.tickets[r], 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  // --- the last CTA of request r: locate the cut ------------------------------
+  __shared__ double sh_P, sh_Z;
+  __shared__ int sh_j;
+  __shared__ double warp_tot[8];
+  __shared__ unsigned long long sh_pick;  // (index << 1) | near-tie flag, min over threads
+  __shared__ int sh_last_pos;
+  int mode = d.mode;
+  uint32_t flagged = 0;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    if (warp == 0) {
+      // Z = running sum of the segment sums, 32 at a time (double)
+      double run = 0.0;
+      for (int c = 0; c < n_seg; c += 32) {
+        double v = (c + lane < n_seg) ? seg[c + lane] : 0.0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double w = __shfl_up_sync(0xFFFFFFFFu, v, o);
+          if (lane >= o) v += w;
+        }
+        run += __shfl_sync(0xFFFFFFFFu, v, 31);
+      }
+      const double Z = run;
+      const double U = static_cast<double>(d.u) * Z;
+      int j = -1;
+      double P = 0.0;
+      run = 0.0;
+      for (int c = 0; c < n_seg && j < 0; c += 32) {
+        double v = (c + lane < n_seg) ? seg[c + lane] : 0.0;
+        const double own = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const double w = __shfl_up_sync(0xFFFFFFFFu, v, o);
+          if (lane >= o) v += w;
+        }
+        const double incl = run + v;
+        const double prev_incl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+        const double excl = lane == 0 ? run : prev_incl;  // running sum before this segment
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, c + lane < n_seg && own > 0.0 && incl > U);
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          j = c + l;
+          P = __shfl_sync(0xFFFFFFFFu, excl, l);
+        }
+        run += __shfl_sync(0xFFFFFFFFu, v, 31);
+      }
+      if (lane == 0) {
+        sh_Z = Z;
+        sh_P = P;
+        sh_j = j;
+      }
+    }
+    __syncthreads();
+    if (sh_Z > 0.0 || attempt == 1) break;
+    // zero residual mass (only in floating point): sample the target row instead
+    mode = kModeTarget;
+    flagged = 1;
+    for (int s = warp; s < n_seg; s += 8) {
+      float hi, lo;
+      segment_sum<Tin, VEC>(zt, zt, s * kSeg, min(V, (s + 1) * kSeg), kModeTarget, nK, 0.f, 0.f,
+                            ep, lane, hi, lo);
+      if (lane == 0) seg[s] = static_cast<double>(hi) + static_cast<double>(lo);
+    }
+    __syncthreads();
+  }
+  const double Z = sh_Z, P = sh_P;
+  const int j = sh_j;
+  if (!(Z > 0.0) || j < 0) {  // no mass at all: non-finite or empty rows
+    if (tid == 0) {
+      set_status(status, DSPARK_ERR_BAD_DATA);
+      emitted[static_cast<long long>(r) * (gamma + 1) + d.m] = 0;
+    }
+    return;
+  }
+  const double U = static_cast<double>(d.u) * Z;
+  // fine scan of segment j: 8 consecutive tokens per thread
+  const int a = j * kSeg, b = min(V, a + kSeg);
+  const int i0 = a + tid * 8;
+  float w[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int i = i0 + q;
+    w[q] = 0.f;
+    if (i < b) {
+      const float z1 = to_float<Tin>(zt[i]);
+      const float z2 = mode == kModeResidual ? to_float<Tin>(zd[i]) : z1;
+      w[q] = resample_weight(z1, z2, mode, nK, d.D_hi, d.D_lo, ep);
+    }
+  }
+  const float mine = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+  double incl = static_cast<double>(mine);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (tid == 0) {
+    sh_pick = ~0ull;
+    sh_last_pos = -1;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  double before = P + (incl - static_cast<double>(mine));
+  for (int q = 0; q < warp; ++q) before += warp_tot[q];
+  int last_pos = -1;
+  for (int q = 0; q < 8; ++q)
+    if (w[q] > 0.f) last_pos = i0 + q;
+  // only the thread whose range can hold the cut walks its tokens in double
+  if (before <= U && before + static_cast<double>(mine) * (1.0 + 1e-6) > U) {
+    double C = before;
+    for (int q = 0; q < 8; ++q) {
+      const double below = C;
+      C += static_cast<double>(w[q]);
+      if (C > U) {
+        const bool near = (U - below) < DSPARK_TIE_EPS * Z || (C - U) < DSPARK_TIE_EPS * Z;
+        atomicMin(&sh_pick, (static_cast<unsigned long long>(i0 + q) << 1) | (near ? 1ull : 0ull));
+        break;
+      }
+    }
+  }
+  if (before <= U && last_pos >= 0) atomicMax(&sh_last_pos, last_pos);
+  __syncthreads();
+  if (tid == 0) {
+    int y;
+    if (sh_pick != ~0ull) {
+      y = static_cast<int>(sh_pick >> 1);
+      flagged |= static_cast<uint32_t>(sh_pick & 1ull);
+    } else {  // rounding left u*Z beyond this segment's running sums
+      y = sh_last_pos >= 0 ? sh_last_pos : a;
+      flagged = 1;
+    }
+    emitted[static_cast<long long>(r) * (gamma + 1) + d.m] = y;
+    if (flagged) atomicAdd(ties, 1u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+constexpr int kStreamWarps = 16;
+constexpr int kStages = 3;
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+};
+std::mutex g_mutex;
+DeviceState g_devices[128];
+
+constexpr size_t tma_smem_bytes() {
+  return static_cast<size_t>(kStreamWarps) * kStages * kChunkBytes +
+         static_cast<size_t>(kStreamWarps) * kStages * sizeof(uint64_t);
+}
+
+int device_setup(int& sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return DSPARK_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& s = g_devices[dev];
+  if (!s.ready) {
+    if (cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    if (cudaFuncSetAttribute(k_rowstats_tma<uint16_t, kStreamWarps, kStages>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(tma_smem_bytes())) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    if (cudaFuncSetAttribute(k_rowstats_tma<float, kStreamWarps, kStages>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(tma_smem_bytes())) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    s.ready = true;
+  }
+  sms = s.sms;
+  return DSPARK_OK;
+}
+
+ExpParams exp_params(float temperature) {
+  ExpParams ep;
+  ep.c_d = 1.4426950408889634 / static_cast<double>(temperature);  // log2(e) / T
+  float hi = static_cast<float>(ep.c_d);
+  if (static_cast<double>(hi) > ep.c_d) hi = std::nextafter(hi, 0.0f);
+  ep.c_hi = hi;
+  ep.c_lo = static_cast<float>(ep.c_d - static_cast<double>(hi));
+  if (!(ep.c_lo > 0.0f)) ep.c_lo = 1e-30f;  // keeps c_lo * (-inf) = -inf
+  return ep;
+}
+
+VerifyWs carve_verify_ws(void* base, int B, int gamma, int V) {
+  char* p = static_cast<char*>(base);
+  VerifyWs ws;
+  ws.hdr = reinterpret_cast<WsHeader*>(p);
+  p += 256;
+  ws.req_row_start = reinterpret_cast<int32_t*>(p);
+  p += DSPARK_ALIGN256((static_cast<size_t>(B) + 1) * 4);
+  ws.row_list = reinterpret_cast<int64_t*>(p);
+  p += DSPARK_ALIGN256(DSPARK_MAX_ROWS(B, gamma) * 8);
+  ws.tiles = reinterpret_cast<TileStat*>(p);
+  p += DSPARK_ALIGN256(DSPARK_MAX_ROWS(B, gamma) * DSPARK_TILES_PER_ROW(V) * 16);
+  ws.desc = reinterpret_cast<ResampleDesc*>(p);
+  p += DSPARK_ALIGN256(static_cast<size_t>(B) * 64);
+  ws.seg_sum = reinterpret_cast<double*>(p);
+  p += DSPARK_ALIGN256(static_cast<size_t>(B) * DSPARK_SEGS_PER_ROW(V) * 8);
+  ws.tickets = reinterpret_cast<uint32_t*>(p);
+  return ws;
+}
+
+template <typename Tin>
+int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int32_t* vlen,
+                  const float* uni, float temperature, int B, int gamma, int V,
+                  const int64_t* toff, const int64_t* doff, int32_t* acc, int32_t* emitted,
+                  float* probs, uint32_t* ties, int32_t* status, void* workspace,
+                  cudaStream_t stream) {
+  int sms = 0;
+  if (int rc = device_setup(sms)) return rc;
+  VerifyWs ws = carve_verify_ws(workspace, B, gamma, V);
+  uint32_t* tie_ctr = ties ? ties : &ws.hdr->ties_scratch;
+  const ExpParams ep = exp_params(temperature);
+  const int unit_elems = kUnitBytes / static_cast<int>(sizeof(Tin));
+  const int n_units = (V + unit_elems - 1) / unit_elems;
+  const int n_seg = (V + kSeg - 1) / kSeg;
+
+  k_plan<<<1, 1024, 0, stream>>>(vlen, toff, doff, B, gamma, ws, tie_ctr, status);
+  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (B == 0) return DSPARK_OK;
+
+  const bool aligned = (static_cast<size_t>(V) * sizeof(Tin)) % 16 == 0 &&
+                       reinterpret_cast<uintptr_t>(tl) % 16 == 0 &&
+                       reinterpret_cast<uintptr_t>(dl) % 16 == 0;
+  const long long max_units = static_cast<long long>(DSPARK_MAX_ROWS(B, gamma)) * n_units;
+  if (aligned) {
+    const long long want = (max_units + kStreamWarps - 1) / kStreamWarps;
+    const int grid = static_cast<int>(want < sms ? want : sms);
+    k_rowstats_tma<Tin, kStreamWarps, kStages>
+        <<<grid, kStreamWarps * 32, tma_smem_bytes(), stream>>>(tl, dl, V, n_units, ws, ep,
+                                                                status);
+  } else {
+    const long long want = (max_units + 7) / 8;
+    const int grid = static_cast<int>(want < 4LL * sms ? want : 4LL * sms);
+    k_rowstats_plain<Tin><<<grid, 256, 0, stream>>>(tl, dl, V, n_units, ws, ep, status);
+  }
+  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+
+  k_verify<Tin><<<(B + 1) / 2, 64, 0, stream>>>(tl, dl, tokens, uni, B, gamma, V, n_units, ep,
+                                                ws, acc, emitted, probs, tie_ctr, status);
+  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+
+  const dim3 rgrid((n_seg + 7) / 8, B);
+  if (aligned)
+    k_resample<Tin, true><<<rgrid, 256, 0, stream>>>(tl, dl, V, n_seg, gamma, ep, ws, emitted,
+                                                     tie_ctr, status);
+  else
+    k_resample<Tin, false><<<rgrid, 256, 0, stream>>>(tl, dl, V, n_seg, gamma, ep, ws, emitted,
+                                                      tie_ctr, status);
+  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+}  // namespace dspark
+
+extern "C" int dspark_verify(const void* target_logits, const void* draft_logits,
+                             const int32_t* draft_tokens, const int32_t* verify_len,
+                             const float* uniforms, float temperature, int32_t dtype, int32_t B,
+                             int32_t gamma, int32_t V, const int64_t* target_row_off,
+                             const int64_t* draft_row_off, int32_t* accepted_len,
+                             int32_t* emitted_tokens, float* probs_out,
+                             uint32_t* near_tie_count, int32_t* device_status, void* workspace,
+                             size_t workspace_bytes, struct CUstream_st* stream) {
+  using namespace dspark;
+  // B indexes a grid dimension of the resample pass; V keeps segment offsets in int
+  if (B < 0 || B > 65535 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || V < 1 || V > (1 << 30))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return DSPARK_ERR_INVALID_ARG;
+  if (dtype != DSPARK_F32 && dtype != DSPARK_BF16) return DSPARK_ERR_INVALID_ARG;
+  if (!device_status) return DSPARK_ERR_INVALID_ARG;
+  if ((target_row_off == nullptr) != (draft_row_off == nullptr)) return DSPARK_ERR_INVALID_ARG;
+  if (B > 0 && (!target_logits || !draft_logits || !draft_tokens || !verify_len || !uniforms ||
+                !accepted_len || !emitted_tokens))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < DSPARK_VERIFY_WS_BYTES(B, gamma, V) ||
+      reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return DSPARK_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == DSPARK_BF16)
+    return launch_verify<uint16_t>(
+        static_cast<const uint16_t*>(target_logits), static_cast<const uint16_t*>(draft_logits),
+        draft_tokens, verify_len, uniforms, temperature, B, gamma, V, target_row_off,
+        draft_row_off, accepted_len, emitted_tokens, probs_out, near_tie_count, device_status,
+        workspace, s);
+  return launch_verify<float>(static_cast<const float*>(target_logits),
+                              static_cast<const float*>(draft_logits), draft_tokens, verify_len,
+                              uniforms, temperature, B, gamma, V, target_row_off, draft_row_off,
+                              accepted_len, emitted_tokens, probs_out, near_tie_count,
+                              device_status, workspace, s);
+}

@@ -1,0 +1,95 @@
+"""The C-ABI boundary, checked on the CPU: the library loads and exports every
+entry point include/dspark.h declares, the workspace macros agree with the
+Python binding's statement of them, and host-side argument checks reject bad
+calls before anything is launched."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from speculative_decoding_verification_41_gb300 import binding
+from speculative_decoding_verification_41_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dspark.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return binding.load()
+
+
+def declared_functions():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"^int\s+(dspark_\w+)\s*\(", txt, flags=re.M)))
+
+
+def test_header_declares_the_two_calls():
+    assert declared_functions() == sorted(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(dspark_\w+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+
+
+def test_header_compiles_as_c_and_macros_match_binding(tmp_path):
+    shapes = [(1, 1, 1), (4, 4, 32), (64, 16, 151936), (256, 16, 129280), (1024, 16, 151936),
+              (7, 32, 1001), (0, 3, 5)]
+    src = ['#include <stdio.h>', '#include "dspark.h"', "int main(void) {"]
+    for B, g, V in shapes:
+        src.append(f'  printf("%zu %zu\\n", DSPARK_VERIFY_WS_BYTES({B}, {g}, {V}), '
+                   f'DSPARK_SCHEDULE_WS_BYTES({max(B, 1)}, {g}));')
+    src.append("  return 0; }")
+    c = tmp_path / "probe.c"
+    c.write_text("\n".join(src))
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", f"-I{os.path.dirname(HEADER)}", str(c),
+                    "-o", str(exe)], check=True)
+    lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    for (B, g, V), line in zip(shapes, lines):
+        v, s = map(int, line.split())
+        assert v == binding.verify_workspace_bytes(B, g, V)
+        assert s == binding.schedule_workspace_bytes(max(B, 1), g)
+
+
+def _verify_call(lib, **kw):
+    args = dict(tl=1, dl=1, tok=1, vlen=1, uni=1, T=1.0, dtype=1, B=4, gamma=4, V=32, toff=None,
+                doff=None, acc=1, em=1, probs=None, ties=None, status=1, ws=256, ws_bytes=1 << 30)
+    args.update(kw)
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.dspark_verify(p(args["tl"]), p(args["dl"]), p(args["tok"]), p(args["vlen"]),
+                             p(args["uni"]), args["T"], args["dtype"], args["B"], args["gamma"],
+                             args["V"], p(args["toff"]), p(args["doff"]), p(args["acc"]),
+                             p(args["em"]), p(args["probs"]), p(args["ties"]), p(args["status"]),
+                             p(args["ws"]), args["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(gamma=0), 1), (dict(gamma=33), 1), (dict(V=0), 1), (dict(B=-1), 1), (dict(B=70000), 1),
+    (dict(T=0.0), 1), (dict(T=float("inf")), 1), (dict(T=float("nan")), 1), (dict(dtype=7), 1),
+    (dict(status=None), 1), (dict(toff=64), 1), (dict(tl=None), 1), (dict(em=None), 1),
+    (dict(ws=None), 3), (dict(ws=128), 3), (dict(ws_bytes=100), 3)])
+def test_verify_rejects_bad_arguments_on_host(lib, bad, code):
+    assert _verify_call(lib, **bad) == code
+
+
+def test_schedule_rejects_bad_arguments_on_host(lib):
+    p = ctypes.c_void_p
+    call = lambda R, g, n, ws=256, wsb=1 << 30, conf=1: lib.dspark_schedule(
+        None if conf is None else p(conf), p(1), n, R, g, p(1), None, None, p(1),
+        None if ws is None else p(ws), wsb, None)
+    assert call(0, 4, 100) == 1
+    assert call(4, 0, 100) == 1
+    assert call(4, 33, 1000) == 1
+    assert call(4, 4, 20) == 1          # profile shorter than R*(gamma+1)+1
+    assert call(4, 4, 21, conf=None) == 1
+    assert call(4, 4, 21, ws=None) == 3
+    assert call(4, 4, 21, wsb=10) == 3
