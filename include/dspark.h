@@ -53,7 +53,8 @@ typedef enum {
   DSPARK_ERR_CUDA = 2,
   DSPARK_ERR_WORKSPACE = 3,
   DSPARK_ERR_TIMEOUT = 4,
-  DSPARK_ERR_BAD_DATA = 5
+  DSPARK_ERR_BAD_DATA = 5,
+  DSPARK_ERR_TOO_LARGE = 6 /* batch needs more scratch than dspark_verify_static has */
 } dspark_status;
 
 typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
@@ -183,6 +184,46 @@ int dspark_schedule(const float* confidences, const double* step_time_ms,
                     uint32_t* near_tie_count, int32_t* device_status,
                     void* workspace, size_t workspace_bytes,
                     struct CUstream_st* stream);
+
+/* Size of the library-owned scratch array behind dspark_verify_static. */
+#define DSPARK_STATIC_WS_BYTES ((size_t)16u << 20)
+
+/*
+ * dspark_verify_static -- dspark_verify for callers that cannot allocate
+ * device memory. (The DSpark paper has no counterpart: this is a deployment
+ * convenience of this library, not part of the method.)
+ *
+ * Some callers cannot call cudaMalloc: plugins that a host framework hands only
+ * their input and output buffers, with no allocator of their own; serving loops
+ * that must not call cudaMalloc because it can synchronise the whole device and
+ * stall other streams; and processes that run under a device-memory budget
+ * reserved up front. This entry point takes the same arguments as
+ * dspark_verify minus the workspace, and computes the same results.
+ *
+ * Scratch: a file-scope device array of DSPARK_STATIC_WS_BYTES (16 MiB) inside
+ * libdspark. Every GPU that loads the library holds it until the process exits.
+ * The first call on each device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before
+ * any stream capture. No call allocates or frees memory.
+ *
+ * Limits and sharing: a batch whose DSPARK_VERIFY_WS_BYTES(B, gamma, V)
+ * exceeds DSPARK_STATIC_WS_BYTES is rejected with DSPARK_ERR_TOO_LARGE before
+ * anything is launched (for example B = 256, gamma = 16, V = 129,280 needs
+ * about 4.5 MB). All calls on a device share the one array, which keeps the
+ * last call's contents; every call resets the counters that must start at zero
+ * itself. Calls whose work overlaps on the GPU (different streams, or host
+ * threads without ordering) race on the array: serialise them.
+ *
+ * Arguments, outputs and error behaviour are those of dspark_verify.
+ */
+int dspark_verify_static(const void* target_logits, const void* draft_logits,
+                         const int32_t* draft_tokens, const int32_t* verify_len,
+                         const float* uniforms, float temperature, int32_t dtype,
+                         int32_t B, int32_t gamma, int32_t V,
+                         const int64_t* target_row_off, const int64_t* draft_row_off,
+                         int32_t* accepted_len, int32_t* emitted_tokens,
+                         float* probs_out, uint32_t* near_tie_count,
+                         int32_t* device_status, struct CUstream_st* stream);
 
 #ifdef __cplusplus
 }

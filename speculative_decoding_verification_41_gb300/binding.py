@@ -22,9 +22,10 @@ HEADER = os.path.join(ROOT, "include", "dspark.h")
 LIB_PATH = os.path.join(PKG, "libdspark.so")
 
 STATUS_NAMES = {0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_CUDA",
-                3: "DSPARK_ERR_WORKSPACE", 4: "DSPARK_ERR_TIMEOUT", 5: "DSPARK_ERR_BAD_DATA"}
+                3: "DSPARK_ERR_WORKSPACE", 4: "DSPARK_ERR_TIMEOUT", 5: "DSPARK_ERR_BAD_DATA",
+                6: "DSPARK_ERR_TOO_LARGE"}
 DSPARK_F32, DSPARK_BF16 = 0, 1
-EXPORTED = ("dspark_verify", "dspark_schedule")
+EXPORTED = ("dspark_verify", "dspark_schedule", "dspark_verify_static")
 
 
 class DsparkError(RuntimeError):
@@ -88,6 +89,9 @@ def load(path: Optional[str] = None):
         lib.dspark_verify.restype = ctypes.c_int
         lib.dspark_verify.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp, vp, vp,
                                       vp, vp, vp, vp, sz, vp]
+        lib.dspark_verify_static.restype = ctypes.c_int
+        lib.dspark_verify_static.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp,
+                                             vp, vp, vp, vp, vp, vp]
         lib.dspark_schedule.restype = ctypes.c_int
         lib.dspark_schedule.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp]
         if path is None:

@@ -981,3 +981,55 @@ extern "C" int dspark_verify(const void* target_logits, const void* draft_logits
                               accepted_len, emitted_tokens, probs_out, near_tie_count,
                               device_status, workspace, s);
 }
+
+// ---------------------------------------------------------------------------
+// dspark_verify_static: the same verification with library-owned scratch, for
+// callers that cannot allocate device memory (no counterpart in the paper).
+// ---------------------------------------------------------------------------
+namespace dspark {
+
+// One array per device that loads the library, kept until the process exits
+// and shared by every call on that device. Its contents need no clearing
+// between calls: k_plan resets the tickets and counters each call relies on.
+static __device__ __align__(256) unsigned char g_static_ws[DSPARK_STATIC_WS_BYTES];
+
+std::mutex g_static_mutex;
+void* g_static_ws_ptr[128];  // device address of g_static_ws, per device
+
+// In host code g_static_ws names a host-side stand-in, not device memory: the
+// device address is looked up once per device, with that device current.
+int static_ws_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return DSPARK_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (g_static_ws_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || p == nullptr)
+      return DSPARK_ERR_CUDA;
+    g_static_ws_ptr[dev] = p;
+  }
+  *out = g_static_ws_ptr[dev];
+  return DSPARK_OK;
+}
+
+}  // namespace dspark
+
+extern "C" int dspark_verify_static(const void* target_logits, const void* draft_logits,
+                                    const int32_t* draft_tokens, const int32_t* verify_len,
+                                    const float* uniforms, float temperature, int32_t dtype,
+                                    int32_t B, int32_t gamma, int32_t V,
+                                    const int64_t* target_row_off, const int64_t* draft_row_off,
+                                    int32_t* accepted_len, int32_t* emitted_tokens,
+                                    float* probs_out, uint32_t* near_tie_count,
+                                    int32_t* device_status, struct CUstream_st* stream) {
+  using namespace dspark;
+  if (B < 0 || B > 65535 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || V < 1 || V > (1 << 30))
+    return DSPARK_ERR_INVALID_ARG;
+  if (DSPARK_VERIFY_WS_BYTES(B, gamma, V) > DSPARK_STATIC_WS_BYTES) return DSPARK_ERR_TOO_LARGE;
+  void* ws = nullptr;
+  if (int rc = static_ws_address(&ws)) return rc;
+  return dspark_verify(target_logits, draft_logits, draft_tokens, verify_len, uniforms,
+                       temperature, dtype, B, gamma, V, target_row_off, draft_row_off,
+                       accepted_len, emitted_tokens, probs_out, near_tie_count, device_status,
+                       ws, DSPARK_STATIC_WS_BYTES, stream);
+}

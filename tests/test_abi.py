@@ -27,7 +27,7 @@ def declared_functions():
     return sorted(set(re.findall(r"^int\s+(dspark_\w+)\s*\(", txt, flags=re.M)))
 
 
-def test_header_declares_the_two_calls():
+def test_header_declares_the_exported_calls():
     assert declared_functions() == sorted(binding.EXPORTED)
 
 
