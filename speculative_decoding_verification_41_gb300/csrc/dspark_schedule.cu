@@ -106,9 +106,16 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
 
   // 1. prefix survival probabilities
   for (int r = tid; r < R; r += kSchedThreads) {
+    // all of the request's loads are issued before the multiply chain
+    float cv[DSPARK_MAX_GAMMA];
+#pragma unroll
+    for (int j = 0; j < DSPARK_MAX_GAMMA; ++j)
+      cv[j] = j < gamma ? conf[static_cast<long long>(r) * gamma + j] : 0.f;
     double prod = 1.0;
-    for (int j = 0; j < gamma; ++j) {
-      float c = conf[static_cast<long long>(r) * gamma + j];
+#pragma unroll
+    for (int j = 0; j < DSPARK_MAX_GAMMA; ++j) {
+      if (j >= gamma) break;
+      float c = cv[j];
       if (!(c >= 0.f && c <= 1.f)) {
         set_status(status, DSPARK_ERR_BAD_DATA);
         c = 0.f;

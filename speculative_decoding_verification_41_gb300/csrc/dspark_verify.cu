@@ -7,7 +7,7 @@
 // nothing is admitted). The residual max(0, p_t - p_d) after a rejection is the
 // standard rule of the speculative sampling papers cited there as [1], [2].
 //
-// Pipeline (four launches on the caller's stream, no host synchronisation):
+// Pipeline (five launches on the caller's stream, no host synchronisation):
 //   k_plan      one CTA: validates verify lengths and row offsets, lays out the
 //               rows to read (l_r + 1 target rows and l_r draft rows per
 //               request) and resets counters.
@@ -28,10 +28,10 @@
 //               in float and redoes it in double only when the uniform lies
 //               within 2e-6 of it, finds the first rejection with a warp ballot
 //               and writes accepted lengths, tokens and probabilities.
-//   k_resample  per (request, 8 segments of 2048 tokens): sums of the residual
-//               (or target) weights per segment; the last CTA of each request
-//               scans the segment sums, re-reads the one segment holding the
-//               cut and scans it to pick the token.
+//   k_resample_sums  grid-stride warps over (request, segment of 2048 tokens):
+//               sums of the residual (or target) weights per segment.
+//   k_resample_pick  one CTA per request: scans the segment sums, re-reads the
+//               one segment holding the cut and scans it to pick the token.
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -616,8 +616,8 @@ __device__ __forceinline__ float resample_weight(float zt, float zd, int mode, f
   const float dz = zt - zd;
   const float d2 = fmaf(dz, ep.c_hi, -D_hi) + fmaf(dz, ep.c_lo, -D_lo);
   if (!(d2 > 0.f)) return 0.f;
-  const float f = (d2 < 4.f && e > 0.00390625f) ? -expm1f(-d2 * 0.6931471805599453f)
-                                                : 1.f - ex2_approx(-d2);
+  float f = 1.f - ex2_approx(-d2);
+  if (d2 < 4.f && e > 0.00390625f) f = -expm1f(-d2 * 0.6931471805599453f);  // rare: heavy token
   return e * f;
 }
 
@@ -627,20 +627,32 @@ __device__ void segment_sum(const Tin* __restrict__ zt, const Tin* __restrict__ 
                             int lane, float& out_hi, float& out_lo) {
   LaneAcc acc;
   if constexpr (VEC) {
+    // NB 16-byte vectors per lane and row are requested before any arithmetic
     constexpr int E = 16 / sizeof(Tin);
+    constexpr int NB = 4;
     const uint4* vt = reinterpret_cast<const uint4*>(zt);
     const uint4* vd = reinterpret_cast<const uint4*>(zd);
-    for (int vi = a / E + lane; vi < b / E; vi += 32) {
-      const uint4 qt = __ldg(vt + vi);
-      uint4 qd = qt;
-      if (mode == kModeResidual) qd = __ldg(vd + vi);
-      const Tin* et = reinterpret_cast<const Tin*>(&qt);
-      const Tin* ed = reinterpret_cast<const Tin*>(&qd);
-      float s = 0.f;
+    const int v_end = b / E;
+    for (int v0 = a / E + lane; v0 < v_end; v0 += 32 * NB) {
+      uint4 qt[NB], qd[NB];
 #pragma unroll
-      for (int i = 0; i < E; ++i)
-        s += resample_weight(to_float<Tin>(et[i]), to_float<Tin>(ed[i]), mode, nK, D_hi, D_lo, ep);
-      kahan_add(acc, s);
+      for (int q = 0; q < NB; ++q) {
+        const int vi = v0 + 32 * q;
+        qt[q] = vi < v_end ? __ldg(vt + vi) : make_uint4(0u, 0u, 0u, 0u);
+        qd[q] = (mode == kModeResidual && vi < v_end) ? __ldg(vd + vi) : qt[q];
+      }
+#pragma unroll
+      for (int q = 0; q < NB; ++q) {
+        if (v0 + 32 * q >= v_end) break;
+        const Tin* et = reinterpret_cast<const Tin*>(&qt[q]);
+        const Tin* ed = reinterpret_cast<const Tin*>(&qd[q]);
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i)
+          s += resample_weight(to_float<Tin>(et[i]), to_float<Tin>(ed[i]), mode, nK, D_hi, D_lo,
+                               ep);
+        kahan_add(acc, s);
+      }
     }
   } else {
     for (int i = a + lane; i < b; i += 32) {
@@ -655,13 +667,38 @@ __device__ void segment_sum(const Tin* __restrict__ zt, const Tin* __restrict__ 
   out_lo = lo;
 }
 
+// Segment sums of every request's resample weights: a grid-stride loop of
+// warps over (request, segment) items.
 template <typename Tin, bool VEC>
-__global__ void __launch_bounds__(256) k_resample(const Tin* __restrict__ tl,
-                                                  const Tin* __restrict__ dl, int V, int n_seg,
-                                                  int gamma, ExpParams ep, VerifyWs ws,
-                                                  int32_t* __restrict__ emitted, uint32_t* ties,
-                                                  int32_t* status) {
-  const int r = blockIdx.y;
+__global__ void __launch_bounds__(256) k_resample_sums(const Tin* __restrict__ tl,
+                                                       const Tin* __restrict__ dl, int V,
+                                                       int n_seg, int B, ExpParams ep,
+                                                       VerifyWs ws) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long items = static_cast<long long>(B) * n_seg;
+  for (long long it = static_cast<long long>(blockIdx.x) * 8 + warp; it < items;
+       it += static_cast<long long>(gridDim.x) * 8) {
+    const int r = static_cast<int>(it / n_seg);
+    const int sgi = static_cast<int>(it - static_cast<long long>(r) * n_seg);
+    const ResampleDesc d = ws.desc[r];
+    if (d.mode == kModeNone) continue;
+    const Tin* zt = tl + d.t_row * static_cast<long long>(V);
+    const Tin* zd = d.mode == kModeResidual ? dl + d.d_row * static_cast<long long>(V) : zt;
+    float hi, lo;
+    segment_sum<Tin, VEC>(zt, zd, sgi * kSeg, min(V, (sgi + 1) * kSeg), d.mode,
+                          -static_cast<float>(d.K_t), d.D_hi, d.D_lo, ep, lane, hi, lo);
+    if (lane == 0) ws.seg_sum[it] = static_cast<double>(hi) + static_cast<double>(lo);
+  }
+}
+
+// One CTA per request: find the segment holding u*Z, then the token inside it.
+template <typename Tin, bool VEC>
+__global__ void __launch_bounds__(256) k_resample_pick(const Tin* __restrict__ tl,
+                                                       const Tin* __restrict__ dl, int V,
+                                                       int n_seg, int gamma, ExpParams ep,
+                                                       VerifyWs ws, int32_t* __restrict__ emitted,
+                                                       uint32_t* ties, int32_t* status) {
+  const int r = blockIdx.x;
   const ResampleDesc d = ws.desc[r];
   if (d.mode == kModeNone) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
@@ -669,26 +706,7 @@ __global__ void __launch_bounds__(256) k_resample(const Tin* __restrict__ tl,
   const Tin* zd = d.mode == kModeResidual ? dl + d.d_row * static_cast<long long>(V) : zt;
   const float nK = -static_cast<float>(d.K_t);
   double* seg = ws.seg_sum + static_cast<long long>(r) * n_seg;
-  {
-    const int s = blockIdx.x * 8 + warp;
-    if (s < n_seg) {
-      float hi, lo;
-      segment_sum<Tin, VEC>(zt, zd, s * kSeg, min(V, (s + 1) * kSeg), d.mode, nK, d.D_hi, d.D_lo,
-                            ep, lane, hi, lo);
-      if (lane == 0) seg[s] = static_cast<double>(hi) + static_cast<double>(lo);
-    }
-  }
-  __shared__ int is_last;
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    is_last = atomicAdd(&ws.tickets[r], 1u) == gridDim.x - 1;
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
 
-  // --- the last CTA of request r: locate the cut ------------------------------
   __shared__ double sh_P, sh_Z;
   __shared__ int sh_j;
   __shared__ double warp_tot[8];
@@ -933,13 +951,20 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
                                                 ws, acc, emitted, probs, tie_ctr, status);
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
 
-  const dim3 rgrid((n_seg + 7) / 8, B);
-  if (aligned)
-    k_resample<Tin, true><<<rgrid, 256, 0, stream>>>(tl, dl, V, n_seg, gamma, ep, ws, emitted,
-                                                     tie_ctr, status);
-  else
-    k_resample<Tin, false><<<rgrid, 256, 0, stream>>>(tl, dl, V, n_seg, gamma, ep, ws, emitted,
+  const long long items = static_cast<long long>(B) * n_seg;
+  const long long want_sums = (items + 7) / 8;
+  const int sums_grid = static_cast<int>(want_sums < 8LL * sms ? want_sums : 8LL * sms);
+  if (aligned) {
+    k_resample_sums<Tin, true><<<sums_grid, 256, 0, stream>>>(tl, dl, V, n_seg, B, ep, ws);
+    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    k_resample_pick<Tin, true><<<B, 256, 0, stream>>>(tl, dl, V, n_seg, gamma, ep, ws, emitted,
                                                       tie_ctr, status);
+  } else {
+    k_resample_sums<Tin, false><<<sums_grid, 256, 0, stream>>>(tl, dl, V, n_seg, B, ep, ws);
+    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+    k_resample_pick<Tin, false><<<B, 256, 0, stream>>>(tl, dl, V, n_seg, gamma, ep, ws, emitted,
+                                                       tie_ctr, status);
+  }
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }
