@@ -360,7 +360,7 @@ def native_arm(args):
         "timing_ms": {"verify_median": v_med, "verify_p10": float(np.percentile(verify_ms, 10)),
                       "verify_p90": float(np.percentile(verify_ms, 90)),
                       "schedule_median": statistics.median(sched_ms)},
-        "gpu_launches": args.steps * 6,  # per step: k_schedule, k_plan, k_rowstats, k_verify, k_resample_sums, k_resample_pick
+        "gpu_launches": args.steps * 5,  # per step: k_sched_rank, k_sched_sweep, k_plan, k_rowstats, k_decide
         "near_ties": int(vbuf.near_tie_count.item()),
         "clocks": clk,
         "e2e": e2e,

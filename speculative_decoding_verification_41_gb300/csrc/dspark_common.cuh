@@ -78,6 +78,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Programmatic dependent launch. Every kernel of the library is launched with
+// programmatic stream serialization, so the next kernel on the stream may be
+// scheduled before this one ends. pdl_wait() blocks until the preceding grid
+// has completed and its memory is visible; each kernel calls it before its
+// first global-memory access, so reads and writes stay ordered exactly as
+// without the attribute. pdl_trigger() then lets the following grid launch
+// early, hiding its launch latency behind this kernel.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // 2^x, hardware approximation (flush-to-zero for results below the normal range).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -117,6 +129,49 @@ __device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
   return v;
 }
 
+// A value carried as an unevaluated sum of two floats (about 48 significant
+// bits): double-like precision on the float pipes.
+struct ff {
+  float hi, lo;
+};
+
+__device__ __forceinline__ ff ff_norm(float s, float e) {
+  const float hi = s + e;
+  return ff{hi, e - (hi - s)};
+}
+
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  const float s = a.hi + b.hi;
+  const float bp = s - a.hi;
+  const float err = (a.hi - (s - bp)) + (b.hi - bp) + a.lo + b.lo;
+  return ff_norm(s, err);
+}
+
+__device__ __forceinline__ ff ff_sub(ff a, ff b) { return ff_add(a, ff{-b.hi, -b.lo}); }
+
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+  const float p = a.hi * b.hi;
+  float e = fmaf(a.hi, b.hi, -p);
+  e = fmaf(a.hi, b.lo, e);
+  e = fmaf(a.lo, b.hi, e);
+  return ff_norm(p, e);
+}
+
+// sign of a - b (-1, 0, 1)
+__device__ __forceinline__ int ff_cmp(ff a, ff b) {
+  const ff d = ff_sub(a, b);
+  const float v = d.hi != 0.f ? d.hi : d.lo;
+  return (v > 0.f) - (v < 0.f);
+}
+
+__device__ __forceinline__ ff shfl_up_ff(ff v, int o) {
+  return ff{__shfl_up_sync(0xFFFFFFFFu, v.hi, o), __shfl_up_sync(0xFFFFFFFFu, v.lo, o)};
+}
+
+__device__ __forceinline__ ff shfl_ff(ff v, int src) {
+  return ff{__shfl_sync(0xFFFFFFFFu, v.hi, src), __shfl_sync(0xFFFFFFFFu, v.lo, src)};
+}
+
 // Kahan-compensated float accumulator.
 struct KahanF {
   float s = 0.f, c = 0.f;
@@ -130,5 +185,22 @@ struct KahanF {
     return static_cast<double>(s) - static_cast<double>(c);
   }
 };
+
+// Launch `kernel` on `stream` with programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace dspark

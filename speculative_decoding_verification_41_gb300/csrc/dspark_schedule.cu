@@ -7,24 +7,28 @@
 // that order with Theta = tau * SPS(B) (SPS = 1/T), stop at the first
 // Theta <= Theta_best.
 //
-// One CTA of 1024 threads:
-//   1. survival products, one thread per request, multiplied left to right in
-//      double (bit-identical to a sequential evaluation);
-//   2. stable sort, descending: each request's run of gamma values is already
-//      sorted (a is non-increasing in j), so runs are merged pairwise; every
-//      element finds its output slot from its rank in the other run (binary
-//      search), ties keep the flattened order. The keys are compared as the
-//      64-bit patterns of the doubles, which order non-negative doubles exactly
-//      (integer compares: GB300's double-precision rate is low). Keys and
-//      indices live in shared memory up to 8192 candidates, in the workspace
-//      beyond;
-//   3. tau(n) = R + sum of the n largest a, as a block scan in double;
-//   4. the first n with Theta(n) <= Theta(n-1) is found for every n in
-//      parallel by a block min-reduction (every earlier step improved, so
-//      Theta_best = Theta(n-1) there). Theta = tau / T is compared by
-//      cross-multiplication, tau(n) T(R+n-1) vs tau(n-1) T(R+n), which decides
-//      as the quotients do outside the 1e-9 near-tie window;
-//   5. l_r = largest j among the first n* admitted candidates of request r.
+// Up to 16,384 candidates (two launches):
+//   k_sched_rank   every CTA forms all survival products a_{r,j} in shared
+//                  memory (multiplied left to right in double: bit-identical to
+//                  a sequential evaluation) and computes the global rank of a
+//                  block of 32 candidates: each warp binary-searches a share of
+//                  the requests' runs, which are already sorted because a is
+//                  non-increasing in j. The order is a descending, equal values
+//                  in flattened order r*gamma + j, compared as the 64-bit
+//                  patterns of the doubles (exact for non-negative doubles,
+//                  and integer compares: GB300's double-precision rate is about
+//                  1/64 of its float rate).
+//   k_sched_sweep  one CTA: tau(n) = R + sum of the n largest a in float-float
+//                  (about 48 bits), the first n with Theta(n) <= Theta(n-1),
+//                  compared by cross-multiplication tau(n) T(R+n-1) vs
+//                  tau(n-1) T(R+n) -- every earlier step improved, so
+//                  Theta_best = Theta(n-1) there -- and l_r = the largest j
+//                  among the first n* candidates of request r. The decisions
+//                  equal the quotient comparisons of the definition outside
+//                  the 1e-9 near-tie window, which is counted.
+// Beyond that, k_schedule does everything in one CTA: the same products, a
+// merge sort of the runs (pairwise merges by rank), a double block scan and a
+// double sweep.
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -78,6 +82,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     k_schedule(const float* __restrict__ conf, const double* __restrict__ T, int R, int gamma,
                int32_t* __restrict__ verify_len, double* theta_out, uint32_t* ties,
                int32_t* status, SchedWs gws, int use_smem) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ double red[32];
   __shared__ int red_i[32];
@@ -233,8 +239,294 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Parallel path (up to kRankMaxN candidates): ranks over the whole GPU, then a
+// one-CTA sweep in float-float arithmetic.
+// ---------------------------------------------------------------------------
+constexpr int kRankMaxN = 16384;   // candidates of the parallel path
+constexpr int kRankThreads = 1024;
+// keys of R runs at an odd stride: at most 8192 runs of 3 slots (gamma = 2)
+constexpr int kRankSmemMax = 196608;
+
+// float -> double without the double-precision pipe (exact: both are IEEE
+// binary formats, the double has room for every float). Zero and subnormal
+// inputs take the conversion instruction.
+__device__ __forceinline__ double f2d_exact(float f) {
+  const uint32_t u = __float_as_uint(f);
+  if ((u & 0x7F800000u) == 0u || (u & 0x80000000u)) return static_cast<double>(f);
+  const u64 bits = (static_cast<u64>(((u >> 23) & 0xFFu) + (1023u - 127u)) << 52) |
+                   (static_cast<u64>(u & 0x7FFFFFu) << 29);
+  return __longlong_as_double(static_cast<long long>(bits));
+}
+
+// A positive double's top 47 bits as a float pair, by bit manipulation. `ok`
+// turns false above the float range (the caller then decides in double
+// precision); values below 2^-126 read as 0.
+__device__ __forceinline__ ff ff_from_bits(u64 b, bool& ok) {
+  const int E = static_cast<int>((b >> 52) & 0x7FF);
+  if (E == 0) {  // zero (subnormal doubles are below any value that matters here)
+    if (b != 0ull) ok = false;
+    return ff{0.f, 0.f};
+  }
+  const int e = E - 1023;
+  if (e < -126) return ff{0.f, 0.f};  // below 1e-38: absorbed by any tau >= 1, as in double
+  if (e > 127) {
+    ok = false;
+    return ff{0.f, 0.f};
+  }
+  const float hi = __uint_as_float((static_cast<uint32_t>(e + 127) << 23) |
+                                   static_cast<uint32_t>((b >> 29) & 0x7FFFFFull));
+  const float lo = ldexpf(static_cast<float>(static_cast<uint32_t>(b & 0x1FFFFFFFull)), e - 52);
+  return ff{hi, lo};
+}
+
+__device__ __forceinline__ ff ff_from_double(double x, bool& ok) {
+  return ff_from_bits(static_cast<u64>(__double_as_longlong(x)), ok);
+}
+
+// Survival products of every request, bit-identical to a left-to-right double
+// evaluation, into keys[r * stride + j] (64-bit patterns). Returns true if a
+// confidence was outside [0, 1] (it is then taken as 0).
+__device__ bool survival_keys(const float* __restrict__ conf, int R, int gamma, u64* keys,
+                              int stride) {
+  bool bad = false;
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
+    float cv[DSPARK_MAX_GAMMA];
+#pragma unroll
+    for (int j = 0; j < DSPARK_MAX_GAMMA; ++j)
+      cv[j] = j < gamma ? conf[static_cast<long long>(r) * gamma + j] : 0.f;
+    double prod = 1.0;
+#pragma unroll
+    for (int j = 0; j < DSPARK_MAX_GAMMA; ++j) {
+      if (j >= gamma) break;
+      float c = cv[j];
+      if (!(c >= 0.f && c <= 1.f)) {
+        bad = true;
+        c = 0.f;
+      }
+      prod *= f2d_exact(c);
+      keys[r * stride + j] = static_cast<u64>(__double_as_longlong(prod));
+    }
+  }
+  return bad;
+}
+
+// Ranks of the candidates in the global order (a descending, equal values in
+// flattened order). Every CTA builds all keys in shared memory once, then takes
+// blocks of 32 candidates (one per lane); its 32 warps split the requests, and
+// all lanes of a warp binary-search the same request's sorted run (a run of 16
+// keys spans the 32 banks once: no conflicts). Partial counts merge through
+// shared-memory atomics. CTA 0 also validates the inputs and writes the status.
+__global__ void __launch_bounds__(kRankThreads, 1)
+    k_sched_rank(const float* __restrict__ conf, int R, int gamma, SchedWs gws,
+                 int32_t* status) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  extern __shared__ __align__(16) unsigned char smem[];
+  u64* keys = reinterpret_cast<u64*>(smem);
+  __shared__ int sh_bad;
+  __shared__ int sh_cnt[32];
+  const int n = R * gamma;
+  // an odd run stride (in 8-byte keys) keeps a warp's writes of one position
+  // of 32 runs within 2-way bank conflicts
+  const int stride = gamma | 1;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int warps = blockDim.x >> 5;
+  if (threadIdx.x == 0) sh_bad = 0;
+  __syncthreads();
+  if (survival_keys(conf, R, gamma, keys, stride)) atomicOr(&sh_bad, 1);
+  __syncthreads();
+  // the confidences' verdict; k_sched_sweep adds the profile's
+  if (blockIdx.x == 0 && threadIdx.x == 0) *status = sh_bad ? DSPARK_ERR_BAD_DATA : DSPARK_OK;
+
+  const int n_blocks = (n + 31) / 32;
+  for (int blk = blockIdx.x; blk < n_blocks; blk += gridDim.x) {
+    if (threadIdx.x < 32) sh_cnt[threadIdx.x] = 0;
+    __syncthreads();
+    const int e = blk * 32 + lane;
+    const bool live = e < n;
+    const int r = live ? e / gamma : -1;
+    const int j = live ? e - r * gamma : 0;
+    const u64 x = live ? keys[r * stride + j] : 0ull;
+    int cnt = 0;
+    for (int rr = warp; rr < R; rr += warps) {
+      if (rr == r) {
+        cnt += j;  // own run: the j elements before it come first (stable)
+        continue;
+      }
+      const u64* run = keys + rr * stride;
+      const bool earlier = rr < r;  // earlier request: ties come first
+      int lo = 0, hi = gamma;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        const u64 y = run[mid];
+        if (y > x || (earlier && y == x)) lo = mid + 1; else hi = mid;
+      }
+      cnt += lo;
+    }
+    atomicAdd(&sh_cnt[lane], cnt);
+    __syncthreads();
+    if (warp == 0 && live) {
+      const int rank = sh_cnt[lane];
+      gws.keysB[rank] = x;
+      gws.idxB[rank] = e;
+    }
+    __syncthreads();
+  }
+}
+
+constexpr int kSweepSmemMax = (kRankMaxN + 1) * 8 + kRankMaxN * 4;  // profile slice + lengths
+
+// Sweep over the sorted candidates (one CTA): tau(n) = R + sum of the n
+// largest a in float-float, the first n whose Theta(n) = tau(n)/T(R+n) does
+// not exceed Theta(n-1) (compared as tau(n) T(R+n-1) vs tau(n-1) T(R+n)),
+// near ties of the evaluated comparisons, and the admitted lengths. Each
+// thread owns a contiguous chunk (at most CHUNK) of the sorted order and loads its keys once,
+// up front; the profile slice T(R..R(gamma+1)) is staged in shared memory and
+// checked (positive, finite) on the way.
+template <int CHUNK>
+__global__ void __launch_bounds__(kRankThreads, 1)
+    k_sched_sweep(const double* __restrict__ T, int R, int gamma, SchedWs gws,
+                  int32_t* __restrict__ verify_len, double* theta_out, uint32_t* ties,
+                  int32_t* status) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int n = R * gamma;
+  double* sh_T = reinterpret_cast<double*>(smem);                       // T(R + m), m = 0..n
+  int* sh_ell = reinterpret_cast<int*>(smem + (static_cast<size_t>(n) + 1) * 8);  // [R]
+  __shared__ ff sh_w[32];
+  __shared__ int sh_nE, sh_break;
+  __shared__ unsigned sh_ties;
+  __shared__ ff sh_tau_star;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int chunk = (n + blockDim.x - 1) / blockDim.x;
+  const int c0 = min(tid * chunk, n), c1 = min(c0 + chunk, n);
+  const int len = c1 - c0;
+
+  // this thread's keys in registers; the profile slice in shared memory (both
+  // loaded once, up front, so that their latencies overlap)
+  u64 kv[CHUNK];
+#pragma unroll
+  for (int q = 0; q < CHUNK; ++q) kv[q] = q < len ? gws.keysB[c0 + q] : 0ull;
+  bool bad_t = false;
+  for (int m = tid; m <= n; m += blockDim.x) {
+    const double t = T[R + m];
+    const u64 b = static_cast<u64>(__double_as_longlong(t));
+    if ((b >> 63) || ((b >> 52) & 0x7FFull) == 0x7FFull || b == 0ull) bad_t = true;
+    sh_T[m] = t;
+  }
+  if (bad_t) set_status(status, DSPARK_ERR_BAD_DATA);
+  if (tid == 0) {
+    sh_nE = 0;
+    sh_break = INT_MAX;
+    sh_ties = 0;
+    sh_tau_star = ff{static_cast<float>(R), 0.f};
+  }
+  for (int r = tid; r < R; r += blockDim.x) sh_ell[r] = 0;
+
+  // candidates: the non-zero keys, which sort first; this chunk's sum
+  int cnt = 0;
+  bool ok = true;
+  ff local{0.f, 0.f};
+#pragma unroll
+  for (int q = 0; q < CHUNK; ++q) {
+    cnt += kv[q] != 0ull;
+    local = ff_add(local, ff_from_bits(kv[q], ok));
+  }
+  cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+  // exclusive block scan of the chunk sums
+  ff v = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const ff t = shfl_up_ff(v, o);
+    if (lane >= o) v = ff_add(t, v);
+  }
+  ff ex = shfl_up_ff(v, 1);
+  if (lane == 0) ex = ff{0.f, 0.f};
+  __syncthreads();  // shared state initialised
+  if (lane == 0) atomicAdd(&sh_nE, cnt);
+  if (lane == 31) sh_w[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    ff w = lane < static_cast<int>(blockDim.x >> 5) ? sh_w[lane] : ff{0.f, 0.f};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const ff t = shfl_up_ff(w, o);
+      if (lane >= o) w = ff_add(t, w);
+    }
+    sh_w[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int nE = sh_nE;
+  ff tau_start = ff_add(ff{static_cast<float>(R), 0.f}, ex);
+  if (warp > 0) tau_start = ff_add(tau_start, sh_w[warp - 1]);
+
+  // walk the chunk: first non-improving admission, near ties up to it
+  int first = INT_MAX;
+  unsigned n_ties = 0;
+  ff tau_prev = tau_start;
+  bool okt = true;
+  ff tp = ff_from_double(sh_T[c0], okt);
+#pragma unroll
+  for (int q = 0; q < CHUNK; ++q) {
+    const int m = c0 + q + 1;
+    if (q < len && m <= nE && first == INT_MAX) {
+      bool okv = ok && okt;
+      const ff tau_m = ff_add(tau_prev, ff_from_bits(kv[q], okv));
+      const double Tp = sh_T[m - 1], Tm = sh_T[m];
+      const ff tm = ff_from_double(Tm, okv);
+      bool improve, tie;
+      if (okv) {
+        const ff lhs = ff_mul(tau_m, tp), rhs = ff_mul(tau_prev, tm);
+        improve = ff_cmp(lhs, rhs) > 0;
+        const ff d = ff_sub(lhs, rhs);
+        tie = fabsf(d.hi) <= static_cast<float>(DSPARK_SCHED_TIE_REL) * rhs.hi;
+      } else {  // values outside the float range: double precision
+        const double A = static_cast<double>(tau_m.hi) + tau_m.lo;
+        const double Bv = static_cast<double>(tau_prev.hi) + tau_prev.lo;
+        improve = A * Tp > Bv * Tm;
+        tie = fabs(A * Tp - Bv * Tm) <= DSPARK_SCHED_TIE_REL * Bv * Tm;
+      }
+      if (tie) ++n_ties;
+      if (!improve) first = m;
+      tau_prev = tau_m;
+      tp = tm;
+    }
+  }
+  const int fw = __reduce_min_sync(0xFFFFFFFFu, first);
+  if (lane == 0) atomicMin(&sh_break, fw);
+  __syncthreads();
+  const int n_break = sh_break;
+  const int n_star = n_break <= nE ? n_break - 1 : nE;
+  if (c0 + 1 <= n_break && n_ties) atomicAdd(&sh_ties, n_ties);
+  // tau(n*) for Theta_best, from the thread whose chunk holds position n*
+  if (n_star > 0 && c0 < n_star && n_star <= c1) {
+    ff t = tau_start;
+    bool okv = true;
+#pragma unroll
+    for (int q = 0; q < CHUNK; ++q)
+      if (c0 + q < n_star) t = ff_add(t, ff_from_bits(kv[q], okv));
+    sh_tau_star = t;
+  }
+  for (int i = tid; i < n_star; i += blockDim.x) {
+    const int id = gws.idxB[i];
+    atomicMax(&sh_ell[id / gamma], id % gamma + 1);
+  }
+  __syncthreads();
+  for (int r = tid; r < R; r += blockDim.x) verify_len[r] = sh_ell[r];
+  if (tid == 0) {
+    *ties = sh_ties;
+    if (theta_out) {
+      const double tau_star = static_cast<double>(sh_tau_star.hi) + sh_tau_star.lo;
+      *theta_out = tau_star / sh_T[n_star];
+    }
+  }
+}
+
 std::mutex g_sched_mutex;
 bool g_sched_ready[128];
+int g_sched_sms[128];
 
 }  // namespace dspark
 
@@ -254,14 +546,29 @@ extern "C" int dspark_schedule(const float* confidences, const double* step_time
     return DSPARK_ERR_WORKSPACE;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return DSPARK_ERR_CUDA;
+  int sms = 0;
   {
     std::lock_guard<std::mutex> lock(g_sched_mutex);
     if (!g_sched_ready[dev]) {
       if (cudaFuncSetAttribute(k_schedule, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSchedSmemMaxN * 24) != cudaSuccess)
         return DSPARK_ERR_CUDA;
+      if (cudaFuncSetAttribute(k_sched_rank, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kRankSmemMax) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+      if (cudaFuncSetAttribute(k_sched_sweep<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSweepSmemMax) != cudaSuccess ||
+          cudaFuncSetAttribute(k_sched_sweep<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSweepSmemMax) != cudaSuccess ||
+          cudaFuncSetAttribute(k_sched_sweep<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSweepSmemMax) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+      if (cudaDeviceGetAttribute(&g_sched_sms[dev], cudaDevAttrMultiProcessorCount, dev) !=
+          cudaSuccess)
+        return DSPARK_ERR_CUDA;
       g_sched_ready[dev] = true;
     }
+    sms = g_sched_sms[dev];
   }
   const int n = R * gamma;
   char* p = static_cast<char*>(workspace);
@@ -277,11 +584,34 @@ extern "C" int dspark_schedule(const float* confidences, const double* step_time
   ws.idxB = reinterpret_cast<int32_t*>(p);
   p += DSPARK_ALIGN256(static_cast<size_t>(n) * 4);
   ws.ell = reinterpret_cast<int32_t*>(p);
-  const int use_smem = n <= kSchedSmemMaxN ? 1 : 0;
-  const size_t smem = use_smem ? static_cast<size_t>(n) * 24 : 0;
-  k_schedule<<<1, kSchedThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-      confidences, step_time_ms, R, gamma, verify_len, theta_best,
-      near_tie_count ? near_tie_count : ws.ties_scratch, device_status, ws, use_smem);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* ties = near_tie_count ? near_tie_count : ws.ties_scratch;
+  const size_t rank_smem = static_cast<size_t>(R) * (gamma | 1) * 8;
+  if (n <= kRankMaxN && rank_smem <= static_cast<size_t>(kRankSmemMax)) {
+    // ranks over the whole GPU, then a one-CTA float-float sweep
+    const int blocks = (n + 31) / 32;
+    const int grid = blocks < sms ? blocks : sms;
+    cudaError_t e = launch_pdl(k_sched_rank, grid, kRankThreads, rank_smem, st, confidences, R,
+                               gamma, ws, device_status);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+    const size_t sweep_smem = (static_cast<size_t>(n) + 1) * 8 + static_cast<size_t>(R) * 4;
+    if (n <= 4 * kRankThreads)
+      e = launch_pdl(k_sched_sweep<4>, 1, kRankThreads, sweep_smem, st, step_time_ms, R, gamma, ws,
+                     verify_len, theta_best, ties, device_status);
+    else if (n <= 8 * kRankThreads)
+      e = launch_pdl(k_sched_sweep<8>, 1, kRankThreads, sweep_smem, st, step_time_ms, R, gamma, ws,
+                     verify_len, theta_best, ties, device_status);
+    else
+      e = launch_pdl(k_sched_sweep<16>, 1, kRankThreads, sweep_smem, st, step_time_ms, R, gamma,
+                     ws, verify_len, theta_best, ties, device_status);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  } else {
+    const int use_smem = n <= kSchedSmemMaxN ? 1 : 0;
+    const size_t smem = use_smem ? static_cast<size_t>(n) * 24 : 0;
+    if (launch_pdl(k_schedule, 1, kSchedThreads, smem, st, confidences, step_time_ms, R, gamma,
+                   verify_len, theta_best, ties, device_status, ws, use_smem) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+  }
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }

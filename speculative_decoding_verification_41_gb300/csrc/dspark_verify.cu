@@ -7,7 +7,7 @@
 // nothing is admitted). The residual max(0, p_t - p_d) after a rejection is the
 // standard rule of the speculative sampling papers cited there as [1], [2].
 //
-// Pipeline (five launches on the caller's stream, no host synchronisation):
+// Pipeline (three launches on the caller's stream, no host synchronisation):
 //   k_plan      one CTA: validates verify lengths and row offsets, lays out the
 //               rows to read (l_r + 1 target rows and l_r draft rows per
 //               request) and resets counters.
@@ -23,15 +23,16 @@
 //               statistics (sum as a float pair, K) go to the workspace. No
 //               double-precision instruction runs per logit: GB300's FP64 rate
 //               is a small fraction of its FP32 rate.
-//   k_verify    one warp per request: merges the unit statistics of its rows
-//               (compensated float), evaluates the ratio p_t^k(x_k)/p_d^k(x_k)
-//               in float and redoes it in double only when the uniform lies
-//               within 2e-6 of it, finds the first rejection with a warp ballot
-//               and writes accepted lengths, tokens and probabilities.
-//   k_resample_sums  grid-stride warps over (request, segment of 2048 tokens):
-//               sums of the residual (or target) weights per segment.
-//   k_resample_pick  one CTA per request: scans the segment sums, re-reads the
-//               one segment holding the cut and scans it to pick the token.
+//   k_decide    kDecideParts CTAs per request. Each merges the unit
+//               statistics of the request's rows in parallel (compensated
+//               float, exact power-of-two alignment), evaluates the ratio
+//               p_t^k(x_k)/p_d^k(x_k) in float -- in double only when the
+//               uniform lies within 2e-6 of it -- and finds the first
+//               rejection with a warp ballot; part 0 writes accepted lengths,
+//               tokens and probabilities. Each part then sums the residual (or
+//               bonus) weights of its share of the 2048-token segments; the
+//               last part to finish scans the segment sums, re-reads the one
+//               segment holding the cut and picks the token.
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -80,7 +81,7 @@ struct VerifyWs {
   int64_t* row_list;       // [rows]: (global row << 1) | is_draft
   TileStat* tiles;         // [rows * n_units]
   ResampleDesc* desc;      // [B]
-  double* seg_sum;         // [B * n_seg]
+  ff* seg_sum;             // [B * n_seg]: per-segment weight sums as float pairs
   uint32_t* tickets;       // [B]
 };
 
@@ -128,6 +129,8 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verif
                                                const int64_t* __restrict__ doff, int B,
                                                int gamma, VerifyWs ws, uint32_t* ties,
                                                int32_t* status) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -315,6 +318,8 @@ template <typename Tin, int W, int STAGES>
 __global__ void __launch_bounds__(W * 32, 1)
     k_rowstats_tma(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int V, int n_units,
                    VerifyWs ws, ExpParams ep, int32_t* status) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
   constexpr int VPL = kChunkBytes / 16 / 32;  // 16-byte vectors per lane per chunk
   extern __shared__ __align__(1024) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -409,6 +414,8 @@ __global__ void __launch_bounds__(256) k_rowstats_plain(const Tin* __restrict__ 
                                                         const Tin* __restrict__ dl, int V,
                                                         int n_units, VerifyWs ws, ExpParams ep,
                                                         int32_t* status) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
   constexpr int kUnitElems = kUnitBytes / sizeof(Tin);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long U = static_cast<long long>(ws.hdr->total_rows) * n_units;
@@ -441,29 +448,6 @@ struct RowStat {
   bool ok;
 };
 
-__device__ RowStat merge_row(const TileStat* __restrict__ t, int n_units) {
-  RowStat r;
-  r.K = INT_MIN;
-  r.ok = true;
-  for (int i = 0; i < n_units; ++i) {
-    const TileStat ts = t[i];
-    if (ts.bad) r.ok = false;
-    if (ts.K != INT_MIN && ts.K > r.K) r.K = ts.K;
-  }
-  float hi = 0.f, lo = 0.f;
-  for (int i = 0; i < n_units; ++i) {
-    const TileStat ts = t[i];
-    if (ts.K == INT_MIN) continue;
-    const int d = ts.K - r.K;
-    two_sum_acc(hi, lo, scale_pow2(ts.s_hi, d), scale_pow2(ts.s_lo, d));
-  }
-  const float s = hi + lo;
-  r.S_hi = s;
-  r.S_lo = lo - (s - hi);
-  r.ok = r.ok && r.K != INT_MIN && s > 0.f && isfinite(s);
-  return r;
-}
-
 // 2^a for a double exponent: split into an integer and a fraction in
 // [-0.5, 0.5] so that the float exponential only sees a small argument
 // (relative error ~1 ulp whatever the size of a). A few double operations per
@@ -485,28 +469,69 @@ __device__ __forceinline__ double prob_f64(float z, const RowStat& s, const ExpP
   return exp2(a) / (static_cast<double>(s.S_hi) + static_cast<double>(s.S_lo));
 }
 
-template <typename Tin>
-__global__ void __launch_bounds__(64) k_verify(
-    const Tin* __restrict__ tl, const Tin* __restrict__ dl, const int32_t* __restrict__ tokens,
-    const float* __restrict__ uniforms, int B, int gamma, int V, int n_units, ExpParams ep,
-    VerifyWs ws, int32_t* __restrict__ accepted_len, int32_t* __restrict__ emitted,
-    float* __restrict__ probs_out, uint32_t* ties, int32_t* status) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * 2 + warp;
-  if (r >= B) return;
-  const int start = ws.req_row_start[r], end = ws.req_row_start[r + 1];
-  int32_t* em = emitted + static_cast<long long>(r) * (gamma + 1);
-  float* pr = probs_out ? probs_out + static_cast<long long>(r) * gamma * 2 : nullptr;
-  if (end == start) {  // invalid request (reported by k_plan): defined, in-bounds outputs
-    for (int k = lane; k <= gamma; k += 32) em[k] = -1;
-    if (pr)
-      for (int k = lane; k < gamma; k += 32) pr[2 * k] = pr[2 * k + 1] = -1.f;
-    if (lane == 0) {
-      accepted_len[r] = 0;
-      ws.desc[r].mode = kModeNone;
-    }
+// (K, hi, lo) += (K2, h2, l2): align by an exact power of two, add by TwoSum.
+__device__ __forceinline__ void stat_combine(int& K, float& hi, float& lo, int K2, float h2,
+                                             float l2) {
+  if (K2 == INT_MIN) return;
+  if (K == INT_MIN) {
+    K = K2;
+    hi = h2;
+    lo = l2;
     return;
   }
+  if (K2 > K) {
+    hi = scale_pow2(hi, K - K2);
+    lo = scale_pow2(lo, K - K2);
+    K = K2;
+  } else {
+    h2 = scale_pow2(h2, K2 - K);
+    l2 = scale_pow2(l2, K2 - K);
+  }
+  two_sum_acc(hi, lo, h2, l2);
+}
+
+// One row's statistics from its unit records, all lanes of a warp: lanes take
+// units, then a butterfly combine. Lane 0's result is the one used.
+__device__ RowStat warp_merge_row(const TileStat* __restrict__ t, int n_units, int lane) {
+  int K = INT_MIN;
+  float hi = 0.f, lo = 0.f;
+  bool bad = false;
+  for (int u = lane; u < n_units; u += 32) {
+    const TileStat ts = t[u];
+    bad = bad || ts.bad != 0;
+    stat_combine(K, hi, lo, ts.K, ts.s_hi, ts.s_lo);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const int K2 = __shfl_xor_sync(0xFFFFFFFFu, K, o);
+    const float h2 = __shfl_xor_sync(0xFFFFFFFFu, hi, o);
+    const float l2 = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+    stat_combine(K, hi, lo, K2, h2, l2);
+  }
+  RowStat r;
+  const float s = hi + lo;
+  r.S_hi = s;
+  r.S_lo = lo - (s - hi);
+  r.K = K;
+  r.ok = !__any_sync(0xFFFFFFFFu, bad) && K != INT_MIN && s > 0.f && isfinite(s);
+  return r;
+}
+
+// Ratio tests of request r by one warp (lane k-1 tests position k), from the
+// row statistics in sh_rs (target rows 0..ell, draft rows ell+1..2ell). With
+// write_out it stores accepted_len, the accepted tokens, the probabilities and
+// the near ties of these decisions. Lane 0 writes the descriptor of the token
+// to draw after the block to *d_out.
+template <typename Tin>
+__device__ void ratio_tests(const Tin* __restrict__ tl, const Tin* __restrict__ dl,
+                            const int32_t* __restrict__ tokens, const float* __restrict__ uniforms,
+                            int r, int gamma, int V, int start, const RowStat* sh_rs,
+                            const ExpParams& ep, const VerifyWs& ws, bool write_out,
+                            int32_t* __restrict__ accepted_len, int32_t* __restrict__ emitted,
+                            float* __restrict__ probs_out, uint32_t* ties, int32_t* status,
+                            ResampleDesc* d_out, int lane, int end) {
+  int32_t* em = emitted + static_cast<long long>(r) * (gamma + 1);
+  float* pr = probs_out ? probs_out + static_cast<long long>(r) * gamma * 2 : nullptr;
   const int ell = (end - start - 1) / 2;
   const int k = lane + 1;  // the position this lane tests
   const bool has = k <= ell;
@@ -515,8 +540,8 @@ __global__ void __launch_bounds__(64) k_verify(
   int32_t x = 0;
   RowStat st{}, sd{};
   if (has) {
-    st = merge_row(ws.tiles + static_cast<long long>(start + k - 1) * n_units, n_units);
-    sd = merge_row(ws.tiles + static_cast<long long>(start + ell + k) * n_units, n_units);
+    st = sh_rs[k - 1];
+    sd = sh_rs[ell + k];
     x = tokens[static_cast<long long>(r) * gamma + k - 1];
     const float u = uniforms[static_cast<long long>(r) * (gamma + 1) + k - 1];
     if (x < 0 || x >= V || !(u >= 0.f && u < 1.f) || !st.ok || !sd.ok) {
@@ -545,17 +570,19 @@ __global__ void __launch_bounds__(64) k_verify(
   const unsigned rej = __ballot_sync(0xFFFFFFFFu, has && !accept);
   const int m = rej ? __ffs(rej) - 1 : ell;
   const unsigned n_ties = __popc(__ballot_sync(0xFFFFFFFFu, tie && k <= m + 1));
-  if (lane == 0 && n_ties) atomicAdd(ties, n_ties);
+  if (write_out && lane == 0 && n_ties) atomicAdd(ties, n_ties);
 
-  if (pr && lane < gamma) {
+  if (write_out && pr && lane < gamma) {
     pr[2 * lane] = has ? pt : -1.f;
     pr[2 * lane + 1] = has ? pd : -1.f;
   }
-  if (lane < m)
-    em[lane] = x;
-  else if (lane > m && lane <= gamma)
-    em[lane] = -1;
-  if (lane == 0 && gamma == 32 && m < 32) em[32] = -1;
+  if (write_out) {
+    if (lane < m)
+      em[lane] = x;
+    else if (lane > m && lane <= gamma)
+      em[lane] = -1;
+    if (lane == 0 && gamma == 32 && m < 32) em[32] = -1;
+  }
 
   // descriptor of the token to sample after the block
   const int src = m < ell ? m : 0;
@@ -566,7 +593,7 @@ __global__ void __launch_bounds__(64) k_verify(
   const int Kt = __shfl_sync(0xFFFFFFFFu, st.K, src);
   const int Kd = __shfl_sync(0xFFFFFFFFu, sd.K, src);
   if (lane == 0) {
-    accepted_len[r] = m;
+    if (write_out) accepted_len[r] = m;
     ResampleDesc d;
     d.u = uniforms[static_cast<long long>(r) * (gamma + 1) + gamma];
     if (!(d.u >= 0.f && d.u < 1.f)) {
@@ -587,8 +614,7 @@ __global__ void __launch_bounds__(64) k_verify(
       d.D_hi = static_cast<float>(D);
       d.D_lo = static_cast<float>(D - static_cast<double>(d.D_hi));
     } else {
-      const RowStat sb = merge_row(ws.tiles + static_cast<long long>(start + ell) * n_units,
-                                   n_units);
+      const RowStat sb = sh_rs[ell];  // the bonus row (position ell + 1)
       if (!sb.ok) set_status(status, DSPARK_ERR_BAD_DATA);
       d.mode = kModeTarget;
       d.t_row = ws.row_list[start + ell] >> 1;
@@ -596,7 +622,7 @@ __global__ void __launch_bounds__(64) k_verify(
       d.K_t = sb.K == INT_MIN ? 0 : sb.K;
       d.D_hi = d.D_lo = 0.f;
     }
-    ws.desc[r] = d;
+    *d_out = d;
   }
 }
 
@@ -667,89 +693,65 @@ __device__ void segment_sum(const Tin* __restrict__ zt, const Tin* __restrict__ 
   out_lo = lo;
 }
 
-// Segment sums of every request's resample weights: a grid-stride loop of
-// warps over (request, segment) items.
+// The whole CTA (256 threads) draws request r's token: finds the segment
+// holding u*Z from the segment sums, then the token inside it. Running sums
+// are float pairs (about 48 bits), far finer than the 1e-6*Z near-tie window.
 template <typename Tin, bool VEC>
-__global__ void __launch_bounds__(256) k_resample_sums(const Tin* __restrict__ tl,
-                                                       const Tin* __restrict__ dl, int V,
-                                                       int n_seg, int B, ExpParams ep,
-                                                       VerifyWs ws) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long items = static_cast<long long>(B) * n_seg;
-  for (long long it = static_cast<long long>(blockIdx.x) * 8 + warp; it < items;
-       it += static_cast<long long>(gridDim.x) * 8) {
-    const int r = static_cast<int>(it / n_seg);
-    const int sgi = static_cast<int>(it - static_cast<long long>(r) * n_seg);
-    const ResampleDesc d = ws.desc[r];
-    if (d.mode == kModeNone) continue;
-    const Tin* zt = tl + d.t_row * static_cast<long long>(V);
-    const Tin* zd = d.mode == kModeResidual ? dl + d.d_row * static_cast<long long>(V) : zt;
-    float hi, lo;
-    segment_sum<Tin, VEC>(zt, zd, sgi * kSeg, min(V, (sgi + 1) * kSeg), d.mode,
-                          -static_cast<float>(d.K_t), d.D_hi, d.D_lo, ep, lane, hi, lo);
-    if (lane == 0) ws.seg_sum[it] = static_cast<double>(hi) + static_cast<double>(lo);
-  }
-}
-
-// One CTA per request: find the segment holding u*Z, then the token inside it.
-template <typename Tin, bool VEC>
-__global__ void __launch_bounds__(256) k_resample_pick(const Tin* __restrict__ tl,
-                                                       const Tin* __restrict__ dl, int V,
-                                                       int n_seg, int gamma, ExpParams ep,
-                                                       VerifyWs ws, int32_t* __restrict__ emitted,
-                                                       uint32_t* ties, int32_t* status) {
-  const int r = blockIdx.x;
-  const ResampleDesc d = ws.desc[r];
-  if (d.mode == kModeNone) return;
+__device__ void pick_token(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int V,
+                           int n_seg, int gamma, const ExpParams& ep, const VerifyWs& ws,
+                           const ResampleDesc& d, int r, int32_t* __restrict__ emitted,
+                           uint32_t* ties, int32_t* status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const Tin* zt = tl + d.t_row * static_cast<long long>(V);
   const Tin* zd = d.mode == kModeResidual ? dl + d.d_row * static_cast<long long>(V) : zt;
   const float nK = -static_cast<float>(d.K_t);
-  double* seg = ws.seg_sum + static_cast<long long>(r) * n_seg;
+  ff* seg = ws.seg_sum + static_cast<long long>(r) * n_seg;
 
-  __shared__ double sh_P, sh_Z;
+  __shared__ ff sh_P, sh_Z;
   __shared__ int sh_j;
-  __shared__ double warp_tot[8];
+  __shared__ ff warp_tot[8];
   __shared__ unsigned long long sh_pick;  // (index << 1) | near-tie flag, min over threads
   __shared__ int sh_last_pos;
   int mode = d.mode;
   uint32_t flagged = 0;
+  const ff zero{0.f, 0.f};
   for (int attempt = 0; attempt < 2; ++attempt) {
     if (warp == 0) {
-      // Z = running sum of the segment sums, 32 at a time (double)
-      double run = 0.0;
+      // Z = running sum of the segment sums, 32 at a time
+      ff run = zero;
       for (int c = 0; c < n_seg; c += 32) {
-        double v = (c + lane < n_seg) ? seg[c + lane] : 0.0;
+        ff v = (c + lane < n_seg) ? seg[c + lane] : zero;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const double w = __shfl_up_sync(0xFFFFFFFFu, v, o);
-          if (lane >= o) v += w;
+          const ff w = shfl_up_ff(v, o);
+          if (lane >= o) v = ff_add(w, v);
         }
-        run += __shfl_sync(0xFFFFFFFFu, v, 31);
+        run = ff_add(run, shfl_ff(v, 31));
       }
-      const double Z = run;
-      const double U = static_cast<double>(d.u) * Z;
+      const ff Z = run;
+      const ff U = ff_mul(Z, ff{d.u, 0.f});
       int j = -1;
-      double P = 0.0;
-      run = 0.0;
+      ff P = zero;
+      run = zero;
       for (int c = 0; c < n_seg && j < 0; c += 32) {
-        double v = (c + lane < n_seg) ? seg[c + lane] : 0.0;
-        const double own = v;
+        ff v = (c + lane < n_seg) ? seg[c + lane] : zero;
+        const bool own_pos = v.hi > 0.f;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const double w = __shfl_up_sync(0xFFFFFFFFu, v, o);
-          if (lane >= o) v += w;
+          const ff w = shfl_up_ff(v, o);
+          if (lane >= o) v = ff_add(w, v);
         }
-        const double incl = run + v;
-        const double prev_incl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-        const double excl = lane == 0 ? run : prev_incl;  // running sum before this segment
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, c + lane < n_seg && own > 0.0 && incl > U);
+        const ff incl = ff_add(run, v);
+        const ff prev_incl = shfl_up_ff(incl, 1);
+        const ff excl = lane == 0 ? run : prev_incl;  // running sum before this segment
+        const unsigned hit =
+            __ballot_sync(0xFFFFFFFFu, c + lane < n_seg && own_pos && ff_cmp(incl, U) > 0);
         if (hit) {
           const int l = __ffs(hit) - 1;
           j = c + l;
-          P = __shfl_sync(0xFFFFFFFFu, excl, l);
+          P = shfl_ff(excl, l);
         }
-        run += __shfl_sync(0xFFFFFFFFu, v, 31);
+        run = ff_add(run, shfl_ff(v, 31));
       }
       if (lane == 0) {
         sh_Z = Z;
@@ -758,28 +760,29 @@ __global__ void __launch_bounds__(256) k_resample_pick(const Tin* __restrict__ t
       }
     }
     __syncthreads();
-    if (sh_Z > 0.0 || attempt == 1) break;
+    if (sh_Z.hi > 0.f || attempt == 1) break;
     // zero residual mass (only in floating point): sample the target row instead
     mode = kModeTarget;
     flagged = 1;
-    for (int s = warp; s < n_seg; s += 8) {
+    for (int s2 = warp; s2 < n_seg; s2 += 8) {
       float hi, lo;
-      segment_sum<Tin, VEC>(zt, zt, s * kSeg, min(V, (s + 1) * kSeg), kModeTarget, nK, 0.f, 0.f,
+      segment_sum<Tin, VEC>(zt, zt, s2 * kSeg, min(V, (s2 + 1) * kSeg), kModeTarget, nK, 0.f, 0.f,
                             ep, lane, hi, lo);
-      if (lane == 0) seg[s] = static_cast<double>(hi) + static_cast<double>(lo);
+      if (lane == 0) seg[s2] = ff_norm(hi, lo);
     }
     __syncthreads();
   }
-  const double Z = sh_Z, P = sh_P;
+  const ff Z = sh_Z, P = sh_P;
   const int j = sh_j;
-  if (!(Z > 0.0) || j < 0) {  // no mass at all: non-finite or empty rows
+  if (!(Z.hi > 0.f) || j < 0) {  // no mass at all: non-finite or empty rows
     if (tid == 0) {
       set_status(status, DSPARK_ERR_BAD_DATA);
       emitted[static_cast<long long>(r) * (gamma + 1) + d.m] = 0;
     }
     return;
   }
-  const double U = static_cast<double>(d.u) * Z;
+  const ff U = ff_mul(Z, ff{d.u, 0.f});
+  const float win = static_cast<float>(DSPARK_TIE_EPS) * Z.hi;  // near-tie window
   // fine scan of segment j: 8 consecutive tokens per thread
   const int a = j * kSeg, b = min(V, a + kSeg);
   const int i0 = a + tid * 8;
@@ -794,38 +797,42 @@ __global__ void __launch_bounds__(256) k_resample_pick(const Tin* __restrict__ t
       w[q] = resample_weight(z1, z2, mode, nK, d.D_hi, d.D_lo, ep);
     }
   }
-  const float mine = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
-  double incl = static_cast<double>(mine);
+  ff mine = zero;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) mine = ff_add(mine, ff{w[q], 0.f});
+  ff incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
+    const ff t = shfl_up_ff(incl, o);
+    if (lane >= o) incl = ff_add(t, incl);
   }
+  ff ex = shfl_up_ff(incl, 1);
+  if (lane == 0) ex = zero;
   if (tid == 0) {
     sh_pick = ~0ull;
     sh_last_pos = -1;
   }
   if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
-  double before = P + (incl - static_cast<double>(mine));
-  for (int q = 0; q < warp; ++q) before += warp_tot[q];
+  ff before = ff_add(P, ex);
+  for (int q = 0; q < warp; ++q) before = ff_add(before, warp_tot[q]);
   int last_pos = -1;
   for (int q = 0; q < 8; ++q)
     if (w[q] > 0.f) last_pos = i0 + q;
-  // only the thread whose range can hold the cut walks its tokens in double
-  if (before <= U && before + static_cast<double>(mine) * (1.0 + 1e-6) > U) {
-    double C = before;
+  // only the thread whose range can hold the cut walks its tokens
+  if (ff_cmp(before, U) <= 0 && ff_cmp(ff_add(before, mine), U) > 0) {
+    ff C = before;
     for (int q = 0; q < 8; ++q) {
-      const double below = C;
-      C += static_cast<double>(w[q]);
-      if (C > U) {
-        const bool near = (U - below) < DSPARK_TIE_EPS * Z || (C - U) < DSPARK_TIE_EPS * Z;
+      const ff below = C;
+      C = ff_add(C, ff{w[q], 0.f});
+      if (ff_cmp(C, U) > 0) {
+        const bool near = ff_sub(U, below).hi < win || ff_sub(C, U).hi < win;
         atomicMin(&sh_pick, (static_cast<unsigned long long>(i0 + q) << 1) | (near ? 1ull : 0ull));
         break;
       }
     }
   }
-  if (before <= U && last_pos >= 0) atomicMax(&sh_last_pos, last_pos);
+  if (ff_cmp(before, U) <= 0 && last_pos >= 0) atomicMax(&sh_last_pos, last_pos);
   __syncthreads();
   if (tid == 0) {
     int y;
@@ -839,6 +846,79 @@ __global__ void __launch_bounds__(256) k_resample_pick(const Tin* __restrict__ t
     emitted[static_cast<long long>(r) * (gamma + 1) + d.m] = y;
     if (flagged) atomicAdd(ties, 1u);
   }
+}
+
+// ---------------------------------------------------------------------------
+// k_decide: ratio tests, residual / bonus segment sums and the draw, fused
+// ---------------------------------------------------------------------------
+constexpr int kDecideParts = 4;  // CTAs per request: their segment shares balance the grid
+constexpr int kDecideWarps = 8;
+
+// kDecideParts CTAs per request. Each one merges the request's row statistics
+// and runs the ratio tests (cheap, so every part recomputes them and no part
+// waits for another); part 0 writes the verification outputs. Each part sums
+// the residual (or bonus) weights of its share of the 2048-token segments;
+// the part that finishes last (ticket reset by k_plan) draws the token.
+template <typename Tin, bool VEC>
+__global__ void __launch_bounds__(kDecideWarps * 32) k_decide(
+    const Tin* __restrict__ tl, const Tin* __restrict__ dl, const int32_t* __restrict__ tokens,
+    const float* __restrict__ uniforms, int B, int gamma, int V, int n_units, int n_seg,
+    ExpParams ep, VerifyWs ws, int32_t* __restrict__ accepted_len, int32_t* __restrict__ emitted,
+    float* __restrict__ probs_out, uint32_t* ties, int32_t* status) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  __shared__ RowStat sh_rs[2 * DSPARK_MAX_GAMMA + 1];
+  __shared__ ResampleDesc sh_d;
+  __shared__ int sh_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x / kDecideParts, part = blockIdx.x - r * kDecideParts;
+  const bool lead = part == 0;
+  const int start = ws.req_row_start[r], end = ws.req_row_start[r + 1];
+  if (end == start) {  // invalid request (reported by k_plan): defined, in-bounds outputs
+    if (lead && warp == 0) {
+      int32_t* em = emitted + static_cast<long long>(r) * (gamma + 1);
+      for (int k = lane; k <= gamma; k += 32) em[k] = -1;
+      if (probs_out) {
+        float* pr = probs_out + static_cast<long long>(r) * gamma * 2;
+        for (int k = lane; k < gamma; k += 32) pr[2 * k] = pr[2 * k + 1] = -1.f;
+      }
+      if (lane == 0) accepted_len[r] = 0;
+    }
+    return;
+  }
+  // 1. the request's row statistics, warps in parallel
+  for (int row = warp; row < end - start; row += kDecideWarps) {
+    const RowStat rs =
+        warp_merge_row(ws.tiles + static_cast<long long>(start + row) * n_units, n_units, lane);
+    if (lane == 0) sh_rs[row] = rs;
+  }
+  __syncthreads();
+  // 2. ratio tests and the first rejection
+  if (warp == 0)
+    ratio_tests<Tin>(tl, dl, tokens, uniforms, r, gamma, V, start, sh_rs, ep, ws, lead,
+                     accepted_len, emitted, probs_out, ties, status, &sh_d, lane, end);
+  __syncthreads();
+  const ResampleDesc d = sh_d;
+  // 3. this part's segment sums of the draw's weights
+  const Tin* zt = tl + d.t_row * static_cast<long long>(V);
+  const Tin* zd = d.mode == kModeResidual ? dl + d.d_row * static_cast<long long>(V) : zt;
+  const float nK = -static_cast<float>(d.K_t);
+  for (int sg = part * kDecideWarps + warp; sg < n_seg; sg += kDecideParts * kDecideWarps) {
+    float hi, lo;
+    segment_sum<Tin, VEC>(zt, zd, sg * kSeg, min(V, (sg + 1) * kSeg), d.mode, nK, d.D_hi, d.D_lo,
+                          ep, lane, hi, lo);
+    if (lane == 0) ws.seg_sum[static_cast<long long>(r) * n_seg + sg] = ff_norm(hi, lo);
+  }
+  // 4. the last part to finish draws the token
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    sh_last = atomicAdd(&ws.tickets[r], 1u) == kDecideParts - 1;
+  }
+  __syncthreads();
+  if (!sh_last) return;
+  __threadfence();
+  pick_token<Tin, VEC>(tl, dl, V, n_seg, gamma, ep, ws, d, r, emitted, ties, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -905,7 +985,7 @@ VerifyWs carve_verify_ws(void* base, int B, int gamma, int V) {
   p += DSPARK_ALIGN256(DSPARK_MAX_ROWS(B, gamma) * DSPARK_TILES_PER_ROW(V) * 16);
   ws.desc = reinterpret_cast<ResampleDesc*>(p);
   p += DSPARK_ALIGN256(static_cast<size_t>(B) * 64);
-  ws.seg_sum = reinterpret_cast<double*>(p);
+  ws.seg_sum = reinterpret_cast<ff*>(p);
   p += DSPARK_ALIGN256(static_cast<size_t>(B) * DSPARK_SEGS_PER_ROW(V) * 8);
   ws.tickets = reinterpret_cast<uint32_t*>(p);
   return ws;
@@ -926,8 +1006,9 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
   const int n_units = (V + unit_elems - 1) / unit_elems;
   const int n_seg = (V + kSeg - 1) / kSeg;
 
-  k_plan<<<1, 1024, 0, stream>>>(vlen, toff, doff, B, gamma, ws, tie_ctr, status);
-  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (launch_pdl(k_plan, 1, 1024, 0, stream, vlen, toff, doff, B, gamma, ws, tie_ctr, status) !=
+      cudaSuccess)
+    return DSPARK_ERR_CUDA;
   if (B == 0) return DSPARK_OK;
 
   const bool aligned = (static_cast<size_t>(V) * sizeof(Tin)) % 16 == 0 &&
@@ -937,34 +1018,27 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
   if (aligned) {
     const long long want = (max_units + kStreamWarps - 1) / kStreamWarps;
     const int grid = static_cast<int>(want < sms ? want : sms);
-    k_rowstats_tma<Tin, kStreamWarps, kStages>
-        <<<grid, kStreamWarps * 32, tma_smem_bytes(), stream>>>(tl, dl, V, n_units, ws, ep,
-                                                                status);
+    if (launch_pdl(k_rowstats_tma<Tin, kStreamWarps, kStages>, grid, kStreamWarps * 32,
+                   tma_smem_bytes(), stream, tl, dl, V, n_units, ws, ep, status) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
   } else {
     const long long want = (max_units + 7) / 8;
     const int grid = static_cast<int>(want < 4LL * sms ? want : 4LL * sms);
-    k_rowstats_plain<Tin><<<grid, 256, 0, stream>>>(tl, dl, V, n_units, ws, ep, status);
+    if (launch_pdl(k_rowstats_plain<Tin>, grid, 256, 0, stream, tl, dl, V, n_units, ws, ep,
+                   status) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
 
-  k_verify<Tin><<<(B + 1) / 2, 64, 0, stream>>>(tl, dl, tokens, uni, B, gamma, V, n_units, ep,
-                                                ws, acc, emitted, probs, tie_ctr, status);
-  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
-
-  const long long items = static_cast<long long>(B) * n_seg;
-  const long long want_sums = (items + 7) / 8;
-  const int sums_grid = static_cast<int>(want_sums < 8LL * sms ? want_sums : 8LL * sms);
-  if (aligned) {
-    k_resample_sums<Tin, true><<<sums_grid, 256, 0, stream>>>(tl, dl, V, n_seg, B, ep, ws);
-    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
-    k_resample_pick<Tin, true><<<B, 256, 0, stream>>>(tl, dl, V, n_seg, gamma, ep, ws, emitted,
-                                                      tie_ctr, status);
-  } else {
-    k_resample_sums<Tin, false><<<sums_grid, 256, 0, stream>>>(tl, dl, V, n_seg, B, ep, ws);
-    if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
-    k_resample_pick<Tin, false><<<B, 256, 0, stream>>>(tl, dl, V, n_seg, gamma, ep, ws, emitted,
-                                                       tie_ctr, status);
-  }
+  const dim3 dgrid(static_cast<unsigned>(B) * kDecideParts);
+  const cudaError_t e =
+      aligned ? launch_pdl(k_decide<Tin, true>, dgrid, kDecideWarps * 32, 0, stream, tl, dl,
+                           tokens, uni, B, gamma, V, n_units, n_seg, ep, ws, acc, emitted, probs,
+                           tie_ctr, status)
+              : launch_pdl(k_decide<Tin, false>, dgrid, kDecideWarps * 32, 0, stream, tl, dl,
+                           tokens, uni, B, gamma, V, n_units, n_seg, ep, ws, acc, emitted, probs,
+                           tie_ctr, status);
+  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }
