@@ -23,11 +23,12 @@
 //               statistics (sum as a float pair, K) go to the workspace. No
 //               double-precision instruction runs per logit: GB300's FP64 rate
 //               is a small fraction of its FP32 rate.
-//   k_decide    kDecideParts CTAs per request. Each merges the unit
-//               statistics of the request's rows in parallel (compensated
-//               float, exact power-of-two alignment), evaluates the ratio
-//               p_t^k(x_k)/p_d^k(x_k) in float -- in double only when the
-//               uniform lies within 2e-6 of it -- and finds the first
+//   k_decide    several CTAs per request, as many as one resident wave holds.
+//               Each loads the tested tokens' logits, merges the unit records
+//               of the request's rows (contiguous; a few threads per row,
+//               compensated float, exact power-of-two alignment), evaluates
+//               the ratio p_t^k(x_k)/p_d^k(x_k) in float -- in double only
+//               when the uniform lies within 2e-6 of it -- and finds the first
 //               rejection with a warp ballot; part 0 writes accepted lengths,
 //               tokens and probabilities. Each part then sums the residual (or
 //               bonus) weights of its share of the 2048-token segments; the
@@ -63,7 +64,9 @@ struct ResampleDesc {
   float u;        // resample uniform
   int32_t mode;   // 0 nothing to do, 1 residual, 2 target distribution
   int32_t m;      // accepted count: position of the sampled token
-  int32_t pad[6];
+  float E_hi;     // residual: D - K_t = E_hi + E_lo, so that p_d/p_t = 2^(z_d*c + E) / e_t
+  float E_lo;
+  int32_t pad[4];
 };
 static_assert(sizeof(ResampleDesc) == 64, "ResampleDesc layout");
 
@@ -517,15 +520,101 @@ __device__ RowStat warp_merge_row(const TileStat* __restrict__ t, int n_units, i
   return r;
 }
 
+// The statistics of nrows consecutive rows (unit records from t0) into
+// sh_rs[0 .. nrows), by the whole CTA: tpr threads per row, each combining
+// every tpr-th unit (four records in flight), then a butterfly over the row's
+// lanes.
+__device__ void merge_rows_block(const TileStat* __restrict__ t0, int nrows, int n_units,
+                                 RowStat* sh_rs) {
+  const int tpr = nrows <= static_cast<int>(blockDim.x) / 8   ? 8
+                  : nrows <= static_cast<int>(blockDim.x) / 4 ? 4
+                                                              : 2;
+  const int tid = threadIdx.x, sub = tid & (tpr - 1);
+  const int per_pass = static_cast<int>(blockDim.x) / tpr;
+  for (int base = 0; base < nrows; base += per_pass) {
+    const int row = base + tid / tpr;
+    int K = INT_MIN;
+    float hi = 0.f, lo = 0.f;
+    bool bad = false;
+    if (row < nrows) {
+      const TileStat* t = t0 + static_cast<long long>(row) * n_units;
+      int u = sub;
+      for (; u + 3 * tpr < n_units; u += 4 * tpr) {
+        const TileStat b0 = t[u], b1 = t[u + tpr], b2 = t[u + 2 * tpr], b3 = t[u + 3 * tpr];
+        bad = bad || (b0.bad | b1.bad | b2.bad | b3.bad) != 0;
+        stat_combine(K, hi, lo, b0.K, b0.s_hi, b0.s_lo);
+        stat_combine(K, hi, lo, b1.K, b1.s_hi, b1.s_lo);
+        stat_combine(K, hi, lo, b2.K, b2.s_hi, b2.s_lo);
+        stat_combine(K, hi, lo, b3.K, b3.s_hi, b3.s_lo);
+      }
+      for (; u < n_units; u += tpr) {
+        const TileStat b = t[u];
+        bad = bad || b.bad != 0;
+        stat_combine(K, hi, lo, b.K, b.s_hi, b.s_lo);
+      }
+    }
+    for (int o = tpr / 2; o > 0; o >>= 1) {  // lanes of a row are an aligned group
+      const int K2 = __shfl_xor_sync(0xFFFFFFFFu, K, o);
+      const float h2 = __shfl_xor_sync(0xFFFFFFFFu, hi, o);
+      const float l2 = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+      bad = (__shfl_xor_sync(0xFFFFFFFFu, bad ? 1 : 0, o) != 0) || bad;
+      stat_combine(K, hi, lo, K2, h2, l2);
+    }
+    if (row < nrows && sub == 0) {
+      RowStat rs;
+      const float sm = hi + lo;
+      rs.S_hi = sm;
+      rs.S_lo = lo - (sm - hi);
+      rs.K = K;
+      rs.ok = !bad && K != INT_MIN && sm > 0.f && isfinite(sm);
+      sh_rs[row] = rs;
+    }
+  }
+}
+
+// Inputs of the ratio test at position k = lane + 1 (and, in lane 0, the
+// uniform of the draw after the block). They do not depend on the row
+// statistics, so they are loaded while those are merged.
+struct RatioIn {
+  int32_t x;      // draft token, clamped into [0, V)
+  float u;        // its uniform
+  float zt, zd;   // target and draft logits at x
+  float u_draw;   // lane 0: the uniform of the token drawn after the block
+  bool bad;       // token or uniform out of range
+};
+
+template <typename Tin>
+__device__ __forceinline__ RatioIn load_ratio_inputs(const Tin* __restrict__ tl,
+                                                     const Tin* __restrict__ dl,
+                                                     const int32_t* __restrict__ tokens,
+                                                     const float* __restrict__ uniforms, int r,
+                                                     int gamma, int V, int start, int ell,
+                                                     const VerifyWs& ws, int lane) {
+  RatioIn in{0, 0.f, 0.f, 0.f, 0.f, false};
+  const int k = lane + 1;
+  if (lane == 0) in.u_draw = uniforms[static_cast<long long>(r) * (gamma + 1) + gamma];
+  if (k <= ell) {
+    int32_t x = tokens[static_cast<long long>(r) * gamma + k - 1];
+    const float u = uniforms[static_cast<long long>(r) * (gamma + 1) + k - 1];
+    in.bad = x < 0 || x >= V || !(u >= 0.f && u < 1.f);
+    x = min(max(x, 0), V - 1);
+    const long long trow = ws.row_list[start + k - 1] >> 1;
+    const long long drow = ws.row_list[start + ell + k] >> 1;
+    in.x = x;
+    in.u = u;
+    in.zt = to_float<Tin>(tl[trow * V + x]);
+    in.zd = to_float<Tin>(dl[drow * V + x]);
+  }
+  return in;
+}
+
 // Ratio tests of request r by one warp (lane k-1 tests position k), from the
 // row statistics in sh_rs (target rows 0..ell, draft rows ell+1..2ell). With
 // write_out it stores accepted_len, the accepted tokens, the probabilities and
 // the near ties of these decisions. Lane 0 writes the descriptor of the token
 // to draw after the block to *d_out.
 template <typename Tin>
-__device__ void ratio_tests(const Tin* __restrict__ tl, const Tin* __restrict__ dl,
-                            const int32_t* __restrict__ tokens, const float* __restrict__ uniforms,
-                            int r, int gamma, int V, int start, const RowStat* sh_rs,
+__device__ void ratio_tests(const RatioIn& in, int r, int gamma, int start, const RowStat* sh_rs,
                             const ExpParams& ep, const VerifyWs& ws, bool write_out,
                             int32_t* __restrict__ accepted_len, int32_t* __restrict__ emitted,
                             float* __restrict__ probs_out, uint32_t* ties, int32_t* status,
@@ -542,16 +631,10 @@ __device__ void ratio_tests(const Tin* __restrict__ tl, const Tin* __restrict__ 
   if (has) {
     st = sh_rs[k - 1];
     sd = sh_rs[ell + k];
-    x = tokens[static_cast<long long>(r) * gamma + k - 1];
-    const float u = uniforms[static_cast<long long>(r) * (gamma + 1) + k - 1];
-    if (x < 0 || x >= V || !(u >= 0.f && u < 1.f) || !st.ok || !sd.ok) {
-      set_status(status, DSPARK_ERR_BAD_DATA);
-      x = min(max(x, 0), V - 1);
-    }
-    const long long trow = ws.row_list[start + k - 1] >> 1;
-    const long long drow = ws.row_list[start + ell + k] >> 1;
-    const float zt = to_float<Tin>(tl[trow * V + x]);
-    const float zd = to_float<Tin>(dl[drow * V + x]);
+    x = in.x;
+    const float u = in.u;
+    if (in.bad || !st.ok || !sd.ok) set_status(status, DSPARK_ERR_BAD_DATA);
+    const float zt = in.zt, zd = in.zd;
     pt = prob_f32(zt, st, ep);
     pd = prob_f32(zd, sd, ep);
     // ratio = 2^((z_t - z_d)*c - (K_t - K_d)) * S_d / S_t (relative error a few 1e-7)
@@ -595,13 +678,14 @@ __device__ void ratio_tests(const Tin* __restrict__ tl, const Tin* __restrict__ 
   if (lane == 0) {
     if (write_out) accepted_len[r] = m;
     ResampleDesc d;
-    d.u = uniforms[static_cast<long long>(r) * (gamma + 1) + gamma];
+    d.u = in.u_draw;
     if (!(d.u >= 0.f && d.u < 1.f)) {
       set_status(status, DSPARK_ERR_BAD_DATA);
       d.u = 0.f;
     }
     d.m = m;
-    for (int i = 0; i < 6; ++i) d.pad[i] = 0;
+    for (int i = 0; i < 4; ++i) d.pad[i] = 0;
+    d.E_hi = d.E_lo = 0.f;
     if (m < ell) {
       d.mode = kModeResidual;
       d.t_row = ws.row_list[start + m] >> 1;
@@ -613,6 +697,9 @@ __device__ void ratio_tests(const Tin* __restrict__ tl, const Tin* __restrict__ 
                             (static_cast<double>(Sd_hi) + Sd_lo));
       d.D_hi = static_cast<float>(D);
       d.D_lo = static_cast<float>(D - static_cast<double>(d.D_hi));
+      const double E = D - static_cast<double>(Kt);
+      d.E_hi = static_cast<float>(E);
+      d.E_lo = static_cast<float>(E - static_cast<double>(d.E_hi));
     } else {
       const RowStat sb = sh_rs[ell];  // the bonus row (position ell + 1)
       if (!sb.ok) set_status(status, DSPARK_ERR_BAD_DATA);
@@ -631,31 +718,49 @@ __device__ void ratio_tests(const Tin* __restrict__ tl, const Tin* __restrict__ 
 // ---------------------------------------------------------------------------
 // Weight of token v, up to a factor common to the whole row:
 //   target mode:   e_t(v) = 2^(z_t*c - K_t)                   (proportional to p_t)
-//   residual mode: e_t(v) * (1 - p_d/p_t)^+                   (proportional to max(0, p_t - p_d))
-// with p_d/p_t = 2^(-d2), d2 = (z_t - z_d)*c - D. Where a token carries much
-// mass and p_d is close to p_t, the factor is -expm1(-d2 ln 2) so that it keeps
-// full relative precision; elsewhere 1 - 2^(-d2) is accurate enough.
-__device__ __forceinline__ float resample_weight(float zt, float zd, int mode, float nK,
-                                                 float D_hi, float D_lo, const ExpParams& ep) {
-  const float e = exp_term(zt, nK, ep);
-  if (mode != kModeResidual) return e;
-  const float dz = zt - zd;
-  const float d2 = fmaf(dz, ep.c_hi, -D_hi) + fmaf(dz, ep.c_lo, -D_lo);
-  if (!(d2 > 0.f)) return 0.f;
-  float f = 1.f - ex2_approx(-d2);
-  if (d2 < 4.f && e > 0.00390625f) f = -expm1f(-d2 * 0.6931471805599453f);  // rare: heavy token
-  return e * f;
+//   residual mode: (e_t(v) - e_d(v))^+, e_d(v) = 2^(z_d*c + E) (proportional to
+//                  max(0, p_t - p_d)), with E = D - K_t.
+// p_d/p_t = 2^(-d2), d2 = (z_t - z_d)*c - D. Where a token carries much mass
+// the difference may cancel; there the weight is e_t * -expm1(-d2 ln 2), which
+// keeps full relative precision.
+struct WeightParams {
+  int mode;
+  float nK;          // -K_t
+  float D_hi, D_lo;  // residual mode
+  float E_hi, E_lo;
+};
+
+__device__ __forceinline__ WeightParams weight_params(const ResampleDesc& d) {
+  return WeightParams{d.mode, -static_cast<float>(d.K_t), d.D_hi, d.D_lo, d.E_hi, d.E_lo};
+}
+
+__device__ __forceinline__ float resample_weight(float zt, float zd, const WeightParams& w,
+                                                 const ExpParams& ep) {
+  const float e = exp_term(zt, w.nK, ep);
+  if (w.mode != kModeResidual) return e;
+  const float ed = ex2_approx(fmaf(zd, ep.c_lo, fmaf(zd, ep.c_hi, w.E_hi)) + w.E_lo);
+  float r = fmaxf(e - ed, 0.f);
+  if (e > 0.00390625f) {  // rare: a heavy token
+    const float dz = zt - zd;
+    const float d2 = fmaf(dz, ep.c_hi, -w.D_hi) + fmaf(dz, ep.c_lo, -w.D_lo);
+    if (!(d2 > 0.f))
+      r = 0.f;
+    else if (d2 < 4.f)
+      r = e * -expm1f(-d2 * 0.6931471805599453f);
+  }
+  return r;
 }
 
 template <typename Tin, bool VEC>
 __device__ void segment_sum(const Tin* __restrict__ zt, const Tin* __restrict__ zd, int a, int b,
-                            int mode, float nK, float D_hi, float D_lo, const ExpParams& ep,
-                            int lane, float& out_hi, float& out_lo) {
+                            const WeightParams& wp, const ExpParams& ep, int lane, float& out_hi,
+                            float& out_lo) {
+  const int mode = wp.mode;
   LaneAcc acc;
   if constexpr (VEC) {
     // NB 16-byte vectors per lane and row are requested before any arithmetic
     constexpr int E = 16 / sizeof(Tin);
-    constexpr int NB = 4;
+    constexpr int NB = 2;
     const uint4* vt = reinterpret_cast<const uint4*>(zt);
     const uint4* vd = reinterpret_cast<const uint4*>(zd);
     const int v_end = b / E;
@@ -675,8 +780,7 @@ __device__ void segment_sum(const Tin* __restrict__ zt, const Tin* __restrict__ 
         float s = 0.f;
 #pragma unroll
         for (int i = 0; i < E; ++i)
-          s += resample_weight(to_float<Tin>(et[i]), to_float<Tin>(ed[i]), mode, nK, D_hi, D_lo,
-                               ep);
+          s += resample_weight(to_float<Tin>(et[i]), to_float<Tin>(ed[i]), wp, ep);
         kahan_add(acc, s);
       }
     }
@@ -684,7 +788,7 @@ __device__ void segment_sum(const Tin* __restrict__ zt, const Tin* __restrict__ 
     for (int i = a + lane; i < b; i += 32) {
       const float z1 = to_float<Tin>(zt[i]);
       const float z2 = mode == kModeResidual ? to_float<Tin>(zd[i]) : z1;
-      kahan_add(acc, resample_weight(z1, z2, mode, nK, D_hi, D_lo, ep));
+      kahan_add(acc, resample_weight(z1, z2, wp, ep));
     }
   }
   float hi = acc.s, lo = -acc.comp;
@@ -697,14 +801,14 @@ __device__ void segment_sum(const Tin* __restrict__ zt, const Tin* __restrict__ 
 // holding u*Z from the segment sums, then the token inside it. Running sums
 // are float pairs (about 48 bits), far finer than the 1e-6*Z near-tie window.
 template <typename Tin, bool VEC>
-__device__ void pick_token(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int V,
+__device__ __noinline__ void pick_token(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int V,
                            int n_seg, int gamma, const ExpParams& ep, const VerifyWs& ws,
                            const ResampleDesc& d, int r, int32_t* __restrict__ emitted,
                            uint32_t* ties, int32_t* status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const Tin* zt = tl + d.t_row * static_cast<long long>(V);
   const Tin* zd = d.mode == kModeResidual ? dl + d.d_row * static_cast<long long>(V) : zt;
-  const float nK = -static_cast<float>(d.K_t);
+  WeightParams wp = weight_params(d);
   ff* seg = ws.seg_sum + static_cast<long long>(r) * n_seg;
 
   __shared__ ff sh_P, sh_Z;
@@ -763,11 +867,11 @@ __device__ void pick_token(const Tin* __restrict__ tl, const Tin* __restrict__ d
     if (sh_Z.hi > 0.f || attempt == 1) break;
     // zero residual mass (only in floating point): sample the target row instead
     mode = kModeTarget;
+    wp.mode = kModeTarget;
     flagged = 1;
     for (int s2 = warp; s2 < n_seg; s2 += 8) {
       float hi, lo;
-      segment_sum<Tin, VEC>(zt, zt, s2 * kSeg, min(V, (s2 + 1) * kSeg), kModeTarget, nK, 0.f, 0.f,
-                            ep, lane, hi, lo);
+      segment_sum<Tin, VEC>(zt, zt, s2 * kSeg, min(V, (s2 + 1) * kSeg), wp, ep, lane, hi, lo);
       if (lane == 0) seg[s2] = ff_norm(hi, lo);
     }
     __syncthreads();
@@ -794,7 +898,7 @@ __device__ void pick_token(const Tin* __restrict__ tl, const Tin* __restrict__ d
     if (i < b) {
       const float z1 = to_float<Tin>(zt[i]);
       const float z2 = mode == kModeResidual ? to_float<Tin>(zd[i]) : z1;
-      w[q] = resample_weight(z1, z2, mode, nK, d.D_hi, d.D_lo, ep);
+      w[q] = resample_weight(z1, z2, wp, ep);
     }
   }
   ff mine = zero;
@@ -851,27 +955,28 @@ __device__ void pick_token(const Tin* __restrict__ tl, const Tin* __restrict__ d
 // ---------------------------------------------------------------------------
 // k_decide: ratio tests, residual / bonus segment sums and the draw, fused
 // ---------------------------------------------------------------------------
-constexpr int kDecideParts = 4;  // CTAs per request: their segment shares balance the grid
 constexpr int kDecideWarps = 8;
+constexpr int kDecideMaxParts = 16;
 
-// kDecideParts CTAs per request. Each one merges the request's row statistics
+// `parts` CTAs per request. Each one merges the request's row statistics
 // and runs the ratio tests (cheap, so every part recomputes them and no part
 // waits for another); part 0 writes the verification outputs. Each part sums
 // the residual (or bonus) weights of its share of the 2048-token segments;
 // the part that finishes last (ticket reset by k_plan) draws the token.
 template <typename Tin, bool VEC>
-__global__ void __launch_bounds__(kDecideWarps * 32) k_decide(
+__global__ void __launch_bounds__(kDecideWarps * 32, 6) k_decide(
     const Tin* __restrict__ tl, const Tin* __restrict__ dl, const int32_t* __restrict__ tokens,
     const float* __restrict__ uniforms, int B, int gamma, int V, int n_units, int n_seg,
-    ExpParams ep, VerifyWs ws, int32_t* __restrict__ accepted_len, int32_t* __restrict__ emitted,
-    float* __restrict__ probs_out, uint32_t* ties, int32_t* status) {
+    int parts, ExpParams ep, VerifyWs ws, int32_t* __restrict__ accepted_len,
+    int32_t* __restrict__ emitted, float* __restrict__ probs_out, uint32_t* ties,
+    int32_t* status) {
   pdl_wait();  // predecessor grid complete, its writes visible
   pdl_trigger();
   __shared__ RowStat sh_rs[2 * DSPARK_MAX_GAMMA + 1];
   __shared__ ResampleDesc sh_d;
   __shared__ int sh_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x / kDecideParts, part = blockIdx.x - r * kDecideParts;
+  const int r = blockIdx.x / parts, part = blockIdx.x - r * parts;
   const bool lead = part == 0;
   const int start = ws.req_row_start[r], end = ws.req_row_start[r + 1];
   if (end == start) {  // invalid request (reported by k_plan): defined, in-bounds outputs
@@ -886,34 +991,35 @@ __global__ void __launch_bounds__(kDecideWarps * 32) k_decide(
     }
     return;
   }
-  // 1. the request's row statistics, warps in parallel
-  for (int row = warp; row < end - start; row += kDecideWarps) {
-    const RowStat rs =
-        warp_merge_row(ws.tiles + static_cast<long long>(start + row) * n_units, n_units, lane);
-    if (lane == 0) sh_rs[row] = rs;
-  }
+  // 0. the tested positions' inputs, in flight during the merge
+  RatioIn rin{};
+  if (warp == 0)
+    rin = load_ratio_inputs<Tin>(tl, dl, tokens, uniforms, r, gamma, V, start,
+                                 (end - start - 1) / 2, ws, lane);
+  // 1. the request's row statistics (its rows' unit records are contiguous)
+  merge_rows_block(ws.tiles + static_cast<long long>(start) * n_units, end - start, n_units,
+                   sh_rs);
   __syncthreads();
   // 2. ratio tests and the first rejection
   if (warp == 0)
-    ratio_tests<Tin>(tl, dl, tokens, uniforms, r, gamma, V, start, sh_rs, ep, ws, lead,
-                     accepted_len, emitted, probs_out, ties, status, &sh_d, lane, end);
+    ratio_tests<Tin>(rin, r, gamma, start, sh_rs, ep, ws, lead, accepted_len, emitted, probs_out,
+                     ties, status, &sh_d, lane, end);
   __syncthreads();
   const ResampleDesc d = sh_d;
   // 3. this part's segment sums of the draw's weights
   const Tin* zt = tl + d.t_row * static_cast<long long>(V);
   const Tin* zd = d.mode == kModeResidual ? dl + d.d_row * static_cast<long long>(V) : zt;
-  const float nK = -static_cast<float>(d.K_t);
-  for (int sg = part * kDecideWarps + warp; sg < n_seg; sg += kDecideParts * kDecideWarps) {
+  const WeightParams wp = weight_params(d);
+  for (int sg = part * kDecideWarps + warp; sg < n_seg; sg += parts * kDecideWarps) {
     float hi, lo;
-    segment_sum<Tin, VEC>(zt, zd, sg * kSeg, min(V, (sg + 1) * kSeg), d.mode, nK, d.D_hi, d.D_lo,
-                          ep, lane, hi, lo);
+    segment_sum<Tin, VEC>(zt, zd, sg * kSeg, min(V, (sg + 1) * kSeg), wp, ep, lane, hi, lo);
     if (lane == 0) ws.seg_sum[static_cast<long long>(r) * n_seg + sg] = ff_norm(hi, lo);
   }
   // 4. the last part to finish draws the token
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    sh_last = atomicAdd(&ws.tickets[r], 1u) == kDecideParts - 1;
+    sh_last = atomicAdd(&ws.tickets[r], 1u) == static_cast<unsigned>(parts) - 1u;
   }
   __syncthreads();
   if (!sh_last) return;
@@ -930,6 +1036,7 @@ constexpr int kStages = 3;
 struct DeviceState {
   bool ready = false;
   int sms = 0;
+  int decide_ctas_per_sm = 1;  // resident k_decide CTAs per SM
 };
 std::mutex g_mutex;
 DeviceState g_devices[128];
@@ -939,7 +1046,7 @@ constexpr size_t tma_smem_bytes() {
          static_cast<size_t>(kStreamWarps) * kStages * sizeof(uint64_t);
 }
 
-int device_setup(int& sms) {
+int device_setup(int& sms, int& decide_per_sm) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return DSPARK_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mutex);
@@ -955,9 +1062,15 @@ int device_setup(int& sms) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(tma_smem_bytes())) != cudaSuccess)
       return DSPARK_ERR_CUDA;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_decide<uint16_t, true>,
+                                                      kDecideWarps * 32, 0) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    s.decide_ctas_per_sm = occ > 0 ? occ : 1;
     s.ready = true;
   }
   sms = s.sms;
+  decide_per_sm = s.decide_ctas_per_sm;
   return DSPARK_OK;
 }
 
@@ -997,8 +1110,8 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
                   const int64_t* toff, const int64_t* doff, int32_t* acc, int32_t* emitted,
                   float* probs, uint32_t* ties, int32_t* status, void* workspace,
                   cudaStream_t stream) {
-  int sms = 0;
-  if (int rc = device_setup(sms)) return rc;
+  int sms = 0, decide_per_sm = 1;
+  if (int rc = device_setup(sms, decide_per_sm)) return rc;
   VerifyWs ws = carve_verify_ws(workspace, B, gamma, V);
   uint32_t* tie_ctr = ties ? ties : &ws.hdr->ties_scratch;
   const ExpParams ep = exp_params(temperature);
@@ -1030,14 +1143,20 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
   }
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
 
-  const dim3 dgrid(static_cast<unsigned>(B) * kDecideParts);
+  // CTAs per request: as many as one wave of resident CTAs holds (at least
+  // one, and no more than there are segments to share)
+  int parts = static_cast<int>(static_cast<long long>(decide_per_sm) * sms / B);
+  parts = parts < 1 ? 1 : (parts > kDecideMaxParts ? kDecideMaxParts : parts);
+  const int seg_groups = (n_seg + kDecideWarps - 1) / kDecideWarps;
+  if (parts > seg_groups) parts = seg_groups;
+  const dim3 dgrid(static_cast<unsigned>(B) * static_cast<unsigned>(parts));
   const cudaError_t e =
       aligned ? launch_pdl(k_decide<Tin, true>, dgrid, kDecideWarps * 32, 0, stream, tl, dl,
-                           tokens, uni, B, gamma, V, n_units, n_seg, ep, ws, acc, emitted, probs,
-                           tie_ctr, status)
+                           tokens, uni, B, gamma, V, n_units, n_seg, parts, ep, ws, acc, emitted,
+                           probs, tie_ctr, status)
               : launch_pdl(k_decide<Tin, false>, dgrid, kDecideWarps * 32, 0, stream, tl, dl,
-                           tokens, uni, B, gamma, V, n_units, n_seg, ep, ws, acc, emitted, probs,
-                           tie_ctr, status);
+                           tokens, uni, B, gamma, V, n_units, n_seg, parts, ep, ws, acc, emitted,
+                           probs, tie_ctr, status);
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
