@@ -46,6 +46,7 @@ extern "C" {
 #endif
 
 struct CUstream_st; /* cudaStream_t / CUstream */
+struct CUevent_st;  /* cudaEvent_t / CUevent */
 
 typedef enum {
   DSPARK_OK = 0,
@@ -224,6 +225,37 @@ int dspark_verify_static(const void* target_logits, const void* draft_logits,
                          int32_t* accepted_len, int32_t* emitted_tokens,
                          float* probs_out, uint32_t* near_tie_count,
                          int32_t* device_status, struct CUstream_st* stream);
+
+/*
+ * dspark_verify_timed -- dspark_verify with per-pass timing events (a
+ * measurement aid; no counterpart in the paper).
+ *
+ * Does exactly the work of dspark_verify and also records, on `stream`:
+ *   events[0] before the planning pass (k_plan),
+ *   events[1] before the streaming pass (k_rowstats),
+ *   events[2] before the decision pass (k_decide: ratio tests, residual sums
+ *             and the draw),
+ *   events[3] after it.
+ * cudaEventElapsedTime(events[i], events[i+1]), after the caller's own
+ * synchronisation, gives the duration of pass i. events points to 4 events
+ * the caller created with timing enabled (cudaEventCreate) and still owns.
+ * Recording between the passes stops a pass's launch from overlapping the end
+ * of the previous one, so the three intervals add up to slightly more than a
+ * dspark_verify call takes.
+ *
+ * Arguments, outputs and error behaviour are those of dspark_verify; a NULL
+ * events pointer or event is DSPARK_ERR_INVALID_ARG.
+ */
+int dspark_verify_timed(const void* target_logits, const void* draft_logits,
+                        const int32_t* draft_tokens, const int32_t* verify_len,
+                        const float* uniforms, float temperature, int32_t dtype,
+                        int32_t B, int32_t gamma, int32_t V,
+                        const int64_t* target_row_off, const int64_t* draft_row_off,
+                        int32_t* accepted_len, int32_t* emitted_tokens,
+                        float* probs_out, uint32_t* near_tie_count,
+                        int32_t* device_status, void* workspace,
+                        size_t workspace_bytes, struct CUstream_st* stream,
+                        struct CUevent_st** events);
 
 #ifdef __cplusplus
 }

@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_CUDA
                 3: "DSPARK_ERR_WORKSPACE", 4: "DSPARK_ERR_TIMEOUT", 5: "DSPARK_ERR_BAD_DATA",
                 6: "DSPARK_ERR_TOO_LARGE"}
 DSPARK_F32, DSPARK_BF16 = 0, 1
-EXPORTED = ("dspark_verify", "dspark_schedule", "dspark_verify_static")
+EXPORTED = ("dspark_verify", "dspark_schedule", "dspark_verify_static", "dspark_verify_timed")
 
 
 class DsparkError(RuntimeError):
@@ -89,6 +89,9 @@ def load(path: Optional[str] = None):
         lib.dspark_verify.restype = ctypes.c_int
         lib.dspark_verify.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp, vp, vp,
                                       vp, vp, vp, vp, sz, vp]
+        lib.dspark_verify_timed.restype = ctypes.c_int
+        lib.dspark_verify_timed.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp, vp,
+                                            vp, vp, vp, vp, vp, sz, vp, vp]
         lib.dspark_verify_static.restype = ctypes.c_int
         lib.dspark_verify_static.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp,
                                              vp, vp, vp, vp, vp, vp]
@@ -139,13 +142,16 @@ def dspark_verify(target_logits: torch.Tensor, draft_logits: torch.Tensor,
                   draft_tokens: torch.Tensor, verify_len: torch.Tensor, uniforms: torch.Tensor,
                   temperature: float, target_row_off: Optional[torch.Tensor] = None,
                   draft_row_off: Optional[torch.Tensor] = None, *, with_probs: bool = True,
-                  buffers: Optional[VerifyBuffers] = None, stream=None, check: bool = False) -> dict:
+                  buffers: Optional[VerifyBuffers] = None, stream=None, check: bool = False,
+                  events=None) -> dict:
     """Batched speculative verification through libdspark (see include/dspark.h).
 
     Returns a dict of device tensors: accepted_len [B] int32, emitted_tokens
     [B, gamma+1] int32, probs [B, gamma, 2] float32 (or None), near_tie_count
     [1], device_status [1]. With check=True the call synchronises and raises on
-    a non-OK device status."""
+    a non-OK device status. With events (four torch.cuda.Event made with
+    enable_timing=True) the call goes through dspark_verify_timed, which records
+    them around the planning, streaming and decision passes."""
     dev = target_logits.device
     if target_logits.dtype == torch.bfloat16:
         dtype = DSPARK_BF16
@@ -173,16 +179,25 @@ def dspark_verify(target_logits: torch.Tensor, draft_logits: torch.Tensor,
     if (buf.B, buf.gamma, buf.V) != (B, gamma, V):
         raise ValueError("buffers were made for another shape")
     lib = load()
-    with torch.cuda.device(dev):
-        rc = lib.dspark_verify(
-            _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(verify_len),
+    args = (_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(verify_len),
             _ptr(uniforms), float(temperature), dtype, B, gamma, V, _ptr(target_row_off),
             _ptr(draft_row_off), _ptr(buf.accepted_len), _ptr(buf.emitted_tokens),
             _ptr(buf.probs if with_probs else None), _ptr(buf.near_tie_count),
-            _ptr(buf.device_status), _ptr(buf.workspace), buf.workspace.numel(),
-            _stream_handle(stream))
+            _ptr(buf.device_status), _ptr(buf.workspace), buf.workspace.numel())
+    with torch.cuda.device(dev):
+        s = _stream_handle(stream)
+        if events is None:
+            rc = lib.dspark_verify(*args, s)
+        else:
+            if len(events) != 4:
+                raise ValueError("events must hold four torch.cuda.Event")
+            st = stream if stream is not None else torch.cuda.current_stream(dev)
+            for e in events:  # a torch event's handle exists once it has been recorded
+                e.record(st)
+            handles = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+            rc = lib.dspark_verify_timed(*args, s, handles)
     if rc != 0:
-        raise DsparkError("dspark_verify", rc)
+        raise DsparkError("dspark_verify_timed" if events is not None else "dspark_verify", rc)
     out = {"accepted_len": buf.accepted_len, "emitted_tokens": buf.emitted_tokens,
            "probs": buf.probs if with_probs else None, "near_tie_count": buf.near_tie_count,
            "device_status": buf.device_status}

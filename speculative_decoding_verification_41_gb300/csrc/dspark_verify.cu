@@ -1109,7 +1109,7 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
                   const float* uni, float temperature, int B, int gamma, int V,
                   const int64_t* toff, const int64_t* doff, int32_t* acc, int32_t* emitted,
                   float* probs, uint32_t* ties, int32_t* status, void* workspace,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, cudaEvent_t* ev) {
   int sms = 0, decide_per_sm = 1;
   if (int rc = device_setup(sms, decide_per_sm)) return rc;
   VerifyWs ws = carve_verify_ws(workspace, B, gamma, V);
@@ -1119,10 +1119,17 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
   const int n_units = (V + unit_elems - 1) / unit_elems;
   const int n_seg = (V + kSeg - 1) / kSeg;
 
+  if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   if (launch_pdl(k_plan, 1, 1024, 0, stream, vlen, toff, doff, B, gamma, ws, tie_ctr, status) !=
       cudaSuccess)
     return DSPARK_ERR_CUDA;
-  if (B == 0) return DSPARK_OK;
+  if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (B == 0) {
+    if (ev && (cudaEventRecord(ev[2], stream) != cudaSuccess ||
+               cudaEventRecord(ev[3], stream) != cudaSuccess))
+      return DSPARK_ERR_CUDA;
+    return DSPARK_OK;
+  }
 
   const bool aligned = (static_cast<size_t>(V) * sizeof(Tin)) % 16 == 0 &&
                        reinterpret_cast<uintptr_t>(tl) % 16 == 0 &&
@@ -1142,6 +1149,7 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
       return DSPARK_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
 
   // CTAs per request: as many as one wave of resident CTAs holds (at least
   // one, and no more than there are segments to share)
@@ -1159,21 +1167,22 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
                            probs, tie_ctr, status);
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[3], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
 }
 
 }  // namespace dspark
 
-extern "C" int dspark_verify(const void* target_logits, const void* draft_logits,
-                             const int32_t* draft_tokens, const int32_t* verify_len,
-                             const float* uniforms, float temperature, int32_t dtype, int32_t B,
-                             int32_t gamma, int32_t V, const int64_t* target_row_off,
-                             const int64_t* draft_row_off, int32_t* accepted_len,
-                             int32_t* emitted_tokens, float* probs_out,
-                             uint32_t* near_tie_count, int32_t* device_status, void* workspace,
-                             size_t workspace_bytes, struct CUstream_st* stream) {
-  using namespace dspark;
-  // B indexes a grid dimension of the resample pass; V keeps segment offsets in int
+namespace dspark {
+
+int verify_entry(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                 const int32_t* verify_len, const float* uniforms, float temperature,
+                 int32_t dtype, int32_t B, int32_t gamma, int32_t V,
+                 const int64_t* target_row_off, const int64_t* draft_row_off,
+                 int32_t* accepted_len, int32_t* emitted_tokens, float* probs_out,
+                 uint32_t* near_tie_count, int32_t* device_status, void* workspace,
+                 size_t workspace_bytes, cudaStream_t s, cudaEvent_t* ev) {
+  // B times the CTAs per request indexes a grid dimension; V keeps segment offsets in int
   if (B < 0 || B > 65535 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || V < 1 || V > (1 << 30))
     return DSPARK_ERR_INVALID_ARG;
   if (!(temperature > 0.0f) || !std::isfinite(temperature)) return DSPARK_ERR_INVALID_ARG;
@@ -1186,18 +1195,55 @@ extern "C" int dspark_verify(const void* target_logits, const void* draft_logits
   if (!workspace || workspace_bytes < DSPARK_VERIFY_WS_BYTES(B, gamma, V) ||
       reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
     return DSPARK_ERR_WORKSPACE;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == DSPARK_BF16)
     return launch_verify<uint16_t>(
         static_cast<const uint16_t*>(target_logits), static_cast<const uint16_t*>(draft_logits),
         draft_tokens, verify_len, uniforms, temperature, B, gamma, V, target_row_off,
         draft_row_off, accepted_len, emitted_tokens, probs_out, near_tie_count, device_status,
-        workspace, s);
+        workspace, s, ev);
   return launch_verify<float>(static_cast<const float*>(target_logits),
                               static_cast<const float*>(draft_logits), draft_tokens, verify_len,
                               uniforms, temperature, B, gamma, V, target_row_off, draft_row_off,
                               accepted_len, emitted_tokens, probs_out, near_tie_count,
-                              device_status, workspace, s);
+                              device_status, workspace, s, ev);
+}
+
+}  // namespace dspark
+
+extern "C" int dspark_verify(const void* target_logits, const void* draft_logits,
+                             const int32_t* draft_tokens, const int32_t* verify_len,
+                             const float* uniforms, float temperature, int32_t dtype, int32_t B,
+                             int32_t gamma, int32_t V, const int64_t* target_row_off,
+                             const int64_t* draft_row_off, int32_t* accepted_len,
+                             int32_t* emitted_tokens, float* probs_out,
+                             uint32_t* near_tie_count, int32_t* device_status, void* workspace,
+                             size_t workspace_bytes, struct CUstream_st* stream) {
+  return dspark::verify_entry(target_logits, draft_logits, draft_tokens, verify_len, uniforms,
+                              temperature, dtype, B, gamma, V, target_row_off, draft_row_off,
+                              accepted_len, emitted_tokens, probs_out, near_tie_count,
+                              device_status, workspace, workspace_bytes,
+                              reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" int dspark_verify_timed(const void* target_logits, const void* draft_logits,
+                                   const int32_t* draft_tokens, const int32_t* verify_len,
+                                   const float* uniforms, float temperature, int32_t dtype,
+                                   int32_t B, int32_t gamma, int32_t V,
+                                   const int64_t* target_row_off, const int64_t* draft_row_off,
+                                   int32_t* accepted_len, int32_t* emitted_tokens,
+                                   float* probs_out, uint32_t* near_tie_count,
+                                   int32_t* device_status, void* workspace,
+                                   size_t workspace_bytes, struct CUstream_st* stream,
+                                   struct CUevent_st** events) {
+  if (!events) return DSPARK_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i)
+    if (!events[i]) return DSPARK_ERR_INVALID_ARG;
+  cudaEvent_t ev[4] = {events[0], events[1], events[2], events[3]};
+  return dspark::verify_entry(target_logits, draft_logits, draft_tokens, verify_len, uniforms,
+                              temperature, dtype, B, gamma, V, target_row_off, draft_row_off,
+                              accepted_len, emitted_tokens, probs_out, near_tie_count,
+                              device_status, workspace, workspace_bytes,
+                              reinterpret_cast<cudaStream_t>(stream), ev);
 }
 
 // ---------------------------------------------------------------------------

@@ -93,3 +93,17 @@ def test_schedule_rejects_bad_arguments_on_host(lib):
     assert call(4, 4, 21, conf=None) == 1
     assert call(4, 4, 21, ws=None) == 3
     assert call(4, 4, 21, wsb=10) == 3
+
+
+def test_timed_verify_rejects_missing_events_on_host(lib):
+    p = ctypes.c_void_p
+    args = [p(1), p(1), p(1), p(1), p(1), 1.0, 1, 4, 4, 32, None, None, p(1), p(1), None, None,
+            p(1), p(256), 1 << 30, None]
+    assert lib.dspark_verify_timed(*args, None) == 1
+    some_null = (ctypes.c_void_p * 4)(1, 1, None, 1)
+    assert lib.dspark_verify_timed(*args, some_null) == 1
+    # the timed entry runs the same host checks as dspark_verify
+    good_events = (ctypes.c_void_p * 4)(1, 1, 1, 1)
+    bad = list(args)
+    bad[8] = 33  # gamma
+    assert lib.dspark_verify_timed(*bad, good_events) == 1

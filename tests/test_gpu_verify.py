@@ -150,6 +150,20 @@ def test_repeated_calls_are_deterministic(dev):
         assert torch.equal(a[k], b[k]), k
 
 
+def test_timed_entry_matches_plain_call(dev):
+    vi = workloads.make_verify(24, 16, 30000, torch.bfloat16, 0.7, rho=(0.6, 0.95), seed=5,
+                               device=dev)
+    bufs = binding.VerifyBuffers(24, 16, 30000, dev)
+    a = {k: v.clone() for k, v in run(vi, buffers=bufs).items() if v is not None}
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    b = run(vi, buffers=bufs, events=ev)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    passes = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+    assert all(t > 0 for t in passes), passes
+
+
 # ---------------------------------------------------------------------------
 # the named workloads at full size (bench launch configuration)
 # ---------------------------------------------------------------------------
