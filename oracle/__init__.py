@@ -67,6 +67,10 @@ def _setup(lib):
     lib.oracle_schedule.argtypes = [
         ctypes.POINTER(ctypes.c_float), c_f64p, ctypes.c_int64, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_int32, c_i32p, c_f64p, c_i64p, c_i32p]
+    lib.oracle_schedule_topk.restype = ctypes.c_int
+    lib.oracle_schedule_topk.argtypes = [
+        ctypes.POINTER(ctypes.c_float), ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, c_i32p,
+        c_i64p]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     return lib
@@ -174,6 +178,21 @@ def schedule(confidences, step_time, early_stop=True, lib=None):
         raise OracleError(f"oracle_schedule returned {rc}")
     return {"verify_len": ell, "theta_best": theta.value, "n_admitted": n_adm.value,
             "near_ties": ties.value}
+
+
+def schedule_topk(confidences, K: int, lib=None):
+    """Top-K admission of the production scheduler: the first min(K, |E|)
+    candidates in Algorithm 1's order. Returns dict: verify_len [R], n_admitted."""
+    lib = lib or load()
+    c = np.ascontiguousarray(confidences, dtype=np.float32)
+    R, gamma = c.shape
+    ell = np.zeros(R, np.int32)
+    n_adm = ctypes.c_int64(0)
+    rc = lib.oracle_schedule_topk(_ptr(c, ctypes.c_float), R, gamma, int(K),
+                                  _ptr(ell, ctypes.c_int32), ctypes.byref(n_adm))
+    if rc != 0:
+        raise OracleError(f"oracle_schedule_topk returned {rc}")
+    return {"verify_len": ell, "n_admitted": n_adm.value}
 
 
 def max_threads(lib=None) -> int:

@@ -396,6 +396,53 @@ int oracle_schedule(const float* confidences, const double* step_time,
   return ORACLE_OK;
 }
 
+/*
+ * Dynamic top-K admission of the production scheduler ("DSpark: Confidence-
+ * Scheduled Speculative Decoding with Semi-Autoregressive Generation", section
+ * 5.2, "Hardware-Aware Prefix Scheduler in Practice"). The candidates are
+ * ranked by their current prefix survival probabilities exactly as in
+ * Algorithm 1 (a_{r,j} = prod_{i<=j} c_{r,i} multiplied left to right; E = the
+ * positive ones, descending, equal values in flattened order), and the first
+ * min(K, |E|) of them are admitted. The capacity K itself comes from the
+ * unconstrained global search (oracle_schedule with early_stop = 0) over the
+ * confidences of two steps before. l_r = the number of admitted positions of
+ * request r: a prefix, because a_{r,j} does not increase with j.
+ */
+int oracle_schedule_topk(const float* confidences, int32_t R, int32_t gamma, int64_t K,
+                         int32_t* verify_len, int64_t* n_admitted) {
+  if (!confidences || !verify_len || R < 1 || gamma < 1 || K < 0) return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < (int64_t)R * gamma; ++i) {
+    const float c = confidences[i];
+    if (!(c >= 0.0f && c <= 1.0f)) return ORACLE_ERR_DATA;
+  }
+  const int64_t n = (int64_t)R * gamma;
+  candidate* E = (candidate*)malloc(sizeof(candidate) * (size_t)n);
+  if (!E) return ORACLE_ERR_NOMEM;
+  int64_t nE = 0;
+  for (int32_t r = 0; r < R; ++r) {
+    double prod = 1.0;
+    for (int32_t j = 0; j < gamma; ++j) {
+      prod *= (double)confidences[(int64_t)r * gamma + j];
+      if (prod > 0.0) {
+        E[nE].a = prod;
+        E[nE].flat = (int64_t)r * gamma + j;
+        ++nE;
+      }
+    }
+  }
+  qsort(E, (size_t)nE, sizeof(candidate), candidate_cmp);
+  const int64_t admit = K < nE ? K : nE;
+  for (int32_t r = 0; r < R; ++r) verify_len[r] = 0;
+  for (int64_t i = 0; i < admit; ++i) {
+    const int32_t r = (int32_t)(E[i].flat / gamma);
+    const int32_t j = (int32_t)(E[i].flat % gamma) + 1;
+    if (j > verify_len[r]) verify_len[r] = j;
+  }
+  if (n_admitted) *n_admitted = admit;
+  free(E);
+  return ORACLE_OK;
+}
+
 /* Number of OpenMP threads the oracle can use (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP
