@@ -290,6 +290,18 @@ typedef struct {
   int64_t flat; /* flattened index r*gamma + (j-1)     */
 } candidate;
 
+/* Prefix survival probabilities a_{r,j} = prod_{i<=j} c_{r,i}, multiplied left
+   to right in double (section 3.2.2), into a[r*gamma + j]. */
+static void survival_products(const float* confidences, int32_t R, int32_t gamma, double* a) {
+  for (int32_t r = 0; r < R; ++r) {
+    double prod = 1.0;
+    for (int32_t j = 0; j < gamma; ++j) {
+      prod *= (double)confidences[(int64_t)r * gamma + j];
+      a[(int64_t)r * gamma + j] = prod;
+    }
+  }
+}
+
 /* Descending by a; equal a keeps ascending flattened index (a stable sort of
    the flattened candidate list). */
 static int candidate_cmp(const void* pa, const void* pb) {
@@ -335,13 +347,7 @@ int oracle_schedule(const float* confidences, const double* step_time,
     free(ell);
     return ORACLE_ERR_NOMEM;
   }
-  for (int32_t r = 0; r < R; ++r) {
-    double prod = 1.0;
-    for (int32_t j = 0; j < gamma; ++j) {
-      prod *= (double)confidences[(int64_t)r * gamma + j];
-      a[(int64_t)r * gamma + j] = prod;
-    }
-  }
+  survival_products(confidences, R, gamma, a);
 
   /* candidate space E = {(r,j) : a_{r,j} > 0}, sorted by a descending */
   int64_t nE = 0;
@@ -416,20 +422,21 @@ int oracle_schedule_topk(const float* confidences, int32_t R, int32_t gamma, int
     if (!(c >= 0.0f && c <= 1.0f)) return ORACLE_ERR_DATA;
   }
   const int64_t n = (int64_t)R * gamma;
+  double* a = (double*)malloc(sizeof(double) * (size_t)n);
   candidate* E = (candidate*)malloc(sizeof(candidate) * (size_t)n);
-  if (!E) return ORACLE_ERR_NOMEM;
-  int64_t nE = 0;
-  for (int32_t r = 0; r < R; ++r) {
-    double prod = 1.0;
-    for (int32_t j = 0; j < gamma; ++j) {
-      prod *= (double)confidences[(int64_t)r * gamma + j];
-      if (prod > 0.0) {
-        E[nE].a = prod;
-        E[nE].flat = (int64_t)r * gamma + j;
-        ++nE;
-      }
-    }
+  if (!a || !E) {
+    free(a);
+    free(E);
+    return ORACLE_ERR_NOMEM;
   }
+  survival_products(confidences, R, gamma, a);
+  int64_t nE = 0;
+  for (int64_t i = 0; i < n; ++i)
+    if (a[i] > 0.0) {
+      E[nE].a = a[i];
+      E[nE].flat = i;
+      ++nE;
+    }
   qsort(E, (size_t)nE, sizeof(candidate), candidate_cmp);
   const int64_t admit = K < nE ? K : nE;
   for (int32_t r = 0; r < R; ++r) verify_len[r] = 0;
@@ -439,6 +446,7 @@ int oracle_schedule_topk(const float* confidences, int32_t R, int32_t gamma, int
     if (j > verify_len[r]) verify_len[r] = j;
   }
   if (n_admitted) *n_admitted = admit;
+  free(a);
   free(E);
   return ORACLE_OK;
 }
