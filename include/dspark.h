@@ -186,6 +186,52 @@ int dspark_schedule(const float* confidences, const double* step_time_ms,
                     void* workspace, size_t workspace_bytes,
                     struct CUstream_st* stream);
 
+/*
+ * dspark_schedule_capacity -- the production scheduler's capacity (DSpark
+ * paper, section 5.2, "Hardware-Aware Prefix Scheduler in Practice").
+ *
+ * The same candidate order and Theta as dspark_schedule, without the
+ * early-stopping break: n* = the first n in 0..|E| that maximises
+ * Theta(n) = tau(n) / T(R + n), which steps over jagged drops of T. A serving
+ * loop computes it from the confidences of two steps before and uses it as
+ * the capacity K of dspark_schedule_topk, so that the admission of the current
+ * step never waits for the search and the search never sees the current
+ * step's tokens.
+ *
+ * Arguments are those of dspark_schedule, plus
+ *   capacity      out [1] int32 (device, required): n*.
+ *   verify_len    out [R] int32: the lengths of the best prefix itself.
+ *   theta_best    out [1] float64 or NULL: Theta(n*).
+ *   near_tie_count out [1] or NULL: admissions whose Theta lies within 1e-9
+ *                 (relative) of the best before them.
+ * Errors as in dspark_schedule; a NULL capacity is DSPARK_ERR_INVALID_ARG.
+ */
+int dspark_schedule_capacity(const float* confidences, const double* step_time_ms,
+                             int64_t n_profile, int32_t R, int32_t gamma, int32_t* capacity,
+                             int32_t* verify_len, double* theta_best,
+                             uint32_t* near_tie_count, int32_t* device_status,
+                             void* workspace, size_t workspace_bytes,
+                             struct CUstream_st* stream);
+
+/*
+ * dspark_schedule_topk -- the production scheduler's admission (DSpark paper,
+ * section 5.2): the candidates of the current confidences in the order of
+ * dspark_schedule, the first min(K, |E|) of them admitted, K = *capacity read
+ * on the device (typically written by an earlier dspark_schedule_capacity on
+ * the same stream). l_r = the number of admitted positions of request r (a
+ * prefix, since a_{r,j} does not increase with j).
+ *
+ * Arguments
+ *   confidences   [R][gamma] float32, each in [0, 1].
+ *   capacity      [1] int32 device (required); a negative value sets
+ *                 DSPARK_ERR_BAD_DATA and admits nothing.
+ *   R, gamma, verify_len, device_status, workspace, workspace_bytes, stream
+ *                 as in dspark_schedule (same workspace size).
+ */
+int dspark_schedule_topk(const float* confidences, const int32_t* capacity, int32_t R,
+                         int32_t gamma, int32_t* verify_len, int32_t* device_status,
+                         void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
 /* Size of the library-owned scratch array behind dspark_verify_static. */
 #define DSPARK_STATIC_WS_BYTES ((size_t)16u << 20)
 

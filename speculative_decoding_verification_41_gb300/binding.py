@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_CUDA
                 3: "DSPARK_ERR_WORKSPACE", 4: "DSPARK_ERR_TIMEOUT", 5: "DSPARK_ERR_BAD_DATA",
                 6: "DSPARK_ERR_TOO_LARGE"}
 DSPARK_F32, DSPARK_BF16 = 0, 1
-EXPORTED = ("dspark_verify", "dspark_schedule", "dspark_verify_static", "dspark_verify_timed")
+EXPORTED = ("dspark_verify", "dspark_schedule", "dspark_schedule_capacity",
+            "dspark_schedule_topk", "dspark_verify_static", "dspark_verify_timed")
 
 
 class DsparkError(RuntimeError):
@@ -97,6 +98,11 @@ def load(path: Optional[str] = None):
                                              vp, vp, vp, vp, vp, vp]
         lib.dspark_schedule.restype = ctypes.c_int
         lib.dspark_schedule.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+        lib.dspark_schedule_capacity.restype = ctypes.c_int
+        lib.dspark_schedule_capacity.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp, vp, vp, vp, sz,
+                                                 vp]
+        lib.dspark_schedule_topk.restype = ctypes.c_int
+        lib.dspark_schedule_topk.argtypes = [vp, vp, i32, i32, vp, vp, vp, sz, vp]
         if path is None:
             _lib = lib
         return lib
@@ -213,6 +219,7 @@ class ScheduleBuffers:
     def __init__(self, R: int, gamma: int, device):
         dev = torch.device(device)
         self.R, self.gamma = R, gamma
+        self.capacity = torch.zeros(1, dtype=torch.int32, device=dev)
         self.verify_len = torch.empty(R, dtype=torch.int32, device=dev)
         self.theta_best = torch.empty(1, dtype=torch.float64, device=dev)
         self.near_tie_count = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -239,11 +246,60 @@ def dspark_schedule(confidences: torch.Tensor, step_time_ms: torch.Tensor, *,
                                  _ptr(buf.workspace), buf.workspace.numel(), _stream_handle(stream))
     if rc != 0:
         raise DsparkError("dspark_schedule", rc)
-    out = {"verify_len": buf.verify_len, "theta_best": buf.theta_best,
+    return _schedule_out(buf, dev, check, "dspark_schedule")
+
+
+def _schedule_out(buf, dev, check, name):
+    out = {"verify_len": buf.verify_len, "theta_best": buf.theta_best, "capacity": buf.capacity,
            "near_tie_count": buf.near_tie_count, "device_status": buf.device_status}
     if check:
         torch.cuda.synchronize(dev)
         st = int(buf.device_status.item())
         if st != 0:
-            raise DsparkError("dspark_schedule (device)", st)
+            raise DsparkError(f"{name} (device)", st)
     return out
+
+
+def dspark_schedule_capacity(confidences: torch.Tensor, step_time_ms: torch.Tensor, *,
+                             buffers: Optional[ScheduleBuffers] = None, stream=None,
+                             check: bool = False) -> dict:
+    """Production scheduler, capacity (section 5.2): the global search without the
+    early-stopping break. Returns capacity [1] int32 (n*), verify_len [R] of the
+    best prefix, theta_best, near_tie_count, device_status (device tensors)."""
+    dev = confidences.device
+    _require_cuda("confidences", confidences, torch.float32)
+    _require_cuda("step_time_ms", step_time_ms, torch.float64, dev)
+    R, gamma = confidences.shape
+    buf = buffers or ScheduleBuffers(R, gamma, dev)
+    lib = load()
+    with torch.cuda.device(dev):
+        rc = lib.dspark_schedule_capacity(
+            _ptr(confidences), _ptr(step_time_ms), step_time_ms.numel(), R, gamma,
+            _ptr(buf.capacity), _ptr(buf.verify_len), _ptr(buf.theta_best),
+            _ptr(buf.near_tie_count), _ptr(buf.device_status), _ptr(buf.workspace),
+            buf.workspace.numel(), _stream_handle(stream))
+    if rc != 0:
+        raise DsparkError("dspark_schedule_capacity", rc)
+    return _schedule_out(buf, dev, check, "dspark_schedule_capacity")
+
+
+def dspark_schedule_topk(confidences: torch.Tensor, capacity: torch.Tensor, *,
+                         buffers: Optional[ScheduleBuffers] = None, stream=None,
+                         check: bool = False) -> dict:
+    """Production scheduler, admission (section 5.2): the first min(K, |E|)
+    candidates of the current confidences, K = capacity[0] read on the device.
+    Returns verify_len [R] and device_status (device tensors)."""
+    dev = confidences.device
+    _require_cuda("confidences", confidences, torch.float32)
+    _require_cuda("capacity", capacity, torch.int32, dev)
+    R, gamma = confidences.shape
+    buf = buffers or ScheduleBuffers(R, gamma, dev)
+    lib = load()
+    with torch.cuda.device(dev):
+        rc = lib.dspark_schedule_topk(_ptr(confidences), _ptr(capacity), R, gamma,
+                                      _ptr(buf.verify_len), _ptr(buf.device_status),
+                                      _ptr(buf.workspace), buf.workspace.numel(),
+                                      _stream_handle(stream))
+    if rc != 0:
+        raise DsparkError("dspark_schedule_topk", rc)
+    return _schedule_out(buf, dev, check, "dspark_schedule_topk")

@@ -78,10 +78,70 @@ __device__ __forceinline__ double block_sum_excl(double v, double* sh, double& t
   return before;
 }
 
+// Scheduling modes shared by the sweep and the one-CTA path:
+//   kModeStop     Algorithm 1: stop at the first Theta(n) <= Theta(n-1)
+//   kModeGlobal   section 5.2: no break; n* = the first maximum of Theta(n)
+//                 over n = 0..|E| (the capacity K of the next steps)
+//   kModeTopK     section 5.2: admit the first min(K, |E|) candidates, K read
+//                 from device memory
+enum { kModeStop = 0, kModeGlobal = 1, kModeTopK = 2 };
+
+// A prefix of the sorted candidates as a point of the global search:
+// Theta = tau / t with t = T(R + m); m < 0 marks "none".
+struct Cand {
+  double tau, t;
+  int m;
+};
+
+// a precedes b in the sorted order; the first maximum of Theta wins (compared
+// by cross-multiplication: both t are positive)
+__device__ __forceinline__ Cand cand_pick(const Cand& a, const Cand& b) {
+  if (b.m < 0) return a;
+  if (a.m < 0) return b;
+  return b.tau * a.t > a.tau * b.t ? b : a;
+}
+
+__device__ __forceinline__ Cand shfl_up_cand(const Cand& v, int o) {
+  return Cand{__shfl_up_sync(0xFFFFFFFFu, v.tau, o), __shfl_up_sync(0xFFFFFFFFu, v.t, o),
+              __shfl_up_sync(0xFFFFFFFFu, v.m, o)};
+}
+
+// Exclusive scan of v over the block in thread order under cand_pick (sh: 32
+// slots of shared memory). Every thread must call it.
+__device__ Cand block_excl_pick(const Cand& v, Cand* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const Cand none{0.0, 1.0, -1};
+  Cand incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const Cand t = shfl_up_cand(incl, o);
+    if (lane >= o) incl = cand_pick(t, incl);
+  }
+  Cand ex = shfl_up_cand(incl, 1);
+  if (lane == 0) ex = none;
+  if (lane == 31) sh[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    Cand w = lane < static_cast<int>(blockDim.x >> 5) ? sh[lane] : none;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const Cand t = shfl_up_cand(w, o);
+      if (lane >= o) w = cand_pick(t, w);
+    }
+    sh[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const Cand before = warp > 0 ? sh[warp - 1] : none;
+  const Cand r = cand_pick(before, ex);
+  __syncthreads();  // sh is free again
+  return r;
+}
+
 __global__ void __launch_bounds__(kSchedThreads, 1)
     k_schedule(const float* __restrict__ conf, const double* __restrict__ T, int R, int gamma,
                int32_t* __restrict__ verify_len, double* theta_out, uint32_t* ties,
-               int32_t* status, SchedWs gws, int use_smem) {
+               int32_t* status, SchedWs gws, int use_smem, int mode, const int32_t* K_in,
+               int32_t* K_out) {
   pdl_wait();  // predecessor grid complete, its writes visible
   pdl_trigger();
   extern __shared__ __align__(16) unsigned char smem[];
@@ -89,6 +149,8 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
   __shared__ int red_i[32];
   __shared__ int sh_n_break, sh_nE;
   __shared__ unsigned sh_ties;
+  __shared__ Cand sh_cand[32];
+  __shared__ int sh_nstar;
   const int n = R * gamma;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   u64* kA = gws.keysA;
@@ -103,7 +165,7 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
   }
   if (tid == 0) {
     *status = DSPARK_OK;
-    *ties = 0;
+    if (ties) *ties = 0;
     sh_n_break = INT_MAX;
     sh_nE = 0;
     sh_ties = 0;
@@ -133,8 +195,9 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     gws.ell[r] = 0;
   }
   // profile entries that can be looked up must be positive and finite
-  for (int b = R + tid; b <= R * (gamma + 1); b += kSchedThreads)
-    if (!(T[b] > 0.0) || !isfinite(T[b])) set_status(status, DSPARK_ERR_BAD_DATA);
+  if (T)
+    for (int b = R + tid; b <= R * (gamma + 1); b += kSchedThreads)
+      if (!(T[b] > 0.0) || !isfinite(T[b])) set_status(status, DSPARK_ERR_BAD_DATA);
   __syncthreads();
 
   // 2. stable descending merge of the per-request runs
@@ -191,28 +254,29 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
   }
   __syncthreads();
 
-  // 4. first non-improving admission
-  int first = INT_MAX;
-  for (int m = 1 + tid; m <= nE; m += kSchedThreads) {
-    const double tau_m = tau[m - 1];
-    const double tau_p = m == 1 ? static_cast<double>(R) : tau[m - 2];
-    if (!(tau_m * T[R + m - 1] > tau_p * T[R + m])) first = min(first, m);
-  }
+  int n_star;
+  if (mode == kModeStop) {
+    // 4. first non-improving admission
+    int first = INT_MAX;
+    for (int m = 1 + tid; m <= nE; m += kSchedThreads) {
+      const double tau_m = tau[m - 1];
+      const double tau_p = m == 1 ? static_cast<double>(R) : tau[m - 2];
+      if (!(tau_m * T[R + m - 1] > tau_p * T[R + m])) first = min(first, m);
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xFFFFFFFFu, first, o));
-  if (lane == 0) red_i[warp] = first;
-  __syncthreads();
-  if (warp == 0) {
-    int f = red_i[lane];
+    for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xFFFFFFFFu, first, o));
+    if (lane == 0) red_i[warp] = first;
+    __syncthreads();
+    if (warp == 0) {
+      int f = red_i[lane];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) f = min(f, __shfl_xor_sync(0xFFFFFFFFu, f, o));
-    if (lane == 0) sh_n_break = f;
-  }
-  __syncthreads();
-  const int n_break = sh_n_break;  // INT_MAX: every admission improved
-  const int n_star = n_break <= nE ? n_break - 1 : nE;
-  // near ties among the comparisons actually evaluated (steps 1..min(n_break, nE))
-  {
+      for (int o = 16; o > 0; o >>= 1) f = min(f, __shfl_xor_sync(0xFFFFFFFFu, f, o));
+      if (lane == 0) sh_n_break = f;
+    }
+    __syncthreads();
+    const int n_break = sh_n_break;  // INT_MAX: every admission improved
+    n_star = n_break <= nE ? n_break - 1 : nE;
+    // near ties among the comparisons actually evaluated (steps 1..min(n_break, nE))
     const int last = min(n_break, nE);
     unsigned t = 0;
     for (int m = 1 + tid; m <= last; m += kSchedThreads) {
@@ -224,6 +288,32 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
     }
     t = warp_sum_u32(t);
     if (lane == 0 && t) atomicAdd(&sh_ties, t);
+  } else if (mode == kModeGlobal) {
+    // 4'. first maximum of Theta over n = 0..|E|: chunk bests, their exclusive
+    // scan, then every admission against the best before it
+    const int gc = (nE + kSchedThreads - 1) / kSchedThreads;
+    const int g0 = min(tid * gc, nE), g1 = min(g0 + gc, nE);
+    Cand loc{0.0, 1.0, -1};
+    for (int m = g0 + 1; m <= g1; ++m) loc = cand_pick(loc, Cand{tau[m - 1], T[R + m], m});
+    Cand run = cand_pick(Cand{static_cast<double>(R), T[R], 0}, block_excl_pick(loc, sh_cand));
+    unsigned t = 0;
+    for (int m = g0 + 1; m <= g1; ++m) {
+      const Cand c{tau[m - 1], T[R + m], m};
+      if (fabs(c.tau * run.t - run.tau * c.t) <= DSPARK_SCHED_TIE_REL * run.tau * c.t) ++t;
+      run = cand_pick(run, c);
+    }
+    t = warp_sum_u32(t);
+    if (lane == 0 && t) atomicAdd(&sh_ties, t);
+    if (tid == kSchedThreads - 1) sh_nstar = run.m;  // the last chunk's run covers every position
+    __syncthreads();
+    n_star = sh_nstar;
+  } else {
+    int K = *K_in;
+    if (K < 0) {
+      if (tid == 0) set_status(status, DSPARK_ERR_BAD_DATA);
+      K = 0;
+    }
+    n_star = K < nE ? K : nE;
   }
   // 5. verify lengths: the admitted prefix of each request
   for (int i = tid; i < n_star; i += kSchedThreads) {
@@ -233,9 +323,10 @@ __global__ void __launch_bounds__(kSchedThreads, 1)
   __syncthreads();
   for (int r = tid; r < R; r += kSchedThreads) verify_len[r] = gws.ell[r];
   if (tid == 0) {
-    if (sh_ties) atomicAdd(ties, sh_ties);
-    if (theta_out)
+    if (ties && sh_ties) atomicAdd(ties, sh_ties);
+    if (theta_out && T)
       *theta_out = n_star > 0 ? tau[n_star - 1] / T[R + n_star] : static_cast<double>(R) / T[R];
+    if (K_out) *K_out = n_star;
   }
 }
 
@@ -384,11 +475,11 @@ constexpr int kSweepSmemMax = (kRankMaxN + 1) * 8 + kRankMaxN * 4;  // profile s
 // thread owns a contiguous chunk (at most CHUNK) of the sorted order and loads its keys once,
 // up front; the profile slice T(R..R(gamma+1)) is staged in shared memory and
 // checked (positive, finite) on the way.
-template <int CHUNK>
+template <int CHUNK, int MODE>
 __global__ void __launch_bounds__(kRankThreads, 1)
     k_sched_sweep(const double* __restrict__ T, int R, int gamma, SchedWs gws,
                   int32_t* __restrict__ verify_len, double* theta_out, uint32_t* ties,
-                  int32_t* status) {
+                  int32_t* status, const int32_t* K_in, int32_t* K_out) {
   pdl_wait();  // predecessor grid complete, its writes visible
   pdl_trigger();
   extern __shared__ __align__(16) unsigned char smem[];
@@ -399,6 +490,8 @@ __global__ void __launch_bounds__(kRankThreads, 1)
   __shared__ int sh_nE, sh_break;
   __shared__ unsigned sh_ties;
   __shared__ ff sh_tau_star;
+  __shared__ Cand sh_cand[32];
+  __shared__ int sh_nstar;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int chunk = (n + blockDim.x - 1) / blockDim.x;
   const int c0 = min(tid * chunk, n), c1 = min(c0 + chunk, n);
@@ -410,11 +503,13 @@ __global__ void __launch_bounds__(kRankThreads, 1)
 #pragma unroll
   for (int q = 0; q < CHUNK; ++q) kv[q] = q < len ? gws.keysB[c0 + q] : 0ull;
   bool bad_t = false;
-  for (int m = tid; m <= n; m += blockDim.x) {
-    const double t = T[R + m];
-    const u64 b = static_cast<u64>(__double_as_longlong(t));
-    if ((b >> 63) || ((b >> 52) & 0x7FFull) == 0x7FFull || b == 0ull) bad_t = true;
-    sh_T[m] = t;
+  if (T) {  // the top-K admission may run without a profile
+    for (int m = tid; m <= n; m += blockDim.x) {
+      const double t = T[R + m];
+      const u64 b = static_cast<u64>(__double_as_longlong(t));
+      if ((b >> 63) || ((b >> 52) & 0x7FFull) == 0x7FFull || b == 0ull) bad_t = true;
+      sh_T[m] = t;
+    }
   }
   if (bad_t) set_status(status, DSPARK_ERR_BAD_DATA);
   if (tid == 0) {
@@ -462,44 +557,88 @@ __global__ void __launch_bounds__(kRankThreads, 1)
   ff tau_start = ff_add(ff{static_cast<float>(R), 0.f}, ex);
   if (warp > 0) tau_start = ff_add(tau_start, sh_w[warp - 1]);
 
-  // walk the chunk: first non-improving admission, near ties up to it
-  int first = INT_MAX;
-  unsigned n_ties = 0;
-  ff tau_prev = tau_start;
-  bool okt = true;
-  ff tp = ff_from_double(sh_T[c0], okt);
+  int n_star;
+  if constexpr (MODE == kModeStop) {
+    // walk the chunk: first non-improving admission, near ties up to it
+    int first = INT_MAX;
+    unsigned n_ties = 0;
+    ff tau_prev = tau_start;
+    bool okt = true;
+    ff tp = ff_from_double(sh_T[c0], okt);
 #pragma unroll
-  for (int q = 0; q < CHUNK; ++q) {
-    const int m = c0 + q + 1;
-    if (q < len && m <= nE && first == INT_MAX) {
-      bool okv = ok && okt;
-      const ff tau_m = ff_add(tau_prev, ff_from_bits(kv[q], okv));
-      const double Tp = sh_T[m - 1], Tm = sh_T[m];
-      const ff tm = ff_from_double(Tm, okv);
-      bool improve, tie;
-      if (okv) {
-        const ff lhs = ff_mul(tau_m, tp), rhs = ff_mul(tau_prev, tm);
-        improve = ff_cmp(lhs, rhs) > 0;
-        const ff d = ff_sub(lhs, rhs);
-        tie = fabsf(d.hi) <= static_cast<float>(DSPARK_SCHED_TIE_REL) * rhs.hi;
-      } else {  // values outside the float range: double precision
-        const double A = static_cast<double>(tau_m.hi) + tau_m.lo;
-        const double Bv = static_cast<double>(tau_prev.hi) + tau_prev.lo;
-        improve = A * Tp > Bv * Tm;
-        tie = fabs(A * Tp - Bv * Tm) <= DSPARK_SCHED_TIE_REL * Bv * Tm;
+    for (int q = 0; q < CHUNK; ++q) {
+      const int m = c0 + q + 1;
+      if (q < len && m <= nE && first == INT_MAX) {
+        bool okv = ok && okt;
+        const ff tau_m = ff_add(tau_prev, ff_from_bits(kv[q], okv));
+        const double Tp = sh_T[m - 1], Tm = sh_T[m];
+        const ff tm = ff_from_double(Tm, okv);
+        bool improve, tie;
+        if (okv) {
+          const ff lhs = ff_mul(tau_m, tp), rhs = ff_mul(tau_prev, tm);
+          improve = ff_cmp(lhs, rhs) > 0;
+          const ff d = ff_sub(lhs, rhs);
+          tie = fabsf(d.hi) <= static_cast<float>(DSPARK_SCHED_TIE_REL) * rhs.hi;
+        } else {  // values outside the float range: double precision
+          const double A = static_cast<double>(tau_m.hi) + tau_m.lo;
+          const double Bv = static_cast<double>(tau_prev.hi) + tau_prev.lo;
+          improve = A * Tp > Bv * Tm;
+          tie = fabs(A * Tp - Bv * Tm) <= DSPARK_SCHED_TIE_REL * Bv * Tm;
+        }
+        if (tie) ++n_ties;
+        if (!improve) first = m;
+        tau_prev = tau_m;
+        tp = tm;
       }
-      if (tie) ++n_ties;
-      if (!improve) first = m;
-      tau_prev = tau_m;
-      tp = tm;
     }
+    const int fw = __reduce_min_sync(0xFFFFFFFFu, first);
+    if (lane == 0) atomicMin(&sh_break, fw);
+    __syncthreads();
+    const int n_break = sh_break;
+    n_star = n_break <= nE ? n_break - 1 : nE;
+    if (c0 + 1 <= n_break && n_ties) atomicAdd(&sh_ties, n_ties);
+  } else if constexpr (MODE == kModeGlobal) {
+    // the best admission of this chunk, then the running best before every
+    // position (first maximum; position 0, nothing admitted, leads)
+    Cand loc{0.0, 1.0, -1};
+    ff tau_m = tau_start;
+#pragma unroll
+    for (int q = 0; q < CHUNK; ++q) {
+      const int m = c0 + q + 1;
+      if (q < len && m <= nE) {
+        bool okv = true;
+        tau_m = ff_add(tau_m, ff_from_bits(kv[q], okv));
+        loc = cand_pick(loc, Cand{static_cast<double>(tau_m.hi) + tau_m.lo, sh_T[m], m});
+      }
+    }
+    Cand run = cand_pick(Cand{static_cast<double>(R), sh_T[0], 0}, block_excl_pick(loc, sh_cand));
+    unsigned n_ties = 0;
+    tau_m = tau_start;
+#pragma unroll
+    for (int q = 0; q < CHUNK; ++q) {
+      const int m = c0 + q + 1;
+      if (q < len && m <= nE) {
+        bool okv = true;
+        tau_m = ff_add(tau_m, ff_from_bits(kv[q], okv));
+        const Cand c{static_cast<double>(tau_m.hi) + tau_m.lo, sh_T[m], m};
+        // |Theta(m) - Theta_best| <= eps Theta_best, multiplied through by both T
+        if (fabs(c.tau * run.t - run.tau * c.t) <= DSPARK_SCHED_TIE_REL * run.tau * c.t) ++n_ties;
+        run = cand_pick(run, c);
+      }
+    }
+    n_ties = warp_sum_u32(n_ties);
+    if (lane == 0 && n_ties) atomicAdd(&sh_ties, n_ties);
+    if (tid == blockDim.x - 1) sh_nstar = run.m;  // the last chunk's run covers every position
+    __syncthreads();
+    n_star = sh_nstar;
+  } else {
+    int K = *K_in;
+    if (K < 0) {
+      if (tid == 0) set_status(status, DSPARK_ERR_BAD_DATA);
+      K = 0;
+    }
+    n_star = K < nE ? K : nE;
   }
-  const int fw = __reduce_min_sync(0xFFFFFFFFu, first);
-  if (lane == 0) atomicMin(&sh_break, fw);
-  __syncthreads();
-  const int n_break = sh_break;
-  const int n_star = n_break <= nE ? n_break - 1 : nE;
-  if (c0 + 1 <= n_break && n_ties) atomicAdd(&sh_ties, n_ties);
   // tau(n*) for Theta_best, from the thread whose chunk holds position n*
   if (n_star > 0 && c0 < n_star && n_star <= c1) {
     ff t = tau_start;
@@ -516,12 +655,39 @@ __global__ void __launch_bounds__(kRankThreads, 1)
   __syncthreads();
   for (int r = tid; r < R; r += blockDim.x) verify_len[r] = sh_ell[r];
   if (tid == 0) {
-    *ties = sh_ties;
-    if (theta_out) {
+    if (ties) *ties = sh_ties;
+    if (theta_out && T) {
       const double tau_star = static_cast<double>(sh_tau_star.hi) + sh_tau_star.lo;
       *theta_out = tau_star / sh_T[n_star];
     }
+    if (K_out) *K_out = n_star;
   }
+}
+
+template <int MODE>
+bool sweep_smem_attr() {
+  return cudaFuncSetAttribute(k_sched_sweep<4, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSweepSmemMax) == cudaSuccess &&
+         cudaFuncSetAttribute(k_sched_sweep<8, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSweepSmemMax) == cudaSuccess &&
+         cudaFuncSetAttribute(k_sched_sweep<16, MODE>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSweepSmemMax) == cudaSuccess;
+}
+
+// the sweep instantiation whose per-thread chunk holds n / 1024 candidates
+template <int MODE>
+cudaError_t launch_sweep(int n, size_t smem, cudaStream_t st, const double* T, int R, int gamma,
+                         const SchedWs& ws, int32_t* verify_len, double* theta, uint32_t* ties,
+                         int32_t* status, const int32_t* K_in, int32_t* K_out) {
+  if (n <= 4 * kRankThreads)
+    return launch_pdl(k_sched_sweep<4, MODE>, 1, kRankThreads, smem, st, T, R, gamma, ws,
+                      verify_len, theta, ties, status, K_in, K_out);
+  if (n <= 8 * kRankThreads)
+    return launch_pdl(k_sched_sweep<8, MODE>, 1, kRankThreads, smem, st, T, R, gamma, ws,
+                      verify_len, theta, ties, status, K_in, K_out);
+  return launch_pdl(k_sched_sweep<16, MODE>, 1, kRankThreads, smem, st, T, R, gamma, ws,
+                    verify_len, theta, ties, status, K_in, K_out);
 }
 
 std::mutex g_sched_mutex;
@@ -530,17 +696,24 @@ int g_sched_sms[128];
 
 }  // namespace dspark
 
-extern "C" int dspark_schedule(const float* confidences, const double* step_time_ms,
-                               int64_t n_profile, int32_t R, int32_t gamma, int32_t* verify_len,
-                               double* theta_best, uint32_t* near_tie_count,
-                               int32_t* device_status, void* workspace, size_t workspace_bytes,
-                               struct CUstream_st* stream) {
-  using namespace dspark;
+namespace dspark {
+
+// Shared host path of the three scheduler entry points. T may be NULL only in
+// the top-K mode (no profile, no Theta).
+int schedule_run(int mode, const float* confidences, const double* step_time_ms,
+                 int64_t n_profile, int32_t R, int32_t gamma, const int32_t* K_in,
+                 int32_t* K_out, int32_t* verify_len, double* theta_best,
+                 uint32_t* near_tie_count, int32_t* device_status, void* workspace,
+                 size_t workspace_bytes, cudaStream_t st) {
   if (R < 1 || gamma < 1 || gamma > DSPARK_MAX_GAMMA) return DSPARK_ERR_INVALID_ARG;
   if (static_cast<long long>(R) * (gamma + 1) >= (1LL << 30)) return DSPARK_ERR_INVALID_ARG;
-  if (!confidences || !step_time_ms || !verify_len || !device_status)
-    return DSPARK_ERR_INVALID_ARG;
-  if (n_profile < static_cast<int64_t>(R) * (gamma + 1) + 1) return DSPARK_ERR_INVALID_ARG;
+  if (!confidences || !verify_len || !device_status) return DSPARK_ERR_INVALID_ARG;
+  if (mode != kModeTopK || step_time_ms) {
+    if (!step_time_ms) return DSPARK_ERR_INVALID_ARG;
+    if (n_profile < static_cast<int64_t>(R) * (gamma + 1) + 1) return DSPARK_ERR_INVALID_ARG;
+  }
+  if (mode == kModeTopK && !K_in) return DSPARK_ERR_INVALID_ARG;
+  if (mode == kModeGlobal && !K_out) return DSPARK_ERR_INVALID_ARG;
   if (!workspace || workspace_bytes < DSPARK_SCHEDULE_WS_BYTES(R, gamma) ||
       reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
     return DSPARK_ERR_WORKSPACE;
@@ -556,12 +729,8 @@ extern "C" int dspark_schedule(const float* confidences, const double* step_time
       if (cudaFuncSetAttribute(k_sched_rank, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kRankSmemMax) != cudaSuccess)
         return DSPARK_ERR_CUDA;
-      if (cudaFuncSetAttribute(k_sched_sweep<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSweepSmemMax) != cudaSuccess ||
-          cudaFuncSetAttribute(k_sched_sweep<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSweepSmemMax) != cudaSuccess ||
-          cudaFuncSetAttribute(k_sched_sweep<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSweepSmemMax) != cudaSuccess)
+      if (!sweep_smem_attr<kModeStop>() || !sweep_smem_attr<kModeGlobal>() ||
+          !sweep_smem_attr<kModeTopK>())
         return DSPARK_ERR_CUDA;
       if (cudaDeviceGetAttribute(&g_sched_sms[dev], cudaDevAttrMultiProcessorCount, dev) !=
           cudaSuccess)
@@ -584,8 +753,8 @@ extern "C" int dspark_schedule(const float* confidences, const double* step_time
   ws.idxB = reinterpret_cast<int32_t*>(p);
   p += DSPARK_ALIGN256(static_cast<size_t>(n) * 4);
   ws.ell = reinterpret_cast<int32_t*>(p);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint32_t* ties = near_tie_count ? near_tie_count : ws.ties_scratch;
+  const double* T = step_time_ms;
   const size_t rank_smem = static_cast<size_t>(R) * (gamma | 1) * 8;
   if (n <= kRankMaxN && rank_smem <= static_cast<size_t>(kRankSmemMax)) {
     // ranks over the whole GPU, then a one-CTA float-float sweep
@@ -595,23 +764,58 @@ extern "C" int dspark_schedule(const float* confidences, const double* step_time
                                gamma, ws, device_status);
     if (e != cudaSuccess) return DSPARK_ERR_CUDA;
     const size_t sweep_smem = (static_cast<size_t>(n) + 1) * 8 + static_cast<size_t>(R) * 4;
-    if (n <= 4 * kRankThreads)
-      e = launch_pdl(k_sched_sweep<4>, 1, kRankThreads, sweep_smem, st, step_time_ms, R, gamma, ws,
-                     verify_len, theta_best, ties, device_status);
-    else if (n <= 8 * kRankThreads)
-      e = launch_pdl(k_sched_sweep<8>, 1, kRankThreads, sweep_smem, st, step_time_ms, R, gamma, ws,
-                     verify_len, theta_best, ties, device_status);
+    if (mode == kModeStop)
+      e = launch_sweep<kModeStop>(n, sweep_smem, st, T, R, gamma, ws, verify_len, theta_best,
+                                  ties, device_status, K_in, K_out);
+    else if (mode == kModeGlobal)
+      e = launch_sweep<kModeGlobal>(n, sweep_smem, st, T, R, gamma, ws, verify_len, theta_best,
+                                    ties, device_status, K_in, K_out);
     else
-      e = launch_pdl(k_sched_sweep<16>, 1, kRankThreads, sweep_smem, st, step_time_ms, R, gamma,
-                     ws, verify_len, theta_best, ties, device_status);
+      e = launch_sweep<kModeTopK>(n, sweep_smem, st, T, R, gamma, ws, verify_len, theta_best,
+                                  ties, device_status, K_in, K_out);
     if (e != cudaSuccess) return DSPARK_ERR_CUDA;
   } else {
     const int use_smem = n <= kSchedSmemMaxN ? 1 : 0;
     const size_t smem = use_smem ? static_cast<size_t>(n) * 24 : 0;
-    if (launch_pdl(k_schedule, 1, kSchedThreads, smem, st, confidences, step_time_ms, R, gamma,
-                   verify_len, theta_best, ties, device_status, ws, use_smem) != cudaSuccess)
+    if (launch_pdl(k_schedule, 1, kSchedThreads, smem, st, confidences, T, R, gamma, verify_len,
+                   theta_best, ties, device_status, ws, use_smem, mode, K_in,
+                   K_out) != cudaSuccess)
       return DSPARK_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
+}
+
+}  // namespace dspark
+
+extern "C" int dspark_schedule(const float* confidences, const double* step_time_ms,
+                               int64_t n_profile, int32_t R, int32_t gamma, int32_t* verify_len,
+                               double* theta_best, uint32_t* near_tie_count,
+                               int32_t* device_status, void* workspace, size_t workspace_bytes,
+                               struct CUstream_st* stream) {
+  return dspark::schedule_run(dspark::kModeStop, confidences, step_time_ms, n_profile, R, gamma,
+                              nullptr, nullptr, verify_len, theta_best, near_tie_count,
+                              device_status, workspace, workspace_bytes,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int dspark_schedule_capacity(const float* confidences, const double* step_time_ms,
+                                        int64_t n_profile, int32_t R, int32_t gamma,
+                                        int32_t* capacity, int32_t* verify_len,
+                                        double* theta_best, uint32_t* near_tie_count,
+                                        int32_t* device_status, void* workspace,
+                                        size_t workspace_bytes, struct CUstream_st* stream) {
+  return dspark::schedule_run(dspark::kModeGlobal, confidences, step_time_ms, n_profile, R,
+                              gamma, nullptr, capacity, verify_len, theta_best, near_tie_count,
+                              device_status, workspace, workspace_bytes,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int dspark_schedule_topk(const float* confidences, const int32_t* capacity, int32_t R,
+                                    int32_t gamma, int32_t* verify_len, int32_t* device_status,
+                                    void* workspace, size_t workspace_bytes,
+                                    struct CUstream_st* stream) {
+  return dspark::schedule_run(dspark::kModeTopK, confidences, nullptr, 0, R, gamma, capacity,
+                              nullptr, verify_len, nullptr, nullptr, device_status, workspace,
+                              workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -107,3 +107,21 @@ def test_timed_verify_rejects_missing_events_on_host(lib):
     bad = list(args)
     bad[8] = 33  # gamma
     assert lib.dspark_verify_timed(*bad, good_events) == 1
+
+
+def test_production_scheduler_rejects_bad_arguments_on_host(lib):
+    p = ctypes.c_void_p
+    cap = lambda R=4, g=4, n=21, capacity=1, T=1, ws=256: lib.dspark_schedule_capacity(
+        p(1), None if T is None else p(T), n, R, g, None if capacity is None else p(capacity),
+        p(1), None, None, p(1), None if ws is None else p(ws), 1 << 30, None)
+    assert cap(capacity=None) == 1
+    assert cap(T=None) == 1
+    assert cap(n=20) == 1
+    assert cap(R=0) == 1
+    assert cap(ws=None) == 3
+    topk = lambda R=4, g=4, capacity=1, ws=256, wsb=1 << 30: lib.dspark_schedule_topk(
+        p(1), None if capacity is None else p(capacity), R, g, p(1), p(1),
+        None if ws is None else p(ws), wsb, None)
+    assert topk(capacity=None) == 1
+    assert topk(g=33) == 1
+    assert topk(wsb=10) == 3
