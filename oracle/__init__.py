@@ -71,6 +71,9 @@ def _setup(lib):
     lib.oracle_schedule_topk.argtypes = [
         ctypes.POINTER(ctypes.c_float), ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, c_i32p,
         c_i64p]
+    lib.oracle_schedule_threshold.restype = ctypes.c_int
+    lib.oracle_schedule_threshold.argtypes = [
+        ctypes.POINTER(ctypes.c_float), ctypes.c_int32, ctypes.c_int32, ctypes.c_float, c_i32p]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     return lib
@@ -193,6 +196,20 @@ def schedule_topk(confidences, K: int, lib=None):
     if rc != 0:
         raise OracleError(f"oracle_schedule_topk returned {rc}")
     return {"verify_len": ell, "n_admitted": n_adm.value}
+
+
+def schedule_threshold(confidences, threshold: float, lib=None):
+    """Static-threshold baseline: l_r = the number of leading draft tokens whose
+    confidence reaches the threshold. Returns verify_len [R] int32."""
+    lib = lib or load()
+    c = np.ascontiguousarray(confidences, dtype=np.float32)
+    R, gamma = c.shape
+    ell = np.zeros(R, np.int32)
+    rc = lib.oracle_schedule_threshold(_ptr(c, ctypes.c_float), R, gamma, float(threshold),
+                                       _ptr(ell, ctypes.c_int32))
+    if rc != 0:
+        raise OracleError(f"oracle_schedule_threshold returned {rc}")
+    return ell
 
 
 def max_threads(lib=None) -> int:

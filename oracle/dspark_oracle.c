@@ -451,6 +451,29 @@ int oracle_schedule_topk(const float* confidences, int32_t R, int32_t gamma, int
   return ORACLE_OK;
 }
 
+/*
+ * Static-threshold verification lengths, the diagnostic baseline of the DSpark
+ * paper's section 4.3.3 ("Static Threshold Sweep"): each request verifies its
+ * draft tokens while their confidence reaches the threshold; the suffix from
+ * the first token below it is pruned. l_r = max{ j : c_{r,i} >= threshold for
+ * all i <= j } (0 if c_{r,1} < threshold).
+ */
+int oracle_schedule_threshold(const float* confidences, int32_t R, int32_t gamma,
+                              float threshold, int32_t* verify_len) {
+  if (!confidences || !verify_len || R < 1 || gamma < 1 || !isfinite(threshold))
+    return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < (int64_t)R * gamma; ++i) {
+    const float c = confidences[i];
+    if (!(c >= 0.0f && c <= 1.0f)) return ORACLE_ERR_DATA;
+  }
+  for (int32_t r = 0; r < R; ++r) {
+    int32_t ell = 0;
+    while (ell < gamma && confidences[(int64_t)r * gamma + ell] >= threshold) ++ell;
+    verify_len[r] = ell;
+  }
+  return ORACLE_OK;
+}
+
 /* Number of OpenMP threads the oracle can use (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP
