@@ -232,6 +232,27 @@ int dspark_schedule_topk(const float* confidences, const int32_t* capacity, int3
                          int32_t gamma, int32_t* verify_len, int32_t* device_status,
                          void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
+/*
+ * dspark_schedule_threshold -- the static-threshold baseline (DSpark paper,
+ * section 4.3.3, "Static Threshold Sweep"): each request verifies its draft
+ * tokens while their confidence reaches the threshold; the suffix from the
+ * first token below it is pruned. l_r = max{ j : c_{r,i} >= threshold for all
+ * i <= j }. It ignores the system load, which is what the prefix scheduler
+ * adds; it serves as the comparison point.
+ *
+ * Arguments
+ *   confidences   [R][gamma] float32, each in [0, 1] (else DSPARK_ERR_BAD_DATA
+ *                 in *device_status; a NaN stops its request's prefix).
+ *   threshold     finite float.
+ *   R >= 1, 1 <= gamma <= DSPARK_MAX_GAMMA.
+ *   verify_len    out [R] int32.
+ *   device_status out [1] int32 (required).
+ * No workspace; one launch on `stream`.
+ */
+int dspark_schedule_threshold(const float* confidences, float threshold, int32_t R,
+                              int32_t gamma, int32_t* verify_len, int32_t* device_status,
+                              struct CUstream_st* stream);
+
 /* Size of the library-owned scratch array behind dspark_verify_static. */
 #define DSPARK_STATIC_WS_BYTES ((size_t)16u << 20)
 

@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_CUDA
                 6: "DSPARK_ERR_TOO_LARGE"}
 DSPARK_F32, DSPARK_BF16 = 0, 1
 EXPORTED = ("dspark_verify", "dspark_schedule", "dspark_schedule_capacity",
-            "dspark_schedule_topk", "dspark_verify_static", "dspark_verify_timed")
+            "dspark_schedule_topk", "dspark_schedule_threshold", "dspark_verify_static",
+            "dspark_verify_timed")
 
 
 class DsparkError(RuntimeError):
@@ -103,6 +104,8 @@ def load(path: Optional[str] = None):
                                                  vp]
         lib.dspark_schedule_topk.restype = ctypes.c_int
         lib.dspark_schedule_topk.argtypes = [vp, vp, i32, i32, vp, vp, vp, sz, vp]
+        lib.dspark_schedule_threshold.restype = ctypes.c_int
+        lib.dspark_schedule_threshold.argtypes = [vp, f32, i32, i32, vp, vp, vp]
         if path is None:
             _lib = lib
         return lib
@@ -303,3 +306,29 @@ def dspark_schedule_topk(confidences: torch.Tensor, capacity: torch.Tensor, *,
     if rc != 0:
         raise DsparkError("dspark_schedule_topk", rc)
     return _schedule_out(buf, dev, check, "dspark_schedule_topk")
+
+
+def dspark_schedule_threshold(confidences: torch.Tensor, threshold: float, *,
+                              verify_len: Optional[torch.Tensor] = None,
+                              device_status: Optional[torch.Tensor] = None, stream=None,
+                              check: bool = False) -> dict:
+    """Static-threshold baseline (section 4.3.3): l_r = the number of leading
+    draft tokens whose confidence reaches the threshold. Returns verify_len [R]
+    int32 and device_status [1] (device tensors)."""
+    dev = confidences.device
+    _require_cuda("confidences", confidences, torch.float32)
+    R, gamma = confidences.shape
+    ell = verify_len if verify_len is not None else torch.empty(R, dtype=torch.int32, device=dev)
+    st = device_status if device_status is not None else torch.zeros(1, dtype=torch.int32,
+                                                                      device=dev)
+    lib = load()
+    with torch.cuda.device(dev):
+        rc = lib.dspark_schedule_threshold(_ptr(confidences), float(threshold), R, gamma,
+                                           _ptr(ell), _ptr(st), _stream_handle(stream))
+    if rc != 0:
+        raise DsparkError("dspark_schedule_threshold", rc)
+    if check:
+        torch.cuda.synchronize(dev)
+        if int(st.item()) != 0:
+            raise DsparkError("dspark_schedule_threshold (device)", int(st.item()))
+    return {"verify_len": ell, "device_status": st}

@@ -664,6 +664,38 @@ __global__ void __launch_bounds__(kRankThreads, 1)
   }
 }
 
+// Static-threshold lengths (section 4.3.3, the diagnostic baseline): l_r =
+// the number of leading draft tokens whose confidence reaches the threshold.
+// One CTA, a thread per request; the CTA sees every confidence, so its verdict
+// on them is complete when thread 0 writes the status.
+__global__ void __launch_bounds__(1024, 1)
+    k_sched_threshold(const float* __restrict__ conf, float thr, int R, int gamma,
+                      int32_t* __restrict__ verify_len, int32_t* status) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  __shared__ int sh_bad;
+  if (threadIdx.x == 0) sh_bad = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int r = threadIdx.x; r < R; r += blockDim.x) {
+    const float* c = conf + static_cast<long long>(r) * gamma;
+    int ell = 0;
+    bool open = true;
+    for (int j = 0; j < gamma; ++j) {
+      const float v = c[j];
+      if (!(v >= 0.f && v <= 1.f)) bad = true;
+      if (open && v >= thr)
+        ++ell;
+      else
+        open = false;
+    }
+    verify_len[r] = ell;
+  }
+  if (bad) atomicOr(&sh_bad, 1);
+  __syncthreads();
+  if (threadIdx.x == 0) *status = sh_bad ? DSPARK_ERR_BAD_DATA : DSPARK_OK;
+}
+
 template <int MODE>
 bool sweep_smem_attr() {
   return cudaFuncSetAttribute(k_sched_sweep<4, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -818,4 +850,18 @@ extern "C" int dspark_schedule_topk(const float* confidences, const int32_t* cap
   return dspark::schedule_run(dspark::kModeTopK, confidences, nullptr, 0, R, gamma, capacity,
                               nullptr, verify_len, nullptr, nullptr, device_status, workspace,
                               workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int dspark_schedule_threshold(const float* confidences, float threshold, int32_t R,
+                                         int32_t gamma, int32_t* verify_len,
+                                         int32_t* device_status, struct CUstream_st* stream) {
+  using namespace dspark;
+  if (R < 1 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || !std::isfinite(threshold))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!confidences || !verify_len || !device_status) return DSPARK_ERR_INVALID_ARG;
+  if (launch_pdl(k_sched_threshold, 1, 1024, 0, reinterpret_cast<cudaStream_t>(stream),
+                 confidences, threshold, R, gamma, verify_len, device_status) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
 }

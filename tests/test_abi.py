@@ -125,3 +125,16 @@ def test_production_scheduler_rejects_bad_arguments_on_host(lib):
     assert topk(capacity=None) == 1
     assert topk(g=33) == 1
     assert topk(wsb=10) == 3
+
+
+def test_threshold_baseline_rejects_bad_arguments_on_host(lib):
+    p = ctypes.c_void_p
+    call = lambda thr=0.5, R=4, g=4, conf=1, out=1, st=1: lib.dspark_schedule_threshold(
+        None if conf is None else p(conf), thr, R, g, None if out is None else p(out),
+        None if st is None else p(st), None)
+    assert call(thr=float("nan")) == 1
+    assert call(thr=float("inf")) == 1
+    assert call(R=0) == 1
+    assert call(g=33) == 1
+    assert call(conf=None) == 1
+    assert call(st=None) == 1
