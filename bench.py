@@ -300,7 +300,7 @@ def native_arm(args):
                               events=pev[i])
     torch.cuda.synchronize(dev)
     pass_ms = {name: statistics.median([e[j].elapsed_time(e[j + 1]) for e in pev])
-               for j, name in enumerate(("k_plan", "k_rowstats_tma", "k_decide"))}
+               for j, name in enumerate(("k_plan", "k_rowstats_tma", "decision"))}
 
     # end to end: pinned host buffers -> device, both calls, results back
     e2e = None
@@ -396,7 +396,7 @@ def native_arm(args):
                       "verify_p90": float(np.percentile(verify_ms, 90)),
                       "schedule_median": statistics.median(sched_ms),
                       "passes_median": pass_ms},
-        "gpu_launches": args.steps * 5,  # per step: k_sched_rank, k_sched_sweep, k_plan, k_rowstats, k_decide
+        "gpu_launches": args.steps * 7,  # per step: k_sched_rank, k_sched_sweep, k_plan, k_rowstats_tma, k_desc, k_resid, k_pick
         "near_ties": int(vbuf.near_tie_count.item()),
         "clocks": clk,
         "e2e": e2e,

@@ -78,6 +78,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Per-thread asynchronous 16-byte copy global -> shared (the thread's own
+// copies complete in commit-group order; cp.async.wait_group N leaves at most
+// N of its groups in flight and makes the completed ones visible to it).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Programmatic dependent launch. Every kernel of the library is launched with
 // programmatic stream serialization, so the next kernel on the stream may be
 // scheduled before this one ends. pdl_wait() blocks until the preceding grid

@@ -7,7 +7,7 @@
 // nothing is admitted). The residual max(0, p_t - p_d) after a rejection is the
 // standard rule of the speculative sampling papers cited there as [1], [2].
 //
-// Pipeline (three launches on the caller's stream, no host synchronisation):
+// Pipeline (launches on the caller's stream, no host synchronisation):
 //   k_plan      one CTA: validates verify lengths and row offsets, lays out the
 //               rows to read (l_r + 1 target rows and l_r draft rows per
 //               request) and resets counters.
@@ -23,17 +23,21 @@
 //               statistics (sum as a float pair, K) go to the workspace. No
 //               double-precision instruction runs per logit: GB300's FP64 rate
 //               is a small fraction of its FP32 rate.
-//   k_decide    several CTAs per request, as many as one resident wave holds.
-//               Each loads the tested tokens' logits, merges the unit records
-//               of the request's rows (contiguous; a few threads per row,
-//               compensated float, exact power-of-two alignment), evaluates
-//               the ratio p_t^k(x_k)/p_d^k(x_k) in float -- in double only
-//               when the uniform lies within 2e-6 of it -- and finds the first
-//               rejection with a warp ballot; part 0 writes accepted lengths,
-//               tokens and probabilities. Each part then sums the residual (or
-//               bonus) weights of its share of the 2048-token segments; the
-//               last part to finish scans the segment sums, re-reads the one
+//   k_desc      one CTA per request: loads the tested tokens' logits, merges the
+//               unit records of the request's rows (contiguous; a few threads
+//               per row, compensated float, exact power-of-two alignment),
+//               evaluates p_t^k(x_k)/p_d^k(x_k) in float -- in double only when
+//               the uniform lies within 2e-6 of it -- finds the first
+//               rejection with a warp ballot, writes accepted lengths, tokens
+//               and probabilities, and the descriptor of the token to draw.
+//   k_resid     the residual (or bonus) weights of every draw, summed per
+//               2048-token segment by a persistent streamer like k_rowstats:
+//               each warp's TMA ring carries 2 KB of the target row and 2 KB
+//               of the draft row per stage.
+//   k_pick      one CTA per request: scans the segment sums, re-reads the one
 //               segment holding the cut and picks the token.
+// Rows that are not 16-byte aligned take k_rowstats_plain (plain loads) and
+// k_decide (several CTAs per request: ratio tests, segment sums, the draw).
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -55,7 +59,7 @@ struct TileStat {  // statistics of one (row, unit): sum_v 2^(z_v*c - K) = s_hi 
 };
 static_assert(sizeof(TileStat) == 16, "TileStat layout");
 
-struct ResampleDesc {
+struct __align__(16) ResampleDesc {
   int64_t t_row;  // global row of the target distribution sampled from
   int64_t d_row;  // global draft row (residual mode)
   int32_t K_t;    // exponent reference of the target row
@@ -493,6 +497,19 @@ __device__ __forceinline__ void stat_combine(int& K, float& hi, float& lo, int K
   two_sum_acc(hi, lo, h2, l2);
 }
 
+// Records written by other CTAs of the running grid are read through L2
+// (ld.global.cg), never through the non-coherent read-only path.
+template <typename T>
+__device__ __forceinline__ T ld_record(const T* p) {
+  static_assert(sizeof(T) % 16 == 0 && alignof(T) == 16, "16-byte records");
+  T v;
+  const int4* src = reinterpret_cast<const int4*>(p);
+  int4* o = reinterpret_cast<int4*>(&v);
+#pragma unroll
+  for (int i = 0; i < static_cast<int>(sizeof(T) / 16); ++i) o[i] = __ldcg(src + i);
+  return v;
+}
+
 // One row's statistics from its unit records, all lanes of a warp: lanes take
 // units, then a butterfly combine. Lane 0's result is the one used.
 __device__ RowStat warp_merge_row(const TileStat* __restrict__ t, int n_units, int lane) {
@@ -628,9 +645,13 @@ __device__ void ratio_tests(const RatioIn& in, int r, int gamma, int start, cons
   bool accept = false, tie = false;
   int32_t x = 0;
   RowStat st{}, sd{};
+  double Dk = 0.0;  // this position's D, should it be the first rejection
   if (has) {
     st = sh_rs[k - 1];
     sd = sh_rs[ell + k];
+    // independent of the ratio below: its latency overlaps the test's
+    Dk = static_cast<double>(st.K - sd.K) +
+         log2((static_cast<double>(st.S_hi) + st.S_lo) / (static_cast<double>(sd.S_hi) + sd.S_lo));
     x = in.x;
     const float u = in.u;
     if (in.bad || !st.ok || !sd.ok) set_status(status, DSPARK_ERR_BAD_DATA);
@@ -669,12 +690,8 @@ __device__ void ratio_tests(const RatioIn& in, int r, int gamma, int start, cons
 
   // descriptor of the token to sample after the block
   const int src = m < ell ? m : 0;
-  const float St_hi = __shfl_sync(0xFFFFFFFFu, st.S_hi, src);
-  const float St_lo = __shfl_sync(0xFFFFFFFFu, st.S_lo, src);
-  const float Sd_hi = __shfl_sync(0xFFFFFFFFu, sd.S_hi, src);
-  const float Sd_lo = __shfl_sync(0xFFFFFFFFu, sd.S_lo, src);
+  const double Dm = __shfl_sync(0xFFFFFFFFu, Dk, src);
   const int Kt = __shfl_sync(0xFFFFFFFFu, st.K, src);
-  const int Kd = __shfl_sync(0xFFFFFFFFu, sd.K, src);
   if (lane == 0) {
     if (write_out) accepted_len[r] = m;
     ResampleDesc d;
@@ -691,10 +708,7 @@ __device__ void ratio_tests(const RatioIn& in, int r, int gamma, int start, cons
       d.t_row = ws.row_list[start + m] >> 1;
       d.d_row = ws.row_list[start + ell + 1 + m] >> 1;
       d.K_t = Kt;
-      // one lane, a handful of double operations per request
-      const double D = static_cast<double>(Kt - Kd) +
-                       log2((static_cast<double>(St_hi) + St_lo) /
-                            (static_cast<double>(Sd_hi) + Sd_lo));
+      const double D = Dm;
       d.D_hi = static_cast<float>(D);
       d.D_lo = static_cast<float>(D - static_cast<double>(d.D_hi));
       const double E = D - static_cast<double>(Kt);
@@ -720,9 +734,11 @@ __device__ void ratio_tests(const RatioIn& in, int r, int gamma, int start, cons
 //   target mode:   e_t(v) = 2^(z_t*c - K_t)                   (proportional to p_t)
 //   residual mode: (e_t(v) - e_d(v))^+, e_d(v) = 2^(z_d*c + E) (proportional to
 //                  max(0, p_t - p_d)), with E = D - K_t.
-// p_d/p_t = 2^(-d2), d2 = (z_t - z_d)*c - D. Where a token carries much mass
-// the difference may cancel; there the weight is e_t * -expm1(-d2 ln 2), which
-// keeps full relative precision.
+// p_d/p_t = 2^(-d2), d2 = (z_t - z_d)*c - D. For a token carrying much mass
+// (e_t > 2^-8) with p_d close to p_t (0 < d2 < 1) the difference may cancel;
+// there the weight is e_t * (1 - 2^(-d2)), the factor from its Taylor series
+// in y = d2 ln 2 (ten terms: truncation below 1e-9 relative for y < ln 2).
+// For d2 >= 1 the difference loses at most a few 1e-7 of relative precision.
 struct WeightParams {
   int mode;
   float nK;          // -K_t
@@ -732,6 +748,21 @@ struct WeightParams {
 
 __device__ __forceinline__ WeightParams weight_params(const ResampleDesc& d) {
   return WeightParams{d.mode, -static_cast<float>(d.K_t), d.D_hi, d.D_lo, d.E_hi, d.E_lo};
+}
+
+// 1 - exp(-y) for 0 <= y < ln 2: y * sum_{k>=1} (-y)^(k-1) / k!, Horner form
+__device__ __forceinline__ float one_minus_exp_neg_small(float y) {
+  float t = -1.f / 3628800.f;                 // (-1)^(10+1) / 10!
+  t = fmaf(t, y, 1.f / 362880.f);             // 1/9!
+  t = fmaf(t, y, -1.f / 40320.f);
+  t = fmaf(t, y, 1.f / 5040.f);
+  t = fmaf(t, y, -1.f / 720.f);
+  t = fmaf(t, y, 1.f / 120.f);
+  t = fmaf(t, y, -1.f / 24.f);
+  t = fmaf(t, y, 1.f / 6.f);
+  t = fmaf(t, y, -0.5f);
+  t = fmaf(t, y, 1.f);
+  return t * y;
 }
 
 __device__ __forceinline__ float resample_weight(float zt, float zd, const WeightParams& w,
@@ -745,10 +776,81 @@ __device__ __forceinline__ float resample_weight(float zt, float zd, const Weigh
     const float d2 = fmaf(dz, ep.c_hi, -w.D_hi) + fmaf(dz, ep.c_lo, -w.D_lo);
     if (!(d2 > 0.f))
       r = 0.f;
-    else if (d2 < 4.f)
-      r = e * -expm1f(-d2 * 0.6931471805599453f);
+    else if (d2 < 1.f)
+      r = e * one_minus_exp_neg_small(d2 * 0.6931471805599453f);
   }
   return r;
+}
+
+template <typename Tin, int MODE>
+__device__ __forceinline__ bool vec_weight_sum(const uint4& qt, const uint4& qd,
+                                               const WeightParams& w, const ExpParams& ep,
+                                               float& sum) {
+  constexpr int E = 16 / sizeof(Tin);
+  const Tin* et = reinterpret_cast<const Tin*>(&qt);
+  const Tin* ed = reinterpret_cast<const Tin*>(&qd);
+  float s = 0.f;
+  bool light = true;
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const float e = exp_term(to_float<Tin>(et[i]), w.nK, ep);
+    if constexpr (MODE == kModeResidual) {
+      const float zd = to_float<Tin>(ed[i]);
+      const float edv = ex2_approx(fmaf(zd, ep.c_lo, fmaf(zd, ep.c_hi, w.E_hi)) + w.E_lo);
+      light = light && !(e > 0.00390625f);
+      s += fmaxf(e - edv, 0.f);
+    } else {
+      s += e;
+    }
+  }
+  sum = s;
+  return light;
+}
+
+// The per-token sum of a vector holding a heavy token (rare).
+template <typename Tin>
+__device__ __forceinline__ float heavy_vec_sum(const uint4& qt, const uint4& qd,
+                                               const WeightParams& wp, const ExpParams& ep) {
+  constexpr int E = 16 / sizeof(Tin);
+  const Tin* et = reinterpret_cast<const Tin*>(&qt);
+  const Tin* ed = reinterpret_cast<const Tin*>(&qd);
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i)
+    sum += resample_weight(to_float<Tin>(et[i]), to_float<Tin>(ed[i]), wp, ep);
+  return sum;
+}
+
+template <typename Tin, int MODE>
+__device__ __forceinline__ void span_sum_vec(const Tin* __restrict__ zt,
+                                             const Tin* __restrict__ zd, int a, int b,
+                                             const WeightParams& wp, const ExpParams& ep,
+                                             int lane, LaneAcc& acc) {
+  constexpr int E = 16 / sizeof(Tin);
+  constexpr int NB = 2;
+  const uint4* vt = reinterpret_cast<const uint4*>(zt);
+  const uint4* vd = reinterpret_cast<const uint4*>(zd);
+  const int v_end = b / E;
+  for (int v0 = a / E + lane; v0 < v_end; v0 += 32 * NB) {
+    uint4 qt[NB], qd[NB];
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+      const int vi = v0 + 32 * q;
+      qt[q] = vi < v_end ? __ldg(vt + vi) : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (MODE == kModeResidual)
+        qd[q] = vi < v_end ? __ldg(vd + vi) : make_uint4(0u, 0u, 0u, 0u);
+      else
+        qd[q] = qt[q];
+    }
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+      if (v0 + 32 * q >= v_end) break;
+      float sum;
+      if (!vec_weight_sum<Tin, MODE>(qt[q], qd[q], wp, ep, sum))
+        sum = heavy_vec_sum<Tin>(qt[q], qd[q], wp, ep);
+      kahan_add(acc, sum);
+    }
+  }
 }
 
 template <typename Tin, bool VEC>
@@ -758,32 +860,10 @@ __device__ void segment_sum(const Tin* __restrict__ zt, const Tin* __restrict__ 
   const int mode = wp.mode;
   LaneAcc acc;
   if constexpr (VEC) {
-    // NB 16-byte vectors per lane and row are requested before any arithmetic
-    constexpr int E = 16 / sizeof(Tin);
-    constexpr int NB = 2;
-    const uint4* vt = reinterpret_cast<const uint4*>(zt);
-    const uint4* vd = reinterpret_cast<const uint4*>(zd);
-    const int v_end = b / E;
-    for (int v0 = a / E + lane; v0 < v_end; v0 += 32 * NB) {
-      uint4 qt[NB], qd[NB];
-#pragma unroll
-      for (int q = 0; q < NB; ++q) {
-        const int vi = v0 + 32 * q;
-        qt[q] = vi < v_end ? __ldg(vt + vi) : make_uint4(0u, 0u, 0u, 0u);
-        qd[q] = (mode == kModeResidual && vi < v_end) ? __ldg(vd + vi) : qt[q];
-      }
-#pragma unroll
-      for (int q = 0; q < NB; ++q) {
-        if (v0 + 32 * q >= v_end) break;
-        const Tin* et = reinterpret_cast<const Tin*>(&qt[q]);
-        const Tin* ed = reinterpret_cast<const Tin*>(&qd[q]);
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < E; ++i)
-          s += resample_weight(to_float<Tin>(et[i]), to_float<Tin>(ed[i]), wp, ep);
-        kahan_add(acc, s);
-      }
-    }
+    if (mode == kModeResidual)
+      span_sum_vec<Tin, kModeResidual>(zt, zd, a, b, wp, ep, lane, acc);
+    else
+      span_sum_vec<Tin, kModeTarget>(zt, zd, a, b, wp, ep, lane, acc);
   } else {
     for (int i = a + lane; i < b; i += 32) {
       const float z1 = to_float<Tin>(zt[i]);
@@ -795,6 +875,53 @@ __device__ void segment_sum(const Tin* __restrict__ zt, const Tin* __restrict__ 
   warp_two_sum(hi, lo);
   out_hi = hi;
   out_lo = lo;
+}
+
+// One warp scans the segment sums of a request: Z = their total, j = the
+// first segment whose running sum exceeds u*Z (a segment with positive sum),
+// P = the running sum before it; j = -1 if there is none. The sums may come
+// from other CTAs of the running grid: they are read through L2.
+__device__ void scan_segments(const ff* seg, int n_seg, float u, int lane, ff& Z_out, ff& P_out,
+                              int& j_out) {
+  const ff zero{0.f, 0.f};
+  ff run = zero;
+  for (int c = 0; c < n_seg; c += 32) {
+    ff v = (c + lane < n_seg) ? ff{__ldcg(&seg[c + lane].hi), __ldcg(&seg[c + lane].lo)} : zero;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const ff w = shfl_up_ff(v, o);
+      if (lane >= o) v = ff_add(w, v);
+    }
+    run = ff_add(run, shfl_ff(v, 31));
+  }
+  const ff Z = run;
+  const ff U = ff_mul(Z, ff{u, 0.f});
+  int j = -1;
+  ff P = zero;
+  run = zero;
+  for (int c = 0; c < n_seg && j < 0; c += 32) {
+    ff v = (c + lane < n_seg) ? ff{__ldcg(&seg[c + lane].hi), __ldcg(&seg[c + lane].lo)} : zero;
+    const bool own_pos = v.hi > 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const ff w = shfl_up_ff(v, o);
+      if (lane >= o) v = ff_add(w, v);
+    }
+    const ff incl = ff_add(run, v);
+    const ff prev_incl = shfl_up_ff(incl, 1);
+    const ff excl = lane == 0 ? run : prev_incl;  // running sum before this segment
+    const unsigned hit =
+        __ballot_sync(0xFFFFFFFFu, c + lane < n_seg && own_pos && ff_cmp(incl, U) > 0);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      j = c + l;
+      P = shfl_ff(excl, l);
+    }
+    run = ff_add(run, shfl_ff(v, 31));
+  }
+  Z_out = Z;
+  P_out = P;
+  j_out = j;
 }
 
 // The whole CTA (256 threads) draws request r's token: finds the segment
@@ -821,42 +948,9 @@ __device__ __noinline__ void pick_token(const Tin* __restrict__ tl, const Tin* _
   const ff zero{0.f, 0.f};
   for (int attempt = 0; attempt < 2; ++attempt) {
     if (warp == 0) {
-      // Z = running sum of the segment sums, 32 at a time
-      ff run = zero;
-      for (int c = 0; c < n_seg; c += 32) {
-        ff v = (c + lane < n_seg) ? seg[c + lane] : zero;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const ff w = shfl_up_ff(v, o);
-          if (lane >= o) v = ff_add(w, v);
-        }
-        run = ff_add(run, shfl_ff(v, 31));
-      }
-      const ff Z = run;
-      const ff U = ff_mul(Z, ff{d.u, 0.f});
-      int j = -1;
-      ff P = zero;
-      run = zero;
-      for (int c = 0; c < n_seg && j < 0; c += 32) {
-        ff v = (c + lane < n_seg) ? seg[c + lane] : zero;
-        const bool own_pos = v.hi > 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const ff w = shfl_up_ff(v, o);
-          if (lane >= o) v = ff_add(w, v);
-        }
-        const ff incl = ff_add(run, v);
-        const ff prev_incl = shfl_up_ff(incl, 1);
-        const ff excl = lane == 0 ? run : prev_incl;  // running sum before this segment
-        const unsigned hit =
-            __ballot_sync(0xFFFFFFFFu, c + lane < n_seg && own_pos && ff_cmp(incl, U) > 0);
-        if (hit) {
-          const int l = __ffs(hit) - 1;
-          j = c + l;
-          P = shfl_ff(excl, l);
-        }
-        run = ff_add(run, shfl_ff(v, 31));
-      }
+      ff Z, P;
+      int j;
+      scan_segments(seg, n_seg, d.u, lane, Z, P, j);
       if (lane == 0) {
         sh_Z = Z;
         sh_P = P;
@@ -1013,7 +1107,10 @@ __global__ void __launch_bounds__(kDecideWarps * 32, 6) k_decide(
   for (int sg = part * kDecideWarps + warp; sg < n_seg; sg += parts * kDecideWarps) {
     float hi, lo;
     segment_sum<Tin, VEC>(zt, zd, sg * kSeg, min(V, (sg + 1) * kSeg), wp, ep, lane, hi, lo);
-    if (lane == 0) ws.seg_sum[static_cast<long long>(r) * n_seg + sg] = ff_norm(hi, lo);
+    if (lane == 0) {
+      ws.seg_sum[static_cast<long long>(r) * n_seg + sg] = ff_norm(hi, lo);
+      __threadfence();  // before the part's ticket below
+    }
   }
   // 4. the last part to finish draws the token
   __syncthreads();
@@ -1025,6 +1122,242 @@ __global__ void __launch_bounds__(kDecideWarps * 32, 6) k_decide(
   if (!sh_last) return;
   __threadfence();
   pick_token<Tin, VEC>(tl, dl, V, n_seg, gamma, ep, ws, d, r, emitted, ties, status);
+}
+
+// ---------------------------------------------------------------------------
+// The decision pass for 16-byte aligned rows: k_desc, then k_resid
+// ---------------------------------------------------------------------------
+// k_desc: one CTA per request. It merges the request's rows, runs the ratio
+// tests, writes accepted lengths, tokens and probabilities, and the
+// descriptor of the token to draw after the block (mode kModeNone for an
+// invalid request: nothing to draw).
+template <typename Tin>
+__global__ void __launch_bounds__(kDecideWarps * 32) k_desc(
+    const Tin* __restrict__ tl, const Tin* __restrict__ dl, const int32_t* __restrict__ tokens,
+    const float* __restrict__ uniforms, int gamma, int V, int n_units, ExpParams ep, VerifyWs ws,
+    int32_t* __restrict__ accepted_len, int32_t* __restrict__ emitted,
+    float* __restrict__ probs_out, uint32_t* ties, int32_t* status) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  __shared__ RowStat sh_rs[2 * DSPARK_MAX_GAMMA + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x;
+  const int start = ws.req_row_start[r], end = ws.req_row_start[r + 1];
+  if (end == start) {  // invalid request (reported by k_plan): defined, in-bounds outputs
+    if (warp == 0) {
+      int32_t* em = emitted + static_cast<long long>(r) * (gamma + 1);
+      for (int k = lane; k <= gamma; k += 32) em[k] = -1;
+      if (probs_out) {
+        float* pr = probs_out + static_cast<long long>(r) * gamma * 2;
+        for (int k = lane; k < gamma; k += 32) pr[2 * k] = pr[2 * k + 1] = -1.f;
+      }
+      if (lane == 0) {
+        accepted_len[r] = 0;
+        ws.desc[r].mode = kModeNone;
+      }
+    }
+    return;
+  }
+  RatioIn rin{};
+  if (warp == 0)
+    rin = load_ratio_inputs<Tin>(tl, dl, tokens, uniforms, r, gamma, V, start,
+                                 (end - start - 1) / 2, ws, lane);
+  merge_rows_block(ws.tiles + static_cast<long long>(start) * n_units, end - start, n_units,
+                   sh_rs);
+  __syncthreads();
+  if (warp == 0)
+    ratio_tests<Tin>(rin, r, gamma, start, sh_rs, ep, ws, true, accepted_len, emitted, probs_out,
+                     ties, status, ws.desc + r, lane, end);
+}
+
+// k_resid: the residual (or bonus) weight sums of every request's draw, one
+// 2048-token segment per item, and the draw. Persistent, W warps per CTA and
+// one CTA per SM, like the streaming pass: warp w takes items w, w + GW, ...
+// (item = s * B + r for segment s of request r) through its own ring of 4 KB stages,
+// each holding 2 KB of the target row and 2 KB of the draft row (only the
+// target row for a bonus draw), fed by bulk copies; the ring runs on across
+// items. k_pick then draws each request's token from the segment sums.
+constexpr int kRowPart = kChunkBytes / 2;  // bytes of each row in one stage
+
+struct __align__(16) StageInfo {  // what a ring stage holds; written by lane 0
+  float nK, E_hi, E_lo, D_hi, D_lo;
+  int32_t mode;   // kModeResidual or kModeTarget
+  int32_t bytes;  // bytes of each row in the stage
+  int32_t last;   // the item's last stage
+  int32_t r, s;   // request and segment
+  int32_t pad[2];
+};
+static_assert(sizeof(StageInfo) == 48, "StageInfo layout");
+
+struct __align__(16) ResidCursor {  // a warp's producer position; lane 0's, in shared memory
+  StageInfo item;                   // parameters of the item being copied
+  long long pi;                     // the item
+  const char* p_t;                  // its target-row segment
+  const char* p_d;                  // its draft-row segment
+  int pc, n_st, ib, have;           // next stage, stages, bytes per row, an item is set up
+};
+
+template <typename Tin, int W, int STAGES>
+__global__ void __launch_bounds__(W * 32, 1)
+    k_resid(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int B, int gamma, int V,
+            int n_seg, ExpParams ep, VerifyWs ws, int32_t* __restrict__ emitted, uint32_t* ties,
+            int32_t* status) {
+  constexpr int RPL = kRowPart / 16 / 32;  // 16-byte vectors per lane and row part
+  constexpr int kSegBytes = kSeg * static_cast<int>(sizeof(Tin));
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* buf = smem + static_cast<size_t>(warp) * STAGES * kChunkBytes;
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(W) * STAGES * kChunkBytes) +
+      warp * STAGES;
+  StageInfo* info =
+      reinterpret_cast<StageInfo*>(smem + static_cast<size_t>(W) * STAGES * (kChunkBytes + 8)) +
+      warp * STAGES;
+  ResidCursor* curs = reinterpret_cast<ResidCursor*>(
+      smem + static_cast<size_t>(W) * STAGES * (kChunkBytes + 8 + sizeof(StageInfo)));
+  if (lane == 0) {
+    for (int st = 0; st < STAGES; ++st) mbar_init(&bars[st], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+
+  const long long row_bytes = static_cast<long long>(V) * sizeof(Tin);
+  const long long N = static_cast<long long>(B) * n_seg;
+  const long long GW = static_cast<long long>(gridDim.x) * W;
+
+  // producer cursor (lane 0): the item being copied and its next stage
+  ResidCursor& cu = curs[warp];
+  auto locate = [&]() {  // next item with something to draw, if any
+    cu.have = 0;
+    for (; cu.pi < N; cu.pi += GW) {
+      // segment-major: a warp's items fall in different segments, so that the
+      // segments rich in heavy tokens do not all land on the same warps
+      const int sg = static_cast<int>(cu.pi / B);
+      const int r = static_cast<int>(cu.pi - static_cast<long long>(sg) * B);
+      const ResampleDesc d = ws.desc[r];  // written by k_desc
+      if (d.mode != kModeResidual && d.mode != kModeTarget) continue;
+      const long long left = row_bytes - static_cast<long long>(sg) * kSegBytes;
+      cu.ib = static_cast<int>(left < kSegBytes ? left : kSegBytes);
+      cu.n_st = (cu.ib + kRowPart - 1) / kRowPart;
+      const long long off = static_cast<long long>(sg) * kSegBytes;
+      cu.p_t = reinterpret_cast<const char*>(tl) + d.t_row * row_bytes + off;
+      cu.p_d = reinterpret_cast<const char*>(dl) + d.d_row * row_bytes + off;
+      cu.item.nK = -static_cast<float>(d.K_t);
+      cu.item.E_hi = d.E_hi;
+      cu.item.E_lo = d.E_lo;
+      cu.item.D_hi = d.D_hi;
+      cu.item.D_lo = d.D_lo;
+      cu.item.mode = d.mode;
+      cu.item.r = r;
+      cu.item.s = sg;
+      cu.pc = 0;
+      cu.have = 1;
+      return;
+    }
+  };
+  auto issue = [&](int st) {  // lane 0, cu.have
+    const int bytes = min(kRowPart, cu.ib - cu.pc * kRowPart);
+    StageInfo& in = info[st];
+    in = cu.item;
+    in.bytes = bytes;
+    in.last = cu.pc == cu.n_st - 1;
+    const bool two = cu.item.mode == kModeResidual;
+    mbar_arrive_expect_tx(&bars[st], static_cast<uint32_t>(two ? 2 * bytes : bytes));
+    bulk_g2s(buf + st * kChunkBytes, cu.p_t + static_cast<long long>(cu.pc) * kRowPart,
+             static_cast<uint32_t>(bytes), &bars[st]);
+    if (two)
+      bulk_g2s(buf + st * kChunkBytes + kRowPart, cu.p_d + static_cast<long long>(cu.pc) * kRowPart,
+               static_cast<uint32_t>(bytes), &bars[st]);
+    if (++cu.pc == cu.n_st) {
+      cu.pi += GW;
+      locate();
+    }
+  };
+  int inflight = 0;
+  if (lane == 0) {
+    cu.pi = static_cast<long long>(blockIdx.x) * W + warp;
+    locate();
+    while (inflight < STAGES && cu.have) issue(inflight++);
+  }
+  inflight = __shfl_sync(0xFFFFFFFFu, inflight, 0);
+
+  int stage = 0;
+  uint32_t phase = 0;
+  LaneAcc acc;
+  while (inflight > 0) {
+    // every lane waits (each gets the barrier's acquire); the give-up decision is warp-uniform
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[stage], phase))) {
+      if (lane == 0) set_status(status, DSPARK_ERR_TIMEOUT);
+      for (int q = 0; q < inflight; ++q) {  // let the copies in flight land before leaving
+        int s2 = stage + q;
+        uint32_t p2 = phase;
+        if (s2 >= STAGES) {
+          s2 -= STAGES;
+          p2 ^= 1u;
+        }
+        (void)mbar_wait(&bars[s2], p2);
+      }
+      return;
+    }
+    const StageInfo in = info[stage];
+    const bool two = in.mode == kModeResidual;
+    uint4 v[2 * RPL];
+    const uint4* sp = reinterpret_cast<const uint4*>(buf + stage * kChunkBytes);
+#pragma unroll
+    for (int q = 0; q < RPL; ++q) {
+      const int idx = q * 32 + lane;
+      const bool ok = idx * 16 < in.bytes;
+      v[q] = ok ? sp[idx] : make_uint4(0u, 0u, 0u, 0u);
+      v[RPL + q] = (ok && two) ? sp[kRowPart / 16 + idx] : v[q];
+    }
+    __syncwarp();
+    const int freed = stage;
+    if (++stage == STAGES) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    --inflight;
+    if (lane == 0 && cu.have) {  // the ring was full: the freed stage is the next one to fill
+      fence_proxy_async();
+      issue(freed);
+      ++inflight;
+    }
+    inflight = __shfl_sync(0xFFFFFFFFu, inflight, 0);
+
+    const WeightParams wp{in.mode, in.nK, in.D_hi, in.D_lo, in.E_hi, in.E_lo};
+#pragma unroll
+    for (int q = 0; q < RPL; ++q) {
+      if ((q * 32 + lane) * 16 >= in.bytes) break;
+      float sum;
+      const bool light = two ? vec_weight_sum<Tin, kModeResidual>(v[q], v[RPL + q], wp, ep, sum)
+                             : vec_weight_sum<Tin, kModeTarget>(v[q], v[q], wp, ep, sum);
+      if (!light) sum = heavy_vec_sum<Tin>(v[q], v[RPL + q], wp, ep);
+      kahan_add(acc, sum);
+    }
+    if (in.last) {
+      float hi = acc.s, lo = -acc.comp;
+      warp_two_sum(hi, lo);
+      acc = LaneAcc();
+      if (lane == 0) ws.seg_sum[static_cast<long long>(in.r) * n_seg + in.s] = ff_norm(hi, lo);
+    }
+  }
+}
+
+// k_pick: one CTA per request draws the token after the block from the
+// segment sums k_resid wrote (nothing to do for an invalid request).
+template <typename Tin>
+__global__ void __launch_bounds__(kDecideWarps * 32)
+    k_pick(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int gamma, int V, int n_seg,
+           ExpParams ep, VerifyWs ws, int32_t* __restrict__ emitted, uint32_t* ties,
+           int32_t* status) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  const int r = blockIdx.x;
+  const ResampleDesc d = ws.desc[r];
+  if (d.mode != kModeResidual && d.mode != kModeTarget) return;
+  pick_token<Tin, true>(tl, dl, V, n_seg, gamma, ep, ws, d, r, emitted, ties, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -1045,6 +1378,10 @@ constexpr size_t tma_smem_bytes() {
   return static_cast<size_t>(kStreamWarps) * kStages * kChunkBytes +
          static_cast<size_t>(kStreamWarps) * kStages * sizeof(uint64_t);
 }
+constexpr size_t resid_smem_bytes() {
+  return tma_smem_bytes() + static_cast<size_t>(kStreamWarps) * kStages * sizeof(StageInfo) +
+         static_cast<size_t>(kStreamWarps) * sizeof(ResidCursor);
+}
 
 int device_setup(int& sms, int& decide_per_sm) {
   int dev = 0;
@@ -1062,8 +1399,15 @@ int device_setup(int& sms, int& decide_per_sm) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(tma_smem_bytes())) != cudaSuccess)
       return DSPARK_ERR_CUDA;
+    if (cudaFuncSetAttribute(k_resid<uint16_t, kStreamWarps, kStages>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(resid_smem_bytes())) != cudaSuccess ||
+        cudaFuncSetAttribute(k_resid<float, kStreamWarps, kStages>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(resid_smem_bytes())) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_decide<uint16_t, true>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_decide<uint16_t, false>,
                                                       kDecideWarps * 32, 0) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     s.decide_ctas_per_sm = occ > 0 ? occ : 1;
@@ -1151,21 +1495,33 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
 
-  // CTAs per request: as many as one wave of resident CTAs holds (at least
-  // one, and no more than there are segments to share)
-  int parts = static_cast<int>(static_cast<long long>(decide_per_sm) * sms / B);
-  parts = parts < 1 ? 1 : (parts > kDecideMaxParts ? kDecideMaxParts : parts);
-  const int seg_groups = (n_seg + kDecideWarps - 1) / kDecideWarps;
-  if (parts > seg_groups) parts = seg_groups;
-  const dim3 dgrid(static_cast<unsigned>(B) * static_cast<unsigned>(parts));
-  const cudaError_t e =
-      aligned ? launch_pdl(k_decide<Tin, true>, dgrid, kDecideWarps * 32, 0, stream, tl, dl,
-                           tokens, uni, B, gamma, V, n_units, n_seg, parts, ep, ws, acc, emitted,
-                           probs, tie_ctr, status)
-              : launch_pdl(k_decide<Tin, false>, dgrid, kDecideWarps * 32, 0, stream, tl, dl,
-                           tokens, uni, B, gamma, V, n_units, n_seg, parts, ep, ws, acc, emitted,
-                           probs, tie_ctr, status);
-  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (aligned) {
+    // decisions per request, then the residual segments by a persistent streamer
+    if (launch_pdl(k_desc<Tin>, B, kDecideWarps * 32, 0, stream, tl, dl, tokens, uni, gamma, V,
+                   n_units, ep, ws, acc, emitted, probs, tie_ctr, status) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    const long long items = static_cast<long long>(B) * n_seg;
+    const long long want = (items + kStreamWarps - 1) / kStreamWarps;
+    const int grid = static_cast<int>(want < sms ? want : sms);
+    if (launch_pdl(k_resid<Tin, kStreamWarps, kStages>, grid, kStreamWarps * 32,
+                   resid_smem_bytes(), stream, tl, dl, B, gamma, V, n_seg, ep, ws, emitted,
+                   tie_ctr, status) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    if (launch_pdl(k_pick<Tin>, B, kDecideWarps * 32, 0, stream, tl, dl, gamma, V, n_seg, ep, ws,
+                   emitted, tie_ctr, status) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+  } else {
+    // CTAs per request: as many as one wave of resident CTAs holds (at least
+    // one, and no more than there are segments to share)
+    int parts = static_cast<int>(static_cast<long long>(decide_per_sm) * sms / B);
+    parts = parts < 1 ? 1 : (parts > kDecideMaxParts ? kDecideMaxParts : parts);
+    const int seg_groups = (n_seg + kDecideWarps - 1) / kDecideWarps;
+    if (parts > seg_groups) parts = seg_groups;
+    if (launch_pdl(k_decide<Tin, false>, dim3(static_cast<unsigned>(B) * parts),
+                   kDecideWarps * 32, 0, stream, tl, dl, tokens, uni, B, gamma, V, n_units, n_seg,
+                   parts, ep, ws, acc, emitted, probs, tie_ctr, status) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+  }
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   if (ev && cudaEventRecord(ev[3], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;
