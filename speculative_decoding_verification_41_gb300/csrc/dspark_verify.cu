@@ -782,29 +782,46 @@ __device__ __forceinline__ float resample_weight(float zt, float zd, const Weigh
   return r;
 }
 
+// The logits of a 16-byte vector as floats (bf16 from their 32-bit words).
+template <typename Tin>
+__device__ __forceinline__ void unpack_vec(const uint4& q, float (&z)[16 / sizeof(Tin)]) {
+  if constexpr (sizeof(Tin) == 2) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      z[2 * k] = bf16_lo(w[k]);
+      z[2 * k + 1] = bf16_hi(w[k]);
+    }
+  } else {
+    z[0] = __uint_as_float(q.x);
+    z[1] = __uint_as_float(q.y);
+    z[2] = __uint_as_float(q.z);
+    z[3] = __uint_as_float(q.w);
+  }
+}
+
 template <typename Tin, int MODE>
 __device__ __forceinline__ bool vec_weight_sum(const uint4& qt, const uint4& qd,
                                                const WeightParams& w, const ExpParams& ep,
                                                float& sum) {
   constexpr int E = 16 / sizeof(Tin);
-  const Tin* et = reinterpret_cast<const Tin*>(&qt);
-  const Tin* ed = reinterpret_cast<const Tin*>(&qd);
-  float s = 0.f;
-  bool light = true;
+  float zt[E], zd[E];
+  unpack_vec<Tin>(qt, zt);
+  if constexpr (MODE == kModeResidual) unpack_vec<Tin>(qd, zd);
+  float s = 0.f, emax = 0.f;
 #pragma unroll
   for (int i = 0; i < E; ++i) {
-    const float e = exp_term(to_float<Tin>(et[i]), w.nK, ep);
+    const float e = exp_term(zt[i], w.nK, ep);
     if constexpr (MODE == kModeResidual) {
-      const float zd = to_float<Tin>(ed[i]);
-      const float edv = ex2_approx(fmaf(zd, ep.c_lo, fmaf(zd, ep.c_hi, w.E_hi)) + w.E_lo);
-      light = light && !(e > 0.00390625f);
+      const float edv = ex2_approx(fmaf(zd[i], ep.c_lo, fmaf(zd[i], ep.c_hi, w.E_hi)) + w.E_lo);
+      emax = fmaxf(emax, e);
       s += fmaxf(e - edv, 0.f);
     } else {
       s += e;
     }
   }
   sum = s;
-  return light;
+  return !(emax > 0.00390625f);
 }
 
 // The per-token sum of a vector holding a heavy token (rare).
@@ -883,10 +900,18 @@ __device__ void segment_sum(const Tin* __restrict__ zt, const Tin* __restrict__ 
 // from other CTAs of the running grid: they are read through L2.
 __device__ void scan_segments(const ff* seg, int n_seg, float u, int lane, ff& Z_out, ff& P_out,
                               int& j_out) {
+  constexpr int kHeld = 4;  // chunks of 32 sums kept in registers between the two passes
   const ff zero{0.f, 0.f};
+  auto load = [&](int c) {
+    return (c + lane < n_seg) ? ff{__ldcg(&seg[c + lane].hi), __ldcg(&seg[c + lane].lo)} : zero;
+  };
+  ff held[kHeld];
+#pragma unroll
+  for (int h = 0; h < kHeld; ++h) held[h] = load(32 * h);  // loads in flight together
+  auto chunk = [&](int c) { return c < 32 * kHeld ? held[c >> 5] : load(c); };
   ff run = zero;
   for (int c = 0; c < n_seg; c += 32) {
-    ff v = (c + lane < n_seg) ? ff{__ldcg(&seg[c + lane].hi), __ldcg(&seg[c + lane].lo)} : zero;
+    ff v = chunk(c);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const ff w = shfl_up_ff(v, o);
@@ -900,7 +925,7 @@ __device__ void scan_segments(const ff* seg, int n_seg, float u, int lane, ff& Z
   ff P = zero;
   run = zero;
   for (int c = 0; c < n_seg && j < 0; c += 32) {
-    ff v = (c + lane < n_seg) ? ff{__ldcg(&seg[c + lane].hi), __ldcg(&seg[c + lane].lo)} : zero;
+    ff v = chunk(c);
     const bool own_pos = v.hi > 0.f;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1177,7 +1202,6 @@ __global__ void __launch_bounds__(kDecideWarps * 32) k_desc(
 // each holding 2 KB of the target row and 2 KB of the draft row (only the
 // target row for a bonus draw), fed by bulk copies; the ring runs on across
 // items. k_pick then draws each request's token from the segment sums.
-constexpr int kRowPart = kChunkBytes / 2;  // bytes of each row in one stage
 
 struct __align__(16) StageInfo {  // what a ring stage holds; written by lane 0
   float nK, E_hi, E_lo, D_hi, D_lo;
@@ -1197,7 +1221,7 @@ struct __align__(16) ResidCursor {  // a warp's producer position; lane 0's, in 
   int pc, n_st, ib, have;           // next stage, stages, bytes per row, an item is set up
 };
 
-template <typename Tin, int W, int STAGES>
+template <typename Tin, int W, int STAGES, int kRowPart>
 __global__ void __launch_bounds__(W * 32, 1)
     k_resid(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int B, int gamma, int V,
             int n_seg, ExpParams ep, VerifyWs ws, int32_t* __restrict__ emitted, uint32_t* ties,
@@ -1206,15 +1230,16 @@ __global__ void __launch_bounds__(W * 32, 1)
   constexpr int kSegBytes = kSeg * static_cast<int>(sizeof(Tin));
   extern __shared__ __align__(1024) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  unsigned char* buf = smem + static_cast<size_t>(warp) * STAGES * kChunkBytes;
+  constexpr int kStage = 2 * kRowPart;  // target part, then draft part
+  unsigned char* buf = smem + static_cast<size_t>(warp) * STAGES * kStage;
   uint64_t* bars =
-      reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(W) * STAGES * kChunkBytes) +
+      reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(W) * STAGES * kStage) +
       warp * STAGES;
   StageInfo* info =
-      reinterpret_cast<StageInfo*>(smem + static_cast<size_t>(W) * STAGES * (kChunkBytes + 8)) +
+      reinterpret_cast<StageInfo*>(smem + static_cast<size_t>(W) * STAGES * (kStage + 8)) +
       warp * STAGES;
   ResidCursor* curs = reinterpret_cast<ResidCursor*>(
-      smem + static_cast<size_t>(W) * STAGES * (kChunkBytes + 8 + sizeof(StageInfo)));
+      smem + static_cast<size_t>(W) * STAGES * (kStage + 8 + sizeof(StageInfo)));
   if (lane == 0) {
     for (int st = 0; st < STAGES; ++st) mbar_init(&bars[st], 1);
     fence_barrier_init();
@@ -1265,10 +1290,10 @@ __global__ void __launch_bounds__(W * 32, 1)
     in.last = cu.pc == cu.n_st - 1;
     const bool two = cu.item.mode == kModeResidual;
     mbar_arrive_expect_tx(&bars[st], static_cast<uint32_t>(two ? 2 * bytes : bytes));
-    bulk_g2s(buf + st * kChunkBytes, cu.p_t + static_cast<long long>(cu.pc) * kRowPart,
+    bulk_g2s(buf + st * kStage, cu.p_t + static_cast<long long>(cu.pc) * kRowPart,
              static_cast<uint32_t>(bytes), &bars[st]);
     if (two)
-      bulk_g2s(buf + st * kChunkBytes + kRowPart, cu.p_d + static_cast<long long>(cu.pc) * kRowPart,
+      bulk_g2s(buf + st * kStage + kRowPart, cu.p_d + static_cast<long long>(cu.pc) * kRowPart,
                static_cast<uint32_t>(bytes), &bars[st]);
     if (++cu.pc == cu.n_st) {
       cu.pi += GW;
@@ -1304,7 +1329,7 @@ __global__ void __launch_bounds__(W * 32, 1)
     const StageInfo in = info[stage];
     const bool two = in.mode == kModeResidual;
     uint4 v[2 * RPL];
-    const uint4* sp = reinterpret_cast<const uint4*>(buf + stage * kChunkBytes);
+    const uint4* sp = reinterpret_cast<const uint4*>(buf + stage * kStage);
 #pragma unroll
     for (int q = 0; q < RPL; ++q) {
       const int idx = q * 32 + lane;
@@ -1327,9 +1352,10 @@ __global__ void __launch_bounds__(W * 32, 1)
     inflight = __shfl_sync(0xFFFFFFFFu, inflight, 0);
 
     const WeightParams wp{in.mode, in.nK, in.D_hi, in.D_lo, in.E_hi, in.E_lo};
+    const int n_vec = in.bytes == kRowPart ? RPL : (in.bytes / 16 - lane + 31) / 32;
 #pragma unroll
     for (int q = 0; q < RPL; ++q) {
-      if ((q * 32 + lane) * 16 >= in.bytes) break;
+      if (q >= n_vec) break;
       float sum;
       const bool light = two ? vec_weight_sum<Tin, kModeResidual>(v[q], v[RPL + q], wp, ep, sum)
                              : vec_weight_sum<Tin, kModeTarget>(v[q], v[q], wp, ep, sum);
@@ -1378,10 +1404,18 @@ constexpr size_t tma_smem_bytes() {
   return static_cast<size_t>(kStreamWarps) * kStages * kChunkBytes +
          static_cast<size_t>(kStreamWarps) * kStages * sizeof(uint64_t);
 }
+// k_resid: 16 warps per SM, each with a ring of 3 stages of 2 KB per row (32
+// warps with 1 KB parts measured slower: the per-stage work halves, its
+// overhead does not)
+constexpr int kResidWarps = 16;
+constexpr int kResidStages = 3;
+constexpr int kResidPart = 2048;
 constexpr size_t resid_smem_bytes() {
-  return tma_smem_bytes() + static_cast<size_t>(kStreamWarps) * kStages * sizeof(StageInfo) +
-         static_cast<size_t>(kStreamWarps) * sizeof(ResidCursor);
+  return static_cast<size_t>(kResidWarps) * kResidStages *
+             (2 * kResidPart + sizeof(uint64_t) + sizeof(StageInfo)) +
+         static_cast<size_t>(kResidWarps) * sizeof(ResidCursor);
 }
+static_assert(resid_smem_bytes() <= 227 * 1024, "shared memory of k_resid");
 
 int device_setup(int& sms, int& decide_per_sm) {
   int dev = 0;
@@ -1399,10 +1433,10 @@ int device_setup(int& sms, int& decide_per_sm) {
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(tma_smem_bytes())) != cudaSuccess)
       return DSPARK_ERR_CUDA;
-    if (cudaFuncSetAttribute(k_resid<uint16_t, kStreamWarps, kStages>,
+    if (cudaFuncSetAttribute(k_resid<uint16_t, kResidWarps, kResidStages, kResidPart>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(resid_smem_bytes())) != cudaSuccess ||
-        cudaFuncSetAttribute(k_resid<float, kStreamWarps, kStages>,
+        cudaFuncSetAttribute(k_resid<float, kResidWarps, kResidStages, kResidPart>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(resid_smem_bytes())) != cudaSuccess)
       return DSPARK_ERR_CUDA;
@@ -1501,9 +1535,9 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
                    n_units, ep, ws, acc, emitted, probs, tie_ctr, status) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     const long long items = static_cast<long long>(B) * n_seg;
-    const long long want = (items + kStreamWarps - 1) / kStreamWarps;
+    const long long want = (items + kResidWarps - 1) / kResidWarps;
     const int grid = static_cast<int>(want < sms ? want : sms);
-    if (launch_pdl(k_resid<Tin, kStreamWarps, kStages>, grid, kStreamWarps * 32,
+    if (launch_pdl(k_resid<Tin, kResidWarps, kResidStages, kResidPart>, grid, kResidWarps * 32,
                    resid_smem_bytes(), stream, tl, dl, B, gamma, V, n_seg, ep, ws, emitted,
                    tie_ctr, status) != cudaSuccess)
       return DSPARK_ERR_CUDA;
