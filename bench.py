@@ -390,8 +390,8 @@ def native_arm(args):
                      "peak_source": peak_src},
         "roofline_call": {"bound": "hbm", "achieved": achieved_call, "peak": peak,
                           "unit": "GB/s", "frac": achieved_call / peak,
-                          "scope": "whole dspark_verify call (k_plan + k_rowstats_tma + "
-                                   "k_decide), median CUDA-event time, logit bytes only"},
+                          "scope": "whole dspark_verify call (k_plan, k_rowstats_tma, k_desc, "
+                                   "k_resid, k_pick), median CUDA-event time, logit bytes only"},
         "timing_ms": {"verify_median": v_med, "verify_p10": float(np.percentile(verify_ms, 10)),
                       "verify_p90": float(np.percentile(verify_ms, 90)),
                       "schedule_median": statistics.median(sched_ms),
@@ -406,11 +406,12 @@ def native_arm(args):
 
 
 # DRAM traffic of the streaming kernel from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), scaled per logit byte; valid only for the kernel source it
-# was taken on (profiles/k_rowstats_tma_b32_g16_v129280_bf16.md).
+# dram__bytes_write.sum), scaled per logit byte; valid only for the sources the
+# kernel is built from (the headers hashed below), as they were at the capture
+# (profiles/k_rowstats_tma_b32_g16_v129280_bf16.md).
 TRAFFIC_CAPTURE = {
-    "sources_sha256": "23c5715a507282ba05da728b1011706d7ea0982f0769e115235c6c25d4727eef",
-    "dram_bytes": 273079808 + 3390464,  # read + write, one launch at B = 32
+    "sources_sha256": "e987890f74a4dc51dd8f6d5a0a9a68a8d792a35be3edb88e81552a7ac6ba950d",
+    "dram_bytes": 273103872 + 3789824,  # read + write, one launch at B = 32
     "logit_bytes": 273039360,
 }
 
@@ -419,7 +420,7 @@ def kernel_sources_sha256() -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_41_gb300", "csrc")
-    for f in ("dspark_verify.cu", "dspark_common.cuh"):
+    for f in ("dspark_rowstats.cuh", "dspark_verify_types.cuh", "dspark_common.cuh"):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()
 
