@@ -67,6 +67,10 @@ def _setup(lib):
     lib.oracle_schedule.argtypes = [
         ctypes.POINTER(ctypes.c_float), c_f64p, ctypes.c_int64, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_int32, c_i32p, c_f64p, c_i64p, c_i32p]
+    lib.oracle_acceptance.restype = ctypes.c_int
+    lib.oracle_acceptance.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, c_i32p, ctypes.c_double, ctypes.c_int32,
+        ctypes.c_int32, ctypes.c_int64, c_i64p, c_i64p, c_f64p, ctypes.c_int32]
     lib.oracle_schedule_topk.restype = ctypes.c_int
     lib.oracle_schedule_topk.argtypes = [
         ctypes.POINTER(ctypes.c_float), ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, c_i32p,
@@ -181,6 +185,34 @@ def schedule(confidences, step_time, early_stop=True, lib=None):
         raise OracleError(f"oracle_schedule returned {rc}")
     return {"verify_len": ell, "theta_best": theta.value, "n_admitted": n_adm.value,
             "near_ties": ties.value}
+
+
+def acceptance(target_logits, draft_logits, verify_len, temperature, gamma,
+               target_row_off=None, draft_row_off=None, nthreads=1, lib=None):
+    """Acceptance probability sum_v min(p_t^k(v), p_d^k(v)) of every verified
+    position k = 1..l_r (equation 8), from the same row layout as verify.
+    Returns rates [B, gamma] float64, -1 beyond each l_r."""
+    lib = lib or load()
+    tl, dtype = _logits_and_dtype(target_logits)
+    dl, dtype_d = _logits_and_dtype(draft_logits)
+    if dtype != dtype_d:
+        raise TypeError("target and draft logits must share a dtype")
+    V = tl.shape[-1]
+    if dl.shape[-1] != V:
+        raise ValueError("vocabulary mismatch")
+    ell = np.ascontiguousarray(verify_len, dtype=np.int32).reshape(-1)
+    B = ell.shape[0]
+    toff = None if target_row_off is None else np.ascontiguousarray(target_row_off, dtype=np.int64)
+    doff = None if draft_row_off is None else np.ascontiguousarray(draft_row_off, dtype=np.int64)
+    rates = np.zeros((B, gamma), np.float64)
+    rc = lib.oracle_acceptance(
+        tl.ctypes.data, dl.ctypes.data, dtype, _ptr(ell, ctypes.c_int32), float(temperature), B,
+        gamma, V, None if toff is None else _ptr(toff, ctypes.c_int64),
+        None if doff is None else _ptr(doff, ctypes.c_int64), _ptr(rates, ctypes.c_double),
+        int(nthreads or 1))
+    if rc != 0:
+        raise OracleError(f"oracle_acceptance returned {rc}")
+    return rates
 
 
 def schedule_topk(confidences, K: int, lib=None):

@@ -274,6 +274,61 @@ int oracle_verify(const void* target_logits, const void* draft_logits,
   return status;
 }
 
+/*
+ * Acceptance probability of every verified draft position: the DSpark paper's
+ * equation 8, P(accept x_k) = sum_v min(p_t^k(v), p_d^k(v)) = 1 - TV(p_t^k,
+ * p_d^k), the label of its confidence head (section 3.2.1). For request r and
+ * k = 1..l_r: the temperature-scaled softmaxes of target row k and draft row
+ * k, and the sum of their minima in ascending token order, into
+ * rates[r*gamma + k-1]; positions beyond l_r get -1.
+ */
+int oracle_acceptance(const void* target_logits, const void* draft_logits, int dtype,
+                      const int32_t* verify_len, double temperature, int32_t B, int32_t gamma,
+                      int64_t V, const int64_t* t_off, const int64_t* d_off, double* rates,
+                      int32_t nthreads) {
+  if (!target_logits || !draft_logits || !verify_len || !rates) return ORACLE_ERR_ARG;
+  if (B < 0 || gamma < 1 || V < 1 || !(temperature > 0.0) || !isfinite(temperature))
+    return ORACLE_ERR_ARG;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16 && dtype != ORACLE_F64) return ORACLE_ERR_ARG;
+  for (int32_t r = 0; r < B; ++r)
+    if (verify_len[r] < 0 || verify_len[r] > gamma) return ORACLE_ERR_DATA;
+  int status = ORACLE_OK;
+  if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+  {
+    double* pt = (double*)malloc(sizeof(double) * (size_t)V);
+    double* pd = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!pt || !pd) {
+#pragma omp critical
+      status = ORACLE_ERR_NOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int32_t r = 0; r < B; ++r) {
+        const int64_t t0 = t_off ? t_off[r] : (int64_t)r * (gamma + 1);
+        const int64_t d0 = d_off ? d_off[r] : (int64_t)r * gamma;
+        for (int32_t k = 0; k < gamma; ++k) {
+          double rate = -1.0;
+          if (k < verify_len[r]) {
+            int rc = softmax_row(target_logits, dtype, t0 + k, V, temperature, pt);
+            if (!rc) rc = softmax_row(draft_logits, dtype, d0 + k, V, temperature, pd);
+            if (rc) {
+#pragma omp critical
+              if (status == ORACLE_OK) status = rc;
+            } else {
+              rate = 0.0;
+              for (int64_t v = 0; v < V; ++v) rate += pt[v] < pd[v] ? pt[v] : pd[v];
+            }
+          }
+          rates[(int64_t)r * gamma + k] = rate;
+        }
+      }
+    }
+    free(pt);
+    free(pd);
+  }
+  return status;
+}
+
 /* Temperature-scaled softmax of a single row, exposed for the tests. */
 int oracle_softmax_row(const void* logits, int dtype, int64_t V,
                        double temperature, double* p_out) {
