@@ -302,6 +302,23 @@ def native_arm(args):
     pass_ms = {name: statistics.median([e[j].elapsed_time(e[j + 1]) for e in pev])
                for j, name in enumerate(("k_plan", "k_rowstats_tma", "decision"))}
 
+    # the acceptance probabilities of every verified position (a separate call,
+    # not part of the step): its own median over a few calls
+    acc_ws = torch.empty(binding.acceptance_workspace_bytes(vi.B, vi.gamma, vi.V),
+                         dtype=torch.uint8, device=dev)
+    acc_rates = torch.empty(vi.B, vi.gamma, dtype=torch.float32, device=dev)
+    acc_ms = []
+    for i in range(6):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        binding.dspark_acceptance(vi.target_logits, vi.draft_logits, sbuf.verify_len,
+                                  vi.temperature, vi.gamma, rates=acc_rates, workspace=acc_ws)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i > 0:
+            acc_ms.append(a0.elapsed_time(a1))
+    del acc_ws
+
     # end to end: pinned host buffers -> device, both calls, results back
     e2e = None
     if args.e2e_steps > 0:
@@ -395,7 +412,8 @@ def native_arm(args):
         "timing_ms": {"verify_median": v_med, "verify_p10": float(np.percentile(verify_ms, 10)),
                       "verify_p90": float(np.percentile(verify_ms, 90)),
                       "schedule_median": statistics.median(sched_ms),
-                      "passes_median": pass_ms},
+                      "passes_median": pass_ms,
+                      "acceptance_median": statistics.median(acc_ms)},
         "gpu_launches": args.steps * 7,  # per step: k_sched_rank, k_sched_sweep, k_plan, k_rowstats_tma, k_desc, k_resid, k_pick
         "near_ties": int(vbuf.near_tie_count.item()),
         "clocks": clk,

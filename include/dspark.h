@@ -92,6 +92,13 @@ typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
    DSPARK_ALIGN256((size_t)(B) * DSPARK_SEGS_PER_ROW(V) * 8u) +               \
    DSPARK_ALIGN256((size_t)(B) * 4u))
 
+/* Workspace of dspark_acceptance, in bytes: dspark_verify's workspace, then
+   one job record per position and its per-segment sums. */
+#define DSPARK_ACCEPTANCE_WS_BYTES(B, gamma, V)                               \
+  (DSPARK_VERIFY_WS_BYTES(B, gamma, V) +                                      \
+   DSPARK_ALIGN256((size_t)(B) * (size_t)(gamma) * 64u) +                     \
+   DSPARK_ALIGN256((size_t)(B) * (size_t)(gamma) * DSPARK_SEGS_PER_ROW(V) * 8u))
+
 /* Workspace of dspark_schedule, in bytes: two (key, index) buffers for the
    sort, per-request lengths and a header. */
 #define DSPARK_SCHEDULE_WS_BYTES(R, gamma)                                    \
@@ -252,6 +259,31 @@ int dspark_schedule_topk(const float* confidences, const int32_t* capacity, int3
 int dspark_schedule_threshold(const float* confidences, float threshold, int32_t R,
                               int32_t gamma, int32_t* verify_len, int32_t* device_status,
                               struct CUstream_st* stream);
+
+/*
+ * dspark_acceptance -- the acceptance probability of every verified draft
+ * position (DSpark paper, equation 8: P(accept x_k) = sum_v min(p_t^k(v),
+ * p_d^k(v)) = 1 - TV(p_t^k, p_d^k); section 3.2.1 trains the confidence head
+ * on it). For request r and k = 1..l_r: the temperature-scaled softmaxes of
+ * target row k and draft row k, as in dspark_verify.
+ *
+ * Arguments are those of dspark_verify's logits, lengths and layout
+ * (target_logits, draft_logits, verify_len, temperature, dtype, B, gamma, V,
+ * target_row_off, draft_row_off), plus
+ *   rates         out [B][gamma] float32: rates[r][k-1] for k <= l_r, -1
+ *                 beyond (and for every position of an invalid request).
+ *   device_status out [1] int32 (required), as in dspark_verify.
+ *   workspace     at least DSPARK_ACCEPTANCE_WS_BYTES(B, gamma, V) bytes,
+ *                 256-byte aligned; no initial contents needed.
+ * It reads every verified row pair twice (the statistics pass, then the
+ * minima), so it costs about two streaming passes; dspark_verify does not
+ * compute it.
+ */
+int dspark_acceptance(const void* target_logits, const void* draft_logits,
+                      const int32_t* verify_len, float temperature, int32_t dtype, int32_t B,
+                      int32_t gamma, int32_t V, const int64_t* target_row_off,
+                      const int64_t* draft_row_off, float* rates, int32_t* device_status,
+                      void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /* Size of the library-owned scratch array behind dspark_verify_static. */
 #define DSPARK_STATIC_WS_BYTES ((size_t)16u << 20)

@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_CUDA
                 3: "DSPARK_ERR_WORKSPACE", 4: "DSPARK_ERR_TIMEOUT", 5: "DSPARK_ERR_BAD_DATA",
                 6: "DSPARK_ERR_TOO_LARGE"}
 DSPARK_F32, DSPARK_BF16 = 0, 1
-EXPORTED = ("dspark_verify", "dspark_schedule", "dspark_schedule_capacity",
+EXPORTED = ("dspark_verify", "dspark_acceptance", "dspark_schedule", "dspark_schedule_capacity",
             "dspark_schedule_topk", "dspark_schedule_threshold", "dspark_verify_static",
             "dspark_verify_timed")
 
@@ -65,6 +65,12 @@ def verify_workspace_bytes(B: int, gamma: int, V: int) -> int:
             + _a256(B * 64) + _a256(B * segs * 8) + _a256(B * 4))
 
 
+def acceptance_workspace_bytes(B: int, gamma: int, V: int) -> int:
+    """Python statement of DSPARK_ACCEPTANCE_WS_BYTES (include/dspark.h)."""
+    segs = _cdiv(V, _CONSTS["DSPARK_RESAMPLE_SEG"])
+    return verify_workspace_bytes(B, gamma, V) + _a256(B * gamma * 64) + _a256(B * gamma * segs * 8)
+
+
 def schedule_workspace_bytes(R: int, gamma: int) -> int:
     """Python statement of DSPARK_SCHEDULE_WS_BYTES (include/dspark.h)."""
     n = R * gamma
@@ -91,6 +97,9 @@ def load(path: Optional[str] = None):
         lib.dspark_verify.restype = ctypes.c_int
         lib.dspark_verify.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp, vp, vp,
                                       vp, vp, vp, vp, sz, vp]
+        lib.dspark_acceptance.restype = ctypes.c_int
+        lib.dspark_acceptance.argtypes = [vp, vp, vp, f32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                          sz, vp]
         lib.dspark_verify_timed.restype = ctypes.c_int
         lib.dspark_verify_timed.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp, vp,
                                             vp, vp, vp, vp, vp, sz, vp, vp]
@@ -216,6 +225,53 @@ def dspark_verify(target_logits: torch.Tensor, draft_logits: torch.Tensor,
         if st != 0:
             raise DsparkError("dspark_verify (device)", st)
     return out
+
+
+def dspark_acceptance(target_logits: torch.Tensor, draft_logits: torch.Tensor,
+                      verify_len: torch.Tensor, temperature: float, gamma: int,
+                      target_row_off: Optional[torch.Tensor] = None,
+                      draft_row_off: Optional[torch.Tensor] = None, *,
+                      rates: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None,
+                      check: bool = False) -> dict:
+    """Acceptance probability sum_v min(p_t^k, p_d^k) of every verified position
+    (equation 8) through libdspark. Returns rates [B, gamma] float32 (-1 beyond
+    each l_r) and device_status [1] (device tensors)."""
+    dev = target_logits.device
+    if target_logits.dtype == torch.bfloat16:
+        dtype = DSPARK_BF16
+    elif target_logits.dtype == torch.float32:
+        dtype = DSPARK_F32
+    else:
+        raise ValueError(f"logits must be bfloat16 or float32, got {target_logits.dtype}")
+    _require_cuda("target_logits", target_logits)
+    _require_cuda("draft_logits", draft_logits, target_logits.dtype, dev)
+    _require_cuda("verify_len", verify_len, torch.int32, dev)
+    if (target_row_off is None) != (draft_row_off is None):
+        raise ValueError("pass both row-offset tensors or neither")
+    if target_row_off is not None:
+        _require_cuda("target_row_off", target_row_off, torch.int64, dev)
+        _require_cuda("draft_row_off", draft_row_off, torch.int64, dev)
+    B = verify_len.shape[0]
+    V = target_logits.shape[-1]
+    out = rates if rates is not None else torch.empty(B, gamma, dtype=torch.float32, device=dev)
+    ws_bytes = acceptance_workspace_bytes(B, gamma, V)
+    ws = workspace if workspace is not None else torch.empty(ws_bytes, dtype=torch.uint8,
+                                                             device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib = load()
+    with torch.cuda.device(dev):
+        rc = lib.dspark_acceptance(_ptr(target_logits), _ptr(draft_logits), _ptr(verify_len),
+                                   float(temperature), dtype, B, gamma, V, _ptr(target_row_off),
+                                   _ptr(draft_row_off), _ptr(out), _ptr(status), _ptr(ws),
+                                   ws.numel(), _stream_handle(stream))
+    if rc != 0:
+        raise DsparkError("dspark_acceptance", rc)
+    if check:
+        torch.cuda.synchronize(dev)
+        if int(status.item()) != 0:
+            raise DsparkError("dspark_acceptance (device)", int(status.item()))
+    return {"rates": out, "device_status": status}
 
 
 class ScheduleBuffers:

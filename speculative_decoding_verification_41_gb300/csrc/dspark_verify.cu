@@ -48,6 +48,27 @@
 
 namespace dspark {
 
+struct __align__(16) ResampleDesc {
+  int64_t t_row;  // global row of the target distribution sampled from
+  int64_t d_row;  // global draft row (residual mode)
+  int32_t K_t;    // exponent reference of the target row
+  float D_hi;     // residual: log2(p_t/p_d)(v) = (z_t - z_d)*c - D, D = D_hi + D_lo
+  float D_lo;
+  float u;        // resample uniform
+  int32_t mode;   // 0 nothing to do, 1 residual, 2 target distribution
+  int32_t m;      // accepted count: position of the sampled token
+  float E_hi;     // residual: D - K_t = E_hi + E_lo, so that p_d/p_t = 2^(z_d*c + E) / e_t
+  float E_lo;
+  float S_hi;     // acceptance jobs: the target row's sum_v 2^(z_v*c - K_t)
+  float S_lo;
+  int32_t pad[2];
+};
+static_assert(sizeof(ResampleDesc) == 64, "ResampleDesc layout");
+
+// kModeMin: the acceptance probability's sum_v min(e_t(v), e_d(v)) (a job of
+// dspark_acceptance, not a draw)
+enum { kModeNone = 0, kModeResidual = 1, kModeTarget = 2, kModeMin = 3 };
+
 // ---------------------------------------------------------------------------
 // k_plan
 // ---------------------------------------------------------------------------
@@ -381,7 +402,8 @@ __device__ void ratio_tests(const RatioIn& in, int r, int gamma, int start, cons
       d.u = 0.f;
     }
     d.m = m;
-    for (int i = 0; i < 4; ++i) d.pad[i] = 0;
+    for (int i = 0; i < 2; ++i) d.pad[i] = 0;
+    d.S_hi = d.S_lo = 0.f;
     d.E_hi = d.E_lo = 0.f;
     if (m < ell) {
       d.mode = kModeResidual;
@@ -448,8 +470,9 @@ __device__ __forceinline__ float one_minus_exp_neg_small(float y) {
 __device__ __forceinline__ float resample_weight(float zt, float zd, const WeightParams& w,
                                                  const ExpParams& ep) {
   const float e = exp_term(zt, w.nK, ep);
-  if (w.mode != kModeResidual) return e;
+  if (w.mode == kModeTarget) return e;
   const float ed = ex2_approx(fmaf(zd, ep.c_lo, fmaf(zd, ep.c_hi, w.E_hi)) + w.E_lo);
+  if (w.mode == kModeMin) return fminf(e, ed);  // no cancellation: a minimum
   float r = fmaxf(e - ed, 0.f);
   if (e > 0.00390625f) {  // rare: a heavy token
     const float dz = zt - zd;
@@ -487,7 +510,7 @@ __device__ __forceinline__ bool vec_weight_sum(const uint4& qt, const uint4& qd,
   constexpr int E = 16 / sizeof(Tin);
   float zt[E], zd[E];
   unpack_vec<Tin>(qt, zt);
-  if constexpr (MODE == kModeResidual) unpack_vec<Tin>(qd, zd);
+  if constexpr (MODE != kModeTarget) unpack_vec<Tin>(qd, zd);
   float s = 0.f, emax = 0.f;
 #pragma unroll
   for (int i = 0; i < E; ++i) {
@@ -496,6 +519,9 @@ __device__ __forceinline__ bool vec_weight_sum(const uint4& qt, const uint4& qd,
       const float edv = ex2_approx(fmaf(zd[i], ep.c_lo, fmaf(zd[i], ep.c_hi, w.E_hi)) + w.E_lo);
       emax = fmaxf(emax, e);
       s += fmaxf(e - edv, 0.f);
+    } else if constexpr (MODE == kModeMin) {
+      const float edv = ex2_approx(fmaf(zd[i], ep.c_lo, fmaf(zd[i], ep.c_hi, w.E_hi)) + w.E_lo);
+      s += fminf(e, edv);
     } else {
       s += e;
     }
@@ -534,7 +560,7 @@ __device__ __forceinline__ void span_sum_vec(const Tin* __restrict__ zt,
     for (int q = 0; q < NB; ++q) {
       const int vi = v0 + 32 * q;
       qt[q] = vi < v_end ? __ldg(vt + vi) : make_uint4(0u, 0u, 0u, 0u);
-      if constexpr (MODE == kModeResidual)
+      if constexpr (MODE != kModeTarget)
         qd[q] = vi < v_end ? __ldg(vd + vi) : make_uint4(0u, 0u, 0u, 0u);
       else
         qd[q] = qt[q];
@@ -559,12 +585,14 @@ __device__ void segment_sum(const Tin* __restrict__ zt, const Tin* __restrict__ 
   if constexpr (VEC) {
     if (mode == kModeResidual)
       span_sum_vec<Tin, kModeResidual>(zt, zd, a, b, wp, ep, lane, acc);
+    else if (mode == kModeMin)
+      span_sum_vec<Tin, kModeMin>(zt, zd, a, b, wp, ep, lane, acc);
     else
       span_sum_vec<Tin, kModeTarget>(zt, zd, a, b, wp, ep, lane, acc);
   } else {
     for (int i = a + lane; i < b; i += 32) {
       const float z1 = to_float<Tin>(zt[i]);
-      const float z2 = mode == kModeResidual ? to_float<Tin>(zd[i]) : z1;
+      const float z2 = mode != kModeTarget ? to_float<Tin>(zd[i]) : z1;
       kahan_add(acc, resample_weight(z1, z2, wp, ep));
     }
   }
@@ -875,9 +903,11 @@ __global__ void __launch_bounds__(kDecideWarps * 32) k_desc(
                      ties, status, ws.desc + r, lane, end);
 }
 
-// k_resid: the residual (or bonus) weight sums of every request's draw, one
-// 2048-token segment per item, and the draw. Persistent, W warps per CTA and
-// one CTA per SM, like the streaming pass: warp w takes items w, w + GW, ...
+// k_resid: per 2048-token segment, the weight sums of a list of jobs (one
+// row pair each): for dspark_verify the residual (or bonus) weights of every
+// request's draw, for dspark_acceptance the minima of every verified position.
+// Persistent, W warps per CTA and one CTA per SM, like the streaming pass:
+// warp w takes items w, w + GW, ...
 // (item = s * B + r for segment s of request r) through its own ring of 4 KB stages,
 // each holding 2 KB of the target row and 2 KB of the draft row (only the
 // target row for a bonus draw), fed by bulk copies; the ring runs on across
@@ -903,9 +933,10 @@ struct __align__(16) ResidCursor {  // a warp's producer position; lane 0's, in 
 
 template <typename Tin, int W, int STAGES, int kRowPart>
 __global__ void __launch_bounds__(W * 32, 1)
-    k_resid(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int B, int gamma, int V,
-            int n_seg, ExpParams ep, VerifyWs ws, int32_t* __restrict__ emitted, uint32_t* ties,
+    k_resid(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int n_jobs, int V, int n_seg,
+            ExpParams ep, const ResampleDesc* __restrict__ jobs, ff* __restrict__ sums,
             int32_t* status) {
+  const int B = n_jobs;
   constexpr int RPL = kRowPart / 16 / 32;  // 16-byte vectors per lane and row part
   constexpr int kSegBytes = kSeg * static_cast<int>(sizeof(Tin));
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -941,8 +972,8 @@ __global__ void __launch_bounds__(W * 32, 1)
       // segments rich in heavy tokens do not all land on the same warps
       const int sg = static_cast<int>(cu.pi / B);
       const int r = static_cast<int>(cu.pi - static_cast<long long>(sg) * B);
-      const ResampleDesc d = ws.desc[r];  // written by k_desc
-      if (d.mode != kModeResidual && d.mode != kModeTarget) continue;
+      const ResampleDesc d = jobs[r];  // written by the previous kernel
+      if (d.mode != kModeResidual && d.mode != kModeTarget && d.mode != kModeMin) continue;
       const long long left = row_bytes - static_cast<long long>(sg) * kSegBytes;
       cu.ib = static_cast<int>(left < kSegBytes ? left : kSegBytes);
       cu.n_st = (cu.ib + kRowPart - 1) / kRowPart;
@@ -968,7 +999,7 @@ __global__ void __launch_bounds__(W * 32, 1)
     in = cu.item;
     in.bytes = bytes;
     in.last = cu.pc == cu.n_st - 1;
-    const bool two = cu.item.mode == kModeResidual;
+    const bool two = cu.item.mode != kModeTarget;
     mbar_arrive_expect_tx(&bars[st], static_cast<uint32_t>(two ? 2 * bytes : bytes));
     bulk_g2s(buf + st * kStage, cu.p_t + static_cast<long long>(cu.pc) * kRowPart,
              static_cast<uint32_t>(bytes), &bars[st]);
@@ -1007,7 +1038,7 @@ __global__ void __launch_bounds__(W * 32, 1)
       return;
     }
     const StageInfo in = info[stage];
-    const bool two = in.mode == kModeResidual;
+    const bool two = in.mode != kModeTarget;
     uint4 v[2 * RPL];
     const uint4* sp = reinterpret_cast<const uint4*>(buf + stage * kStage);
 #pragma unroll
@@ -1037,8 +1068,13 @@ __global__ void __launch_bounds__(W * 32, 1)
     for (int q = 0; q < RPL; ++q) {
       if (q >= n_vec) break;
       float sum;
-      const bool light = two ? vec_weight_sum<Tin, kModeResidual>(v[q], v[RPL + q], wp, ep, sum)
-                             : vec_weight_sum<Tin, kModeTarget>(v[q], v[q], wp, ep, sum);
+      bool light = true;
+      if (in.mode == kModeResidual)
+        light = vec_weight_sum<Tin, kModeResidual>(v[q], v[RPL + q], wp, ep, sum);
+      else if (in.mode == kModeMin)
+        (void)vec_weight_sum<Tin, kModeMin>(v[q], v[RPL + q], wp, ep, sum);
+      else
+        (void)vec_weight_sum<Tin, kModeTarget>(v[q], v[q], wp, ep, sum);
       if (!light) sum = heavy_vec_sum<Tin>(v[q], v[RPL + q], wp, ep);
       kahan_add(acc, sum);
     }
@@ -1046,7 +1082,7 @@ __global__ void __launch_bounds__(W * 32, 1)
       float hi = acc.s, lo = -acc.comp;
       warp_two_sum(hi, lo);
       acc = LaneAcc();
-      if (lane == 0) ws.seg_sum[static_cast<long long>(in.r) * n_seg + in.s] = ff_norm(hi, lo);
+      if (lane == 0) sums[static_cast<long long>(in.r) * n_seg + in.s] = ff_norm(hi, lo);
     }
   }
 }
@@ -1064,6 +1100,98 @@ __global__ void __launch_bounds__(kDecideWarps * 32)
   const ResampleDesc d = ws.desc[r];
   if (d.mode != kModeResidual && d.mode != kModeTarget) return;
   pick_token<Tin, true>(tl, dl, V, n_seg, gamma, ep, ws, d, r, emitted, ties, status);
+}
+
+// ---------------------------------------------------------------------------
+// dspark_acceptance: sum_v min(p_t^k, p_d^k) for every verified position
+// ---------------------------------------------------------------------------
+// k_rate_desc: one CTA per request merges its rows and writes one job per
+// position: the row pair, K_t, E = D - K_t and the target row's sum S_t, so that
+// the rate is sum_v min(e_t(v), e_d(v)) / S_t with e_d = 2^(z_d*c + E).
+// Positions beyond l_r (and every position of an invalid request) get no job.
+__global__ void __launch_bounds__(kDecideWarps * 32)
+    k_rate_desc(int gamma, int n_units, VerifyWs ws, ResampleDesc* __restrict__ jobs,
+                int32_t* status) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  __shared__ RowStat sh_rs[2 * DSPARK_MAX_GAMMA + 1];
+  const int r = blockIdx.x;
+  const int start = ws.req_row_start[r], end = ws.req_row_start[r + 1];
+  const int ell = end > start ? (end - start - 1) / 2 : 0;
+  if (end > start)
+    merge_rows_block(ws.tiles + static_cast<long long>(start) * n_units, end - start, n_units,
+                     sh_rs);
+  __syncthreads();
+  for (int k = threadIdx.x; k < gamma; k += blockDim.x) {
+    ResampleDesc d{};
+    d.mode = kModeNone;
+    if (k < ell) {
+      const RowStat st = sh_rs[k], sd = sh_rs[ell + 1 + k];
+      if (!st.ok || !sd.ok) {
+        set_status(status, DSPARK_ERR_BAD_DATA);
+      } else {
+        const double D = static_cast<double>(st.K - sd.K) +
+                         log2((static_cast<double>(st.S_hi) + st.S_lo) /
+                              (static_cast<double>(sd.S_hi) + sd.S_lo));
+        const double E = D - static_cast<double>(st.K);
+        d.t_row = ws.row_list[start + k] >> 1;
+        d.d_row = ws.row_list[start + ell + 1 + k] >> 1;
+        d.K_t = st.K;
+        d.E_hi = static_cast<float>(E);
+        d.E_lo = static_cast<float>(E - static_cast<double>(d.E_hi));
+        d.S_hi = st.S_hi;
+        d.S_lo = st.S_lo;
+        d.m = k;
+        d.mode = kModeMin;
+      }
+    }
+    jobs[static_cast<long long>(r) * gamma + k] = d;
+  }
+}
+
+// The minima's segment sums for rows that are not 16-byte aligned: one warp per
+// (job, segment), plain loads.
+template <typename Tin>
+__global__ void __launch_bounds__(256)
+    k_rate_sum_plain(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int n_jobs, int V,
+                     int n_seg, ExpParams ep, const ResampleDesc* __restrict__ jobs,
+                     ff* __restrict__ sums) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const long long n_items = static_cast<long long>(n_jobs) * n_seg;
+  const long long GW = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long it = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       it < n_items; it += GW) {
+    const int j = static_cast<int>(it / n_seg), sg = static_cast<int>(it - (it / n_seg) * n_seg);
+    const ResampleDesc d = jobs[j];
+    if (d.mode != kModeMin) continue;
+    float hi, lo;
+    segment_sum<Tin, false>(tl + d.t_row * static_cast<long long>(V),
+                            dl + d.d_row * static_cast<long long>(V), sg * kSeg,
+                            min(V, (sg + 1) * kSeg), weight_params(d), ep, lane, hi, lo);
+    if (lane == 0) sums[it] = ff_norm(hi, lo);
+  }
+}
+
+// k_rate_finish: one thread per position adds its segment sums in order and
+// divides by S_t; -1 where there is no job.
+__global__ void __launch_bounds__(256)
+    k_rate_finish(int n_jobs, int n_seg, const ResampleDesc* __restrict__ jobs,
+                  const ff* __restrict__ sums, float* __restrict__ rates) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= n_jobs) return;
+  const ResampleDesc d = jobs[j];
+  if (d.mode != kModeMin) {
+    rates[j] = -1.f;
+    return;
+  }
+  ff t{0.f, 0.f};
+  for (int sg = 0; sg < n_seg; ++sg) t = ff_add(t, sums[static_cast<long long>(j) * n_seg + sg]);
+  const double rate = (static_cast<double>(t.hi) + t.lo) / (static_cast<double>(d.S_hi) + d.S_lo);
+  rates[j] = static_cast<float>(rate);
 }
 
 // ---------------------------------------------------------------------------
@@ -1218,8 +1346,8 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
     const long long want = (items + kResidWarps - 1) / kResidWarps;
     const int grid = static_cast<int>(want < sms ? want : sms);
     if (launch_pdl(k_resid<Tin, kResidWarps, kResidStages, kResidPart>, grid, kResidWarps * 32,
-                   resid_smem_bytes(), stream, tl, dl, B, gamma, V, n_seg, ep, ws, emitted,
-                   tie_ctr, status) != cudaSuccess)
+                   resid_smem_bytes(), stream, tl, dl, B, V, n_seg, ep,
+                   static_cast<const ResampleDesc*>(ws.desc), ws.seg_sum, status) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     if (launch_pdl(k_pick<Tin>, B, kDecideWarps * 32, 0, stream, tl, dl, gamma, V, n_seg, ep, ws,
                    emitted, tie_ctr, status) != cudaSuccess)
@@ -1366,4 +1494,102 @@ extern "C" int dspark_verify_static(const void* target_logits, const void* draft
                        temperature, dtype, B, gamma, V, target_row_off, draft_row_off,
                        accepted_len, emitted_tokens, probs_out, near_tie_count, device_status,
                        ws, DSPARK_STATIC_WS_BYTES, stream);
+}
+
+// ---------------------------------------------------------------------------
+// dspark_acceptance (equation 8 per position; section 3.2.1's label)
+// ---------------------------------------------------------------------------
+namespace dspark {
+
+template <typename Tin>
+int launch_acceptance(const Tin* tl, const Tin* dl, const int32_t* vlen, float temperature,
+                      int B, int gamma, int V, const int64_t* toff, const int64_t* doff,
+                      float* rates, int32_t* status, void* workspace, cudaStream_t stream) {
+  int sms = 0, decide_per_sm = 1;
+  if (int rc = device_setup(sms, decide_per_sm)) return rc;
+  VerifyWs ws = carve_verify_ws(workspace, B, gamma, V);
+  char* p = static_cast<char*>(workspace) + DSPARK_VERIFY_WS_BYTES(B, gamma, V);
+  ResampleDesc* jobs = reinterpret_cast<ResampleDesc*>(p);
+  p += DSPARK_ALIGN256(static_cast<size_t>(B) * gamma * 64);
+  ff* sums = reinterpret_cast<ff*>(p);
+  const ExpParams ep = exp_params(temperature);
+  const int unit_elems = kUnitBytes / static_cast<int>(sizeof(Tin));
+  const int n_units = (V + unit_elems - 1) / unit_elems;
+  const int n_seg = (V + kSeg - 1) / kSeg;
+  const int n_jobs = B * gamma;
+  if (launch_pdl(k_plan, 1, 1024, 0, stream, vlen, toff, doff, B, gamma, ws,
+                 &ws.hdr->ties_scratch, status) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (B == 0) return DSPARK_OK;
+  const bool aligned = (static_cast<size_t>(V) * sizeof(Tin)) % 16 == 0 &&
+                       reinterpret_cast<uintptr_t>(tl) % 16 == 0 &&
+                       reinterpret_cast<uintptr_t>(dl) % 16 == 0;
+  const long long max_units = static_cast<long long>(DSPARK_MAX_ROWS(B, gamma)) * n_units;
+  cudaError_t e;
+  if (aligned) {
+    const long long want = (max_units + kStreamWarps - 1) / kStreamWarps;
+    e = launch_pdl(k_rowstats_tma<Tin, kStreamWarps, kStages>,
+                   static_cast<int>(want < sms ? want : sms), kStreamWarps * 32, tma_smem_bytes(),
+                   stream, tl, dl, V, n_units, ws, ep, status);
+  } else {
+    const long long want = (max_units + 7) / 8;
+    e = launch_pdl(k_rowstats_plain<Tin>, static_cast<int>(want < 4LL * sms ? want : 4LL * sms),
+                   256, 0, stream, tl, dl, V, n_units, ws, ep, status);
+  }
+  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (launch_pdl(k_rate_desc, B, kDecideWarps * 32, 0, stream, gamma, n_units, ws, jobs,
+                 status) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  const long long items = static_cast<long long>(n_jobs) * n_seg;
+  if (aligned) {
+    const long long want = (items + kResidWarps - 1) / kResidWarps;
+    e = launch_pdl(k_resid<Tin, kResidWarps, kResidStages, kResidPart>,
+                   static_cast<int>(want < sms ? want : sms), kResidWarps * 32, resid_smem_bytes(),
+                   stream, tl, dl, n_jobs, V, n_seg, ep, static_cast<const ResampleDesc*>(jobs),
+                   sums, status);
+  } else {
+    const long long want = (items + 7) / 8;
+    e = launch_pdl(k_rate_sum_plain<Tin>, static_cast<int>(want < 4LL * sms ? want : 4LL * sms),
+                   256, 0, stream, tl, dl, n_jobs, V, n_seg, ep,
+                   static_cast<const ResampleDesc*>(jobs), sums);
+  }
+  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (launch_pdl(k_rate_finish, (n_jobs + 255) / 256, 256, 0, stream, n_jobs, n_seg,
+                 static_cast<const ResampleDesc*>(jobs), static_cast<const ff*>(sums),
+                 rates) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+}  // namespace dspark
+
+extern "C" int dspark_acceptance(const void* target_logits, const void* draft_logits,
+                                 const int32_t* verify_len, float temperature, int32_t dtype,
+                                 int32_t B, int32_t gamma, int32_t V,
+                                 const int64_t* target_row_off, const int64_t* draft_row_off,
+                                 float* rates, int32_t* device_status, void* workspace,
+                                 size_t workspace_bytes, struct CUstream_st* stream) {
+  using namespace dspark;
+  if (B < 0 || B > 65535 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || V < 1 || V > (1 << 30))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return DSPARK_ERR_INVALID_ARG;
+  if (dtype != DSPARK_F32 && dtype != DSPARK_BF16) return DSPARK_ERR_INVALID_ARG;
+  if (!device_status) return DSPARK_ERR_INVALID_ARG;
+  if ((target_row_off == nullptr) != (draft_row_off == nullptr)) return DSPARK_ERR_INVALID_ARG;
+  if (B > 0 && (!target_logits || !draft_logits || !verify_len || !rates))
+    return DSPARK_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < DSPARK_ACCEPTANCE_WS_BYTES(B, gamma, V) ||
+      reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return DSPARK_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == DSPARK_BF16)
+    return launch_acceptance<uint16_t>(static_cast<const uint16_t*>(target_logits),
+                                       static_cast<const uint16_t*>(draft_logits), verify_len,
+                                       temperature, B, gamma, V, target_row_off, draft_row_off,
+                                       rates, device_status, workspace, s);
+  return launch_acceptance<float>(static_cast<const float*>(target_logits),
+                                  static_cast<const float*>(draft_logits), verify_len,
+                                  temperature, B, gamma, V, target_row_off, draft_row_off, rates,
+                                  device_status, workspace, s);
 }

@@ -21,22 +21,7 @@ struct TileStat {  // statistics of one (row, unit): sum_v 2^(z_v*c - K) = s_hi 
 };
 static_assert(sizeof(TileStat) == 16, "TileStat layout");
 
-struct __align__(16) ResampleDesc {
-  int64_t t_row;  // global row of the target distribution sampled from
-  int64_t d_row;  // global draft row (residual mode)
-  int32_t K_t;    // exponent reference of the target row
-  float D_hi;     // residual: log2(p_t/p_d)(v) = (z_t - z_d)*c - D, D = D_hi + D_lo
-  float D_lo;
-  float u;        // resample uniform
-  int32_t mode;   // 0 nothing to do, 1 residual, 2 target distribution
-  int32_t m;      // accepted count: position of the sampled token
-  float E_hi;     // residual: D - K_t = E_hi + E_lo, so that p_d/p_t = 2^(z_d*c + E) / e_t
-  float E_lo;
-  int32_t pad[4];
-};
-static_assert(sizeof(ResampleDesc) == 64, "ResampleDesc layout");
-
-enum { kModeNone = 0, kModeResidual = 1, kModeTarget = 2 };
+struct ResampleDesc;  // the draw after a block (dspark_verify.cu)
 
 struct WsHeader {
   int32_t total_rows;

@@ -45,8 +45,9 @@ def test_header_compiles_as_c_and_macros_match_binding(tmp_path):
               (7, 32, 1001), (0, 3, 5)]
     src = ['#include <stdio.h>', '#include "dspark.h"', "int main(void) {"]
     for B, g, V in shapes:
-        src.append(f'  printf("%zu %zu\\n", DSPARK_VERIFY_WS_BYTES({B}, {g}, {V}), '
-                   f'DSPARK_SCHEDULE_WS_BYTES({max(B, 1)}, {g}));')
+        src.append(f'  printf("%zu %zu %zu\\n", DSPARK_VERIFY_WS_BYTES({B}, {g}, {V}), '
+                   f'DSPARK_SCHEDULE_WS_BYTES({max(B, 1)}, {g}), '
+                   f'DSPARK_ACCEPTANCE_WS_BYTES({B}, {g}, {V}));')
     src.append("  return 0; }")
     c = tmp_path / "probe.c"
     c.write_text("\n".join(src))
@@ -55,9 +56,10 @@ def test_header_compiles_as_c_and_macros_match_binding(tmp_path):
                     "-o", str(exe)], check=True)
     lines = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
     for (B, g, V), line in zip(shapes, lines):
-        v, s = map(int, line.split())
+        v, s, a = map(int, line.split())
         assert v == binding.verify_workspace_bytes(B, g, V)
         assert s == binding.schedule_workspace_bytes(max(B, 1), g)
+        assert a == binding.acceptance_workspace_bytes(B, g, V)
 
 
 def _verify_call(lib, **kw):
@@ -138,3 +140,22 @@ def test_threshold_baseline_rejects_bad_arguments_on_host(lib):
     assert call(g=33) == 1
     assert call(conf=None) == 1
     assert call(st=None) == 1
+
+
+def test_acceptance_rejects_bad_arguments_on_host(lib):
+    p = ctypes.c_void_p
+    def call(**kw):
+        a = dict(tl=1, dl=1, vlen=1, T=1.0, dtype=1, B=4, g=4, V=32, toff=None, doff=None,
+                 rates=1, st=1, ws=256, wsb=1 << 30)
+        a.update(kw)
+        q = lambda x: None if x is None else p(x)
+        return lib.dspark_acceptance(q(a["tl"]), q(a["dl"]), q(a["vlen"]), a["T"], a["dtype"],
+                                     a["B"], a["g"], a["V"], q(a["toff"]), q(a["doff"]),
+                                     q(a["rates"]), q(a["st"]), q(a["ws"]), a["wsb"], None)
+    assert call(T=0.0) == 1
+    assert call(g=33) == 1
+    assert call(rates=None) == 1
+    assert call(st=None) == 1
+    assert call(toff=64) == 1
+    assert call(ws=None) == 3
+    assert call(wsb=100) == 3
