@@ -78,6 +78,14 @@ def _setup(lib):
     lib.oracle_schedule_threshold.restype = ctypes.c_int
     lib.oracle_schedule_threshold.argtypes = [
         ctypes.POINTER(ctypes.c_float), ctypes.c_int32, ctypes.c_int32, ctypes.c_float, c_i32p]
+    c_u16p = ctypes.POINTER(ctypes.c_uint16)
+    lib.oracle_bf16_round.restype = ctypes.c_int
+    lib.oracle_bf16_round.argtypes = [c_f64p, ctypes.c_int64, c_u16p]
+    lib.oracle_markov_draft.restype = ctypes.c_int
+    lib.oracle_markov_draft.argtypes = [
+        c_u16p, c_u16p, c_u16p, c_i32p, ctypes.POINTER(ctypes.c_float), ctypes.c_double,
+        ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, c_i32p, ctypes.c_int32,
+        c_i32p, c_f64p, c_i32p, c_u16p, ctypes.c_int32]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     return lib
@@ -242,6 +250,58 @@ def schedule_threshold(confidences, threshold: float, lib=None):
     if rc != 0:
         raise OracleError(f"oracle_schedule_threshold returned {rc}")
     return ell
+
+
+def bf16_round(x, lib=None):
+    """Nearest bfloat16 (ties to even) of each float64 value, as uint16 bits."""
+    lib = lib or load()
+    a = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.zeros(a.shape, np.uint16)
+    rc = lib.oracle_bf16_round(_ptr(a, ctypes.c_double), a.size, _ptr(out, ctypes.c_uint16))
+    if rc != 0:
+        raise OracleError(f"oracle_bf16_round returned {rc}")
+    return out
+
+
+def markov_draft(base_logits, w1, w2t, anchors, uniforms, temperature, requests=None,
+                 want_logits=False, nthreads=1, lib=None):
+    """Sequential stage with the Markov head (section 3.1, equations 4 and 5).
+
+    base_logits [B, gamma, V] bf16 bits (uint16); w1, w2t [V, r] bf16 bits
+    (w2t row v = column v of W2); anchors [B]; uniforms [B, gamma] float32.
+    requests: indices of the requests to draft (None: all). Returns a dict:
+    tokens [n, gamma], probs [n, gamma] (p_k of the drawn token), flags
+    [n, gamma] (FLAG_* bits of each draw), logits [n, gamma, V] bf16 bits if
+    want_logits."""
+    lib = lib or load()
+    U = np.ascontiguousarray(base_logits, dtype=np.uint16)
+    B, gamma, V = U.shape
+    W1 = np.ascontiguousarray(w1, dtype=np.uint16)
+    W2t = np.ascontiguousarray(w2t, dtype=np.uint16)
+    if W1.shape[0] != V or W2t.shape != W1.shape:
+        raise ValueError("w1 and w2t must both be [V, r]")
+    r = W1.shape[1]
+    x0 = np.ascontiguousarray(anchors, dtype=np.int32).reshape(B)
+    u = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(B, gamma)
+    req = None if requests is None else np.ascontiguousarray(requests, dtype=np.int32).reshape(-1)
+    n = B if req is None else req.shape[0]
+    tokens = np.zeros((n, gamma), np.int32)
+    probs = np.zeros((n, gamma), np.float64)
+    flags = np.zeros((n, gamma), np.int32)
+    logits = np.zeros((n, gamma, V), np.uint16) if want_logits else None
+    u16 = ctypes.c_uint16
+    rc = lib.oracle_markov_draft(
+        _ptr(U, u16), _ptr(W1, u16), _ptr(W2t, u16), _ptr(x0, ctypes.c_int32),
+        _ptr(u, ctypes.c_float), float(temperature), B, gamma, V, r,
+        None if req is None else _ptr(req, ctypes.c_int32), n, _ptr(tokens, ctypes.c_int32),
+        _ptr(probs, ctypes.c_double), _ptr(flags, ctypes.c_int32),
+        None if logits is None else _ptr(logits, u16), int(nthreads or 1))
+    if rc != 0:
+        raise OracleError(f"oracle_markov_draft returned {rc}")
+    out = {"tokens": tokens, "probs": probs, "flags": flags}
+    if want_logits:
+        out["logits"] = logits
+    return out
 
 
 def max_threads(lib=None) -> int:

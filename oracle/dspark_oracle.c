@@ -26,6 +26,10 @@
  *            scheduler): the loop, its initial state and its break condition.
  *   [P-5.2]  English paper, section 5.2: the production scheduler removes the
  *            early-stopping break (unconstrained global search).
+ *   [P-3.1]  English paper, section 3.1, "Sequential stage": equation 4 (the
+ *            block factorises left to right, p_k(v) = softmax(U_k + B_k)(v))
+ *            and equation 5 (Markov head: B(x_{k-1}, .) = W1[x_{k-1}] W2, W1 of
+ *            V x r, W2 of r x V); x_0 is the anchor token.
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - The residual distribution on rejection, norm(max(0, p_t - p_d)), is not
@@ -37,6 +41,14 @@
  *   - SPS(B) = 1 / T(B), where T(B) is the tabulated step time at B tokens.
  *   - p_d(x_k) == 0 in floating point gives ratio +inf (accept) and a flag; a
  *     zero residual mass falls back to sampling p_t and is flagged.
+ *
+ *   - Markov drafter: the drafter emits its rows in bfloat16. The bias is
+ *     summed exactly, its sum with U_k(v) is rounded to binary32, and the
+ *     emitted logit is that value rounded to bfloat16 (both ties to even).
+ *     Position k's token is drawn from the temperature-scaled softmax of the
+ *     emitted row, by the same inverse CDF, so that the verifier sees exactly
+ *     the distribution the token came from. W2 is stored transposed (row v
+ *     holds column v of W2).
  *
  * Near-tie flags (a decision whose uniform lies within 1e-6 of its threshold,
  * or a scheduler comparison within 1e-9 relative) are reported so that a
@@ -527,6 +539,154 @@ int oracle_schedule_threshold(const float* confidences, int32_t R, int32_t gamma
     verify_len[r] = ell;
   }
   return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Sequential stage with the Markov head [P-3.1, equations 4 and 5]        */
+/* ---------------------------------------------------------------------- */
+
+/* A bfloat16 bit pattern widened exactly to double. */
+static double bf16_to_double(uint16_t h) {
+  uint32_t bits = ((uint32_t)h) << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/*
+ * x rounded to the nearest bfloat16 value, ties to the even significand: a
+ * bfloat16 number has 8 significant bits and the exponent range of binary32,
+ * so the spacing at |x| in [2^E, 2^(E+1)) is 2^(E-7) (E >= -126; below that the
+ * subnormal spacing 2^-133). Returns the bit pattern.
+ */
+static uint16_t bf16_round(double x) {
+  if (isnan(x)) return (uint16_t)0x7FC0u;
+  const uint16_t sign = signbit(x) ? (uint16_t)0x8000u : (uint16_t)0;
+  double a = fabs(x);
+  if (isinf(a)) return (uint16_t)(sign | 0x7F80u);
+  if (a == 0.0) return sign;
+  int e;
+  (void)frexp(a, &e);            /* a = f * 2^e, f in [0.5, 1): E = e - 1 */
+  int E = e - 1;
+  if (E < -126) E = -126;
+  const double n = ldexp(a, 7 - E); /* a in units of the spacing: exact */
+  const double q = rint(n);         /* to nearest, ties to even (default mode) */
+  const double y = ldexp(q, E - 7);
+  if (y >= ldexp(1.0, 128)) return (uint16_t)(sign | 0x7F80u); /* overflow */
+  const float fy = (float)y;        /* exact: y is a bfloat16 value */
+  uint32_t bits;
+  memcpy(&bits, &fy, sizeof bits);
+  return (uint16_t)(sign | (uint16_t)((bits >> 16) & 0x7FFFu));
+}
+
+int oracle_bf16_round(const double* x, int64_t n, uint16_t* out) {
+  if ((!x || !out) && n > 0) return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < n; ++i) out[i] = bf16_round(x[i]);
+  return ORACLE_OK;
+}
+
+/*
+ * One request's draft block [P-3.1]. For k = 1..gamma, with x_0 = the anchor:
+ *   bias(v)  = sum_j W1[x_{k-1}][j] * W2[j][v]        (equation 5, exact sum)
+ *   L_k(v)   = bf16(fl32(U_k(v) + bias(v)))            (the emitted draft row)
+ *   p_k(v)   = exp(L_k(v)/T - M) / sum_w exp(L_k(w)/T - M)  (equation 4 at T)
+ *   x_k      = inverse CDF of p_k at u_k (ascending token order)
+ * Outputs per position: tokens[k-1], probs[k-1] = p_k(x_k), flags[k-1]
+ * (ORACLE_FLAG_* bits of the draw), and, if logits != NULL, the emitted row
+ * L_k at logits[(k-1)*V ...].
+ */
+static int draft_request(const uint16_t* U, const uint16_t* W1, const uint16_t* W2t,
+                         int32_t x0, const float* u, double T, int32_t gamma, int64_t V,
+                         int32_t r, double* a, double* L, double* w, int32_t* tokens,
+                         double* probs, int32_t* flags, uint16_t* logits) {
+  if (x0 < 0 || (int64_t)x0 >= V) return ORACLE_ERR_DATA;
+  int32_t prev = x0;
+  for (int32_t k = 0; k < gamma; ++k) {
+    const double uk = (double)u[k];
+    if (!(uk >= 0.0 && uk < 1.0)) return ORACLE_ERR_DATA;
+    for (int32_t j = 0; j < r; ++j) a[j] = bf16_to_double(W1[(int64_t)prev * r + j]);
+    const uint16_t* Uk = U + (int64_t)k * V;
+    double M = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+      const uint16_t* col = W2t + v * r;
+      double bias = 0.0;
+      for (int32_t j = 0; j < r; ++j) bias += a[j] * bf16_to_double(col[j]);
+      const float s = (float)(bf16_to_double(Uk[v]) + bias);
+      const uint16_t h = bf16_round((double)s);
+      if (logits) logits[(int64_t)k * V + v] = h;
+      L[v] = bf16_to_double(h);
+      if (isnan(L[v]) || L[v] == INFINITY) return ORACLE_ERR_DATA;
+      if (L[v] / T > M) M = L[v] / T;
+    }
+    if (!isfinite(M)) return ORACLE_ERR_DATA; /* every logit -inf */
+    double Z = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+      w[v] = exp(L[v] / T - M);
+      Z += w[v];
+    }
+    int32_t f = 0;
+    const int32_t y = inverse_cdf(w, V, Z, uk, &f);
+    tokens[k] = y;
+    probs[k] = w[y] / Z;
+    flags[k] = f;
+    prev = y;
+  }
+  return ORACLE_OK;
+}
+
+/*
+ * The sequential stage of a batch of draft blocks [P-3.1]. Layouts: U and the
+ * emitted logits [B][gamma][V] bfloat16 bits (request b's position k at row
+ * b*gamma + k-1); W1 and W2t [V][r] bfloat16 bits; anchors [B]; uniforms
+ * [B][gamma] binary32 in [0, 1). `requests` lists the nreq requests to draft
+ * (NULL: all B in order); outputs are indexed by the list position: tokens,
+ * probs, flags [nreq][gamma]; logits [nreq][gamma][V] or NULL.
+ */
+int oracle_markov_draft(const uint16_t* U, const uint16_t* W1, const uint16_t* W2t,
+                        const int32_t* anchors, const float* uniforms, double temperature,
+                        int32_t B, int32_t gamma, int64_t V, int32_t r, const int32_t* requests,
+                        int32_t nreq, int32_t* tokens, double* probs, int32_t* flags,
+                        uint16_t* logits, int32_t nthreads) {
+  if (!U || !W1 || !W2t || !anchors || !uniforms || !tokens || !probs || !flags)
+    return ORACLE_ERR_ARG;
+  if (B < 0 || gamma < 1 || V < 1 || r < 1 || !(temperature > 0.0) || !isfinite(temperature))
+    return ORACLE_ERR_ARG;
+  if (!requests) nreq = B;
+  if (nreq < 0) return ORACLE_ERR_ARG;
+  for (int32_t i = 0; i < nreq; ++i) {
+    const int32_t b = requests ? requests[i] : i;
+    if (b < 0 || b >= B) return ORACLE_ERR_ARG;
+  }
+  int status = ORACLE_OK;
+  if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+  {
+    double* a = (double*)malloc(sizeof(double) * (size_t)r);
+    double* L = (double*)malloc(sizeof(double) * (size_t)V);
+    double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!a || !L || !w) {
+#pragma omp critical
+      status = ORACLE_ERR_NOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int32_t i = 0; i < nreq; ++i) {
+        const int32_t b = requests ? requests[i] : i;
+        const int64_t o = (int64_t)i * gamma;
+        int rc = draft_request(U + (int64_t)b * gamma * V, W1, W2t, anchors[b],
+                               uniforms + (int64_t)b * gamma, temperature, gamma, V, r, a, L,
+                               w, tokens + o, probs + o, flags + o,
+                               logits ? logits + o * V : NULL);
+        if (rc) {
+#pragma omp critical
+          if (status == ORACLE_OK) status = rc;
+        }
+      }
+    }
+    free(a);
+    free(L);
+    free(w);
+  }
+  return status;
 }
 
 /* Number of OpenMP threads the oracle can use (1 without OpenMP). */

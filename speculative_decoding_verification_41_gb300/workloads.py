@@ -13,7 +13,8 @@ key = (seed, 0), counter = (index, purpose, 0, 0); a uniform is
 (word >> 8) * 2^-24, a value on the 2^-24 grid that float32 holds exactly.
 
 Purposes: 0 logit normals (tiny case only), 1 draft-token sampling,
-2 verification uniforms, 3 per-request rho / verify-length draws.
+2 verification uniforms, 3 per-request rho / verify-length draws, 4 anchor
+tokens of the sequential drafter.
 
 The workload shapes stand in for the DSpark paper's evaluation (section 4.1:
 Qwen3-class vocabularies of 151,936 tokens, temperature 1.0; section 5.1:
@@ -43,6 +44,7 @@ PURPOSE_NORMALS = 0
 PURPOSE_DRAFT_SAMPLING = 1
 PURPOSE_VERIFY_UNIFORMS = 2
 PURPOSE_REQUEST_PARAMS = 3
+PURPOSE_ANCHORS = 4
 
 
 def philox4x32_10(counters: np.ndarray, key) -> np.ndarray:
@@ -324,6 +326,82 @@ def make_schedule(R: int = 512, gamma: int = 16, seed: int = 7, device="cuda",
     return ScheduleInputs(torch.from_numpy(make_confidences(R, gamma, seed)).to(dev),
                           torch.from_numpy(prof).to(dev),
                           name=f"sched_r{R}_g{gamma}" + ("_flat" if flat_profile else ""))
+
+
+@dataclass
+class MarkovDraftInputs:
+    """Inputs of the sequential stage with the Markov head (DSpark paper,
+    section 3.1): base logits U [B, gamma, V] bf16 from the parallel stage, the
+    head's factors W1 [V, r] and W2 stored transposed as w2t [V, r] (row v =
+    column v of W2), both bf16, anchor tokens [B] int32 and one uniform per
+    position [B, gamma] float32."""
+    base_logits: torch.Tensor
+    w1: torch.Tensor
+    w2t: torch.Tensor
+    anchors: torch.Tensor
+    uniforms: torch.Tensor
+    temperature: float
+    name: str = ""
+
+    @property
+    def B(self) -> int:
+        return int(self.base_logits.shape[0])
+
+    @property
+    def gamma(self) -> int:
+        return int(self.base_logits.shape[1])
+
+    @property
+    def V(self) -> int:
+        return int(self.base_logits.shape[2])
+
+    @property
+    def r(self) -> int:
+        return int(self.w1.shape[1])
+
+    def to(self, device) -> "MarkovDraftInputs":
+        return MarkovDraftInputs(self.base_logits.to(device), self.w1.to(device),
+                                 self.w2t.to(device), self.anchors.to(device),
+                                 self.uniforms.to(device), self.temperature, self.name)
+
+
+def make_markov_draft(B: int, gamma: int, V: int, r: int = 256, temperature: float = 0.7,
+                      seed: int = 7, device="cuda", weights: str = "grid",
+                      name: str = "") -> MarkovDraftInputs:
+    """Synthetic drafter inputs (random weights: the pages publish no trained head).
+
+    Base logits: 3*N(0,1) - 1.1*ln(v+1), rounded to bf16, like the verifier's
+    target rows. weights="grid": W1 and W2 entries k/256 with k uniform on
+    {-127..127} (an int8-like grid; the bias B(a, v) then has a standard
+    deviation of about 1.3 and every partial sum of W1[a] . W2[:, v] is exact in
+    binary32). weights="gauss": N(0, 0.29^2) entries rounded to bf16.
+    Anchors: Philox words (purpose 4) mod V; uniforms: Philox (purpose 1)."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed * 7919 + 101)
+    if weights == "grid":
+        w1 = (torch.randint(-127, 128, (V, r), generator=gen, device=dev).float() / 256.0)
+        w2t = (torch.randint(-127, 128, (V, r), generator=gen, device=dev).float() / 256.0)
+    elif weights == "gauss":
+        w1 = 0.29 * torch.randn(V, r, generator=gen, device=dev)
+        w2t = 0.29 * torch.randn(V, r, generator=gen, device=dev)
+    else:
+        raise ValueError(weights)
+    bias = torch.from_numpy(zipf_bias(V)).to(dev, torch.float32)
+    U = torch.empty(B, gamma, V, dtype=torch.bfloat16, device=dev)
+    for b in range(B):
+        U[b] = (3.0 * torch.randn(gamma, V, generator=gen, device=dev) + bias).to(torch.bfloat16)
+    anchors = (philox_words(seed, PURPOSE_ANCHORS, B).astype(np.int64) % V).astype(np.int32)
+    uni = philox_uniforms(seed, PURPOSE_DRAFT_SAMPLING, B * gamma).reshape(B, gamma)
+    return MarkovDraftInputs(U, w1.to(torch.bfloat16), w2t.to(torch.bfloat16),
+                             torch.from_numpy(anchors).to(dev), torch.from_numpy(uni).to(dev),
+                             float(temperature),
+                             name or f"draft_b{B}_g{gamma}_v{V}_r{r}_{weights}")
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """bfloat16 tensor -> numpy uint16 bit patterns (host copy)."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
 # The five named workloads (names state the sizes).

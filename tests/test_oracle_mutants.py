@@ -37,6 +37,19 @@ MUTANTS = {
                                 "prod = (double)confidences[(int64_t)r * gamma + j];"),
     "batch_not_counted": ("    Bsz += 1;\n", "\n"),
     "anchor_token_dropped": ("double tau = (double)R;", "double tau = 0.0;"),
+    "draft_embedding_from_w2": ("a[j] = bf16_to_double(W1[(int64_t)prev * r + j]);",
+                                "a[j] = bf16_to_double(W2t[(int64_t)prev * r + j]);"),
+    "draft_projection_from_w1": ("const uint16_t* col = W2t + v * r;",
+                                 "const uint16_t* col = W1 + v * r;"),
+    "draft_prev_stays_anchor": ("    prev = y;\n", "    prev = x0;\n"),
+    "draft_base_row_off_by_one": ("const uint16_t* Uk = U + (int64_t)k * V;",
+                                  "const uint16_t* Uk = U + (int64_t)(k ? k - 1 : 0) * V;"),
+    "draft_no_binary32_step": ("const float s = (float)(bf16_to_double(Uk[v]) + bias);",
+                               "const double s = bf16_to_double(Uk[v]) + bias;"),
+    "draft_round_half_up": ("const double q = rint(n);", "const double q = floor(n + 0.5);"),
+    "draft_temperature_dropped": ("w[v] = exp(L[v] / T - M);", "w[v] = exp(L[v] - M / T);"),
+    "draft_first_uniform_reused": ("const double uk = (double)u[k];",
+                                   "const double uk = (double)u[0];"),
 }
 
 
@@ -88,9 +101,65 @@ def check_schedule(lib):
         assert abs(s["theta_best"] - best) <= 1e-12 * best
 
 
+def _bits(vals):
+    return (np.asarray(vals, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def check_draft(lib):
+    """Compact forms of the drafter pins (tests/test_oracle_markov_draft.py)."""
+    V, r = 16, 64
+    # successor chain: each token forces succ(a) = (5a + 3) mod 16
+    succ = [(5 * a + 3) % V for a in range(V)]
+    W1 = np.zeros((V, r), np.uint16)
+    W2t = np.zeros((V, r), np.uint16)
+    for a in range(V):
+        W1[a, 4 * a:4 * a + 4] = _bits([0.5] * 4)
+        W2t[succ[a], 4 * a:4 * a + 4] = _bits([0.5] * 4)
+    g = 6
+    U = np.zeros((2, g, V), np.uint16)
+    u = np.full((2, g), 0.5, np.float32)
+    out = oracle.markov_draft(U, W1, W2t, np.array([3, 11], np.int32), u, 0.05, lib=lib)
+    for b, x in enumerate((3, 11)):
+        for k in range(g):
+            x = succ[x]
+            assert out["tokens"][b, k] == x
+    # rounding: ties to even, binary32 first
+    for terms, want in [([(0.5, 2.0 ** -7)], 1.0), ([(0.5, 2.0 ** -7), (2.0 ** -15, 2.0 ** -15)], 1.0),
+                        ([(0.5, 2.0 ** -7), (2.0 ** -10, 2.0 ** -10)], 1.0078125)]:
+        W1 = np.zeros((8, r), np.uint16)
+        W2t = np.zeros((8, r), np.uint16)
+        for j, (a, b) in enumerate(terms):
+            W1[0, j], W2t[1, j] = _bits([a])[0], _bits([b])[0]
+        L = oracle.markov_draft(np.tile(_bits([1.0] * 8), (1, 1, 1)), W1, W2t,
+                                np.array([0], np.int32), np.array([[0.5]], np.float32), 1.0,
+                                want_logits=True, lib=lib)["logits"][0, 0]
+        got = (L.astype(np.uint32) << 16).view(np.float32)
+        assert got[1] == want and got[0] == 1.0
+    # two tokens: p(0) = 1 / (1 + exp((L1 - L0) / T)) at T = 0.5
+    W1 = np.zeros((2, r), np.uint16)
+    W2t = np.zeros((2, r), np.uint16)
+    W1[0, 0], W2t[0, 0], W2t[1, 0] = _bits([0.5, 0.25, -0.5])
+    out = oracle.markov_draft(np.zeros((1, 1, 2), np.uint16), W1, W2t, np.array([0], np.int32),
+                              np.array([[0.1]], np.float32), 0.5, lib=lib)
+    assert abs(out["probs"][0, 0] - 1.0 / (1.0 + np.exp(-0.375 / 0.5))) < 1e-15
+    # zero head: the block samples softmax(U_k / T) by the inverse CDF, row k at step k
+    rng = np.random.default_rng(2)
+    V, g, T = 40, 4, 0.8
+    Uf = (3 * rng.standard_normal((1, g, V))).astype(np.float32)
+    U = _bits((Uf.view(np.uint32) & 0xFFFF0000).view(np.float32))
+    u = rng.uniform(0, 1, (1, g)).astype(np.float32)
+    out = oracle.markov_draft(U, np.zeros((V, r), np.uint16), np.zeros((V, r), np.uint16),
+                              np.array([0], np.int32), u, T, want_logits=True, lib=lib)
+    assert np.array_equal(out["logits"], U)
+    for k in range(g):
+        z = (U[0, k].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        y = int(np.searchsorted(np.cumsum(scipy.special.softmax(z / T)), u[0, k], side="right"))
+        assert out["flags"][0, k] or out["tokens"][0, k] == y
+
+
 def _all_checks(lib):
     failures = []
-    for chk in (check_softmax, check_verify, check_schedule):
+    for chk in (check_softmax, check_verify, check_schedule, check_draft):
         try:
             chk(lib)
         except (AssertionError, oracle.OracleError) as e:
