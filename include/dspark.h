@@ -99,6 +99,16 @@ typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
    DSPARK_ALIGN256((size_t)(B) * (size_t)(gamma) * 64u) +                     \
    DSPARK_ALIGN256((size_t)(B) * (size_t)(gamma) * DSPARK_SEGS_PER_ROW(V) * 8u))
 
+/* Vocabulary entries per tensor-core tile and per softmax statistic of the
+   drafter, and the largest Markov-head rank it takes. */
+#define DSPARK_DRAFT_TILE 128
+#define DSPARK_DRAFT_MAX_RANK 256
+/* Workspace of dspark_draft_markov, in bytes: the gathered embedding rows
+   W1[x_{k-1}] of the batch, then one statistic per (request, tile). */
+#define DSPARK_DRAFT_WS_BYTES(B, r, V)                                        \
+  (DSPARK_ALIGN256((size_t)(B) * (size_t)(r) * 2u) +                          \
+   DSPARK_ALIGN256((size_t)(B) * DSPARK_CEILDIV((V), DSPARK_DRAFT_TILE) * 8u))
+
 /* Workspace of dspark_schedule, in bytes: two (key, index) buffers for the
    sort, per-request lengths and a header. */
 #define DSPARK_SCHEDULE_WS_BYTES(R, gamma)                                    \
@@ -355,6 +365,71 @@ int dspark_verify_timed(const void* target_logits, const void* draft_logits,
                         int32_t* device_status, void* workspace,
                         size_t workspace_bytes, struct CUstream_st* stream,
                         struct CUevent_st** events);
+
+/*
+ * dspark_draft_markov -- the sequential stage of the DSpark drafter with the
+ * Markov head (DSpark paper, section 3.1 "Sequential stage", equations 4 and
+ * 5): gamma draft tokens per request, drawn left to right.
+ *
+ * For request b and k = 1..gamma, with x_0 = anchors[b]:
+ *   bias(v) = sum_j W1[x_{k-1}][j] * W2[j][v]          (equation 5)
+ *   L_k(v)  = bf16(fl32(U_k(v) + bias(v)))              (the emitted draft row)
+ *   x_k     = smallest v whose running sum of exp(L_k/T - M) exceeds
+ *             uniforms[b][k-1] * Z                     (equation 4 at T)
+ * The bias is accumulated in binary32 on the tensor cores (exact whenever every
+ * partial sum is, e.g. weights on a 2^-8 grid), added to U_k, rounded to
+ * binary32, then to bf16 (ties to even). The tokens are drawn from the emitted
+ * rows themselves, so a verifier reading draft_logits sees exactly the draft
+ * distribution p_d^k the tokens came from.
+ *
+ * Arguments
+ *   base_logits   [B][gamma][V] bf16: U_k of the parallel stage, request b's
+ *                 position k at row b*gamma + k-1 (the dense draft-row layout
+ *                 of dspark_verify).
+ *   w1            [V][r] bf16: the embedding table W1.
+ *   w2t           [V][r] bf16: W2 transposed (row v holds W2[0..r-1][v]).
+ *   anchors       [B] int32: x_0, the last token of the previous cycle.
+ *   uniforms      [B][gamma] float32 in [0, 1): one per position.
+ *   temperature   T > 0 and finite.
+ *   B >= 0 (B = 0 does nothing), 1 <= gamma <= DSPARK_MAX_GAMMA,
+ *   V >= 8 a multiple of 8, r in {64, 128, 192, 256}.
+ * Outputs
+ *   draft_logits  [B][gamma][V] bf16: L_k. May be the same buffer as
+ *                 base_logits (overwritten in place); otherwise disjoint.
+ *   draft_tokens  [B][gamma] int32: x_1..x_gamma.
+ *   device_status DSPARK_ERR_BAD_DATA for an anchor outside [0, V), a uniform
+ *                 outside [0, 1), a NaN or +inf logit, or a row whose logits
+ *                 are all -inf (that request's token is then 0).
+ *   workspace     at least DSPARK_DRAFT_WS_BYTES(B, r, V) bytes, 256-byte
+ *                 aligned; no state is kept in it between calls.
+ * base_logits, w1, w2t and draft_logits must be 16-byte aligned (the tensor
+ * memory access unit copies 16-byte aligned boxes); otherwise, and for
+ * arguments outside the ranges above, DSPARK_ERR_INVALID_ARG.
+ */
+int dspark_draft_markov(const void* base_logits, const void* w1, const void* w2t,
+                        const int32_t* anchors, const float* uniforms,
+                        float temperature, int32_t B, int32_t gamma, int64_t V,
+                        int32_t r, void* draft_logits, int32_t* draft_tokens,
+                        int32_t* device_status, void* workspace,
+                        size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * dspark_draft_markov_timed -- dspark_draft_markov with timing events (a
+ * measurement aid; no counterpart in the paper). Records events[0] before the
+ * first gather, events[1] after it, and for k = 0..gamma-1 events[2+2k] after
+ * position k's tensor-core kernel (k_draft_step) and events[3+2k] after its
+ * draw (k_draft_pick): 2*gamma + 2 events created by the caller with timing
+ * enabled. The recordings keep consecutive kernels from overlapping, so the
+ * intervals add up to a little more than an untimed call. A NULL events
+ * pointer or event is DSPARK_ERR_INVALID_ARG.
+ */
+int dspark_draft_markov_timed(const void* base_logits, const void* w1, const void* w2t,
+                              const int32_t* anchors, const float* uniforms,
+                              float temperature, int32_t B, int32_t gamma, int64_t V,
+                              int32_t r, void* draft_logits, int32_t* draft_tokens,
+                              int32_t* device_status, void* workspace,
+                              size_t workspace_bytes, struct CUstream_st* stream,
+                              struct CUevent_st** events);
 
 #ifdef __cplusplus
 }

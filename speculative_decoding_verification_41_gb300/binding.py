@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_CUDA
 DSPARK_F32, DSPARK_BF16 = 0, 1
 EXPORTED = ("dspark_verify", "dspark_acceptance", "dspark_schedule", "dspark_schedule_capacity",
             "dspark_schedule_topk", "dspark_schedule_threshold", "dspark_verify_static",
-            "dspark_verify_timed")
+            "dspark_verify_timed", "dspark_draft_markov", "dspark_draft_markov_timed")
 
 
 class DsparkError(RuntimeError):
@@ -39,7 +39,8 @@ class DsparkError(RuntimeError):
 def _header_consts() -> dict:
     txt = open(HEADER).read()
     out = {}
-    for name in ("DSPARK_TILE_BYTES", "DSPARK_RESAMPLE_SEG", "DSPARK_MAX_GAMMA"):
+    for name in ("DSPARK_TILE_BYTES", "DSPARK_RESAMPLE_SEG", "DSPARK_MAX_GAMMA",
+                 "DSPARK_DRAFT_TILE", "DSPARK_DRAFT_MAX_RANK"):
         out[name] = int(re.search(rf"#define {name} (\d+)", txt).group(1))
     return out
 
@@ -69,6 +70,11 @@ def acceptance_workspace_bytes(B: int, gamma: int, V: int) -> int:
     """Python statement of DSPARK_ACCEPTANCE_WS_BYTES (include/dspark.h)."""
     segs = _cdiv(V, _CONSTS["DSPARK_RESAMPLE_SEG"])
     return verify_workspace_bytes(B, gamma, V) + _a256(B * gamma * 64) + _a256(B * gamma * segs * 8)
+
+
+def draft_workspace_bytes(B: int, r: int, V: int) -> int:
+    """Python statement of DSPARK_DRAFT_WS_BYTES (include/dspark.h)."""
+    return _a256(B * r * 2) + _a256(B * _cdiv(V, _CONSTS["DSPARK_DRAFT_TILE"]) * 8)
 
 
 def schedule_workspace_bytes(R: int, gamma: int) -> int:
@@ -115,6 +121,12 @@ def load(path: Optional[str] = None):
         lib.dspark_schedule_topk.argtypes = [vp, vp, i32, i32, vp, vp, vp, sz, vp]
         lib.dspark_schedule_threshold.restype = ctypes.c_int
         lib.dspark_schedule_threshold.argtypes = [vp, f32, i32, i32, vp, vp, vp]
+        lib.dspark_draft_markov.restype = ctypes.c_int
+        lib.dspark_draft_markov.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i64, i32, vp, vp,
+                                            vp, vp, sz, vp]
+        lib.dspark_draft_markov_timed.restype = ctypes.c_int
+        lib.dspark_draft_markov_timed.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i64, i32, vp,
+                                                  vp, vp, vp, sz, vp, vp]
         if path is None:
             _lib = lib
         return lib
@@ -388,3 +400,68 @@ def dspark_schedule_threshold(confidences: torch.Tensor, threshold: float, *,
         if int(st.item()) != 0:
             raise DsparkError("dspark_schedule_threshold (device)", int(st.item()))
     return {"verify_len": ell, "device_status": st}
+
+
+def dspark_draft_markov(base_logits: torch.Tensor, w1: torch.Tensor, w2t: torch.Tensor,
+                        anchors: torch.Tensor, uniforms: torch.Tensor, temperature: float, *,
+                        draft_logits: Optional[torch.Tensor] = None,
+                        draft_tokens: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, stream=None,
+                        check: bool = False, events=None) -> dict:
+    """Sequential stage of the drafter with the Markov head (section 3.1,
+    equations 4 and 5) through libdspark.
+
+    base_logits [B, gamma, V] bf16, w1 and w2t [V, r] bf16 (w2t row v = column v
+    of W2), anchors [B] int32, uniforms [B, gamma] float32. draft_logits may be
+    base_logits itself (in place). Returns device tensors: draft_logits [B,
+    gamma, V] bf16, draft_tokens [B, gamma] int32, device_status [1]. With
+    events (2*gamma + 2 torch.cuda.Event made with enable_timing=True) the call
+    goes through dspark_draft_markov_timed."""
+    dev = base_logits.device
+    _require_cuda("base_logits", base_logits, torch.bfloat16)
+    _require_cuda("w1", w1, torch.bfloat16, dev)
+    _require_cuda("w2t", w2t, torch.bfloat16, dev)
+    _require_cuda("anchors", anchors, torch.int32, dev)
+    _require_cuda("uniforms", uniforms, torch.float32, dev)
+    if base_logits.dim() != 3:
+        raise ValueError("base_logits must be [B, gamma, V]")
+    B, gamma, V = base_logits.shape
+    if w1.dim() != 2 or w1.shape[0] != V or w2t.shape != w1.shape:
+        raise ValueError("w1 and w2t must both be [V, r]")
+    r = w1.shape[1]
+    if anchors.shape != (B,) or uniforms.shape != (B, gamma):
+        raise ValueError("anchors must be [B] and uniforms [B, gamma]")
+    out = draft_logits if draft_logits is not None else torch.empty_like(base_logits)
+    _require_cuda("draft_logits", out, torch.bfloat16, dev)
+    if out.shape != base_logits.shape:
+        raise ValueError("draft_logits must be [B, gamma, V]")
+    tok = draft_tokens if draft_tokens is not None else torch.empty(B, gamma, dtype=torch.int32,
+                                                                     device=dev)
+    ws = workspace if workspace is not None else torch.empty(
+        max(draft_workspace_bytes(B, r, V), 256), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    lib = load()
+    args = (_ptr(base_logits), _ptr(w1), _ptr(w2t), _ptr(anchors), _ptr(uniforms),
+            float(temperature), B, gamma, V, r, _ptr(out), _ptr(tok), _ptr(status), _ptr(ws),
+            ws.numel())
+    with torch.cuda.device(dev):
+        s = _stream_handle(stream)
+        if events is None:
+            rc = lib.dspark_draft_markov(*args, s)
+        else:
+            if len(events) != 2 * gamma + 2:
+                raise ValueError("events must hold 2*gamma + 2 torch.cuda.Event")
+            st = stream if stream is not None else torch.cuda.current_stream(dev)
+            for e in events:
+                e.record(st)
+            handles = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event)
+                                                        for e in events])
+            rc = lib.dspark_draft_markov_timed(*args, s, handles)
+    if rc != 0:
+        raise DsparkError("dspark_draft_markov", rc)
+    if check:
+        torch.cuda.synchronize(dev)
+        st = int(status.item())
+        if st != 0:
+            raise DsparkError("dspark_draft_markov (device)", st)
+    return {"draft_logits": out, "draft_tokens": tok, "device_status": status}

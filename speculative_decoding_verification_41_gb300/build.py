@@ -10,8 +10,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libdspark.so")
-SOURCES = ["dspark_verify.cu", "dspark_schedule.cu"]
-HEADERS = ["dspark_common.cuh"]
+SOURCES = ["dspark_verify.cu", "dspark_schedule.cu", "dspark_draft.cu"]
+HEADERS = sorted(f for f in os.listdir(CSRC) if f.endswith(".cuh"))
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", f"-I{os.path.join(ROOT, 'include')}"]

@@ -1,0 +1,723 @@
+// dspark_draft.cu -- the sequential stage of the DSpark drafter with the
+// Markov head, on one GB300 (sm_103a).
+//
+// DSpark paper, section 3.1 ("Sequential stage"): the block is drawn left to
+// right from p_k(v) = softmax(U_k + B_k)(v) (equation 4), with the Markov head's
+// transition bias B(x_{k-1}, .) = W1[x_{k-1}] W2 (equation 5, W1 of V x r, W2 of
+// r x V, r = 256 by default). Every position is one pass of two kernels:
+//
+//   k_draft_step  (tensor cores) D = G W2 for the batch, G[b] = W1[x_{k-1}(b)]:
+//                 an M = requests x N = vocabulary x K = r product by
+//                 tcgen05.mma (bf16 in, f32 accumulators in tensor memory),
+//                 operands brought in by tiled TMA in the 128-byte swizzled
+//                 layout. The epilogue adds U_k, rounds to bf16 (the emitted
+//                 draft row that the verifier reads), stores it by TMA and
+//                 writes one softmax statistic per (request, 128-token tile).
+//   k_draft_pick  (one CTA per request) merges the tile statistics, finds the
+//                 tile where the running sum crosses u*Z, re-reads that tile's
+//                 128 emitted logits and returns the token: an inverse-CDF
+//                 draw of softmax(L_k / T) in ascending token order. It then
+//                 copies W1[x_k] into G for the next position.
+//
+// W2 is stored transposed, w2t[v][j] = W2[j][v], so both operands are K-major.
+// Kernels are chained with programmatic dependent launch: each k_draft_step
+// streams its first W2 and U tiles (which do not depend on the previous token)
+// while the previous k_draft_pick is still running.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "dspark_tc.cuh"
+#include "dspark_verify_types.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kDM = 128;                             // requests per tile (MMA M)
+constexpr int kDN = DSPARK_DRAFT_TILE;               // vocabulary per tile (MMA N)
+constexpr int kDK = 64;                              // K per chunk: one 128-byte row of bf16
+constexpr int kDMaxKC = DSPARK_DRAFT_MAX_RANK / kDK;  // chunks of the largest rank
+constexpr int kDStages = 4;                          // W2 ring (one 128 x 64 chunk each)
+constexpr int kDSlots = 3;                           // U / L tile slots
+constexpr int kDEpiWarps = 8;                        // two groups of four
+constexpr int kDThreads = 64 + kDEpiWarps * 32;      // producer, MMA, epilogue
+constexpr uint32_t kBox = 128u * 128u;               // 128 rows x 128 bytes
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffW = kOffA + kDMaxKC * kBox;
+constexpr uint32_t kOffU = kOffW + kDStages * kBox;
+constexpr uint32_t kOffBar = kOffU + kDSlots * 2 * kBox;
+constexpr uint32_t kDraftSmem = kOffBar + 256 + 1024;  // barriers, 1024-byte alignment slack
+constexpr uint32_t kTmemCols = 2 * kDN;              // two accumulators
+constexpr uint32_t kIdesc = idesc_bf16_f32(kDM, kDN);
+static_assert(kDN == 128, "epilogue and statistics assume 128-token tiles");
+static_assert(kDraftSmem <= 232448, "shared memory of k_draft_step");
+
+struct DraftStat {  // one (request, tile): sum over the tile of 2^(L_v * c - R)
+  float s;
+  int32_t R;  // INT_MIN when every logit of the tile is -inf
+};
+
+struct DraftBars {
+  uint64_t a_full;
+  uint64_t w_full[kDStages], w_empty[kDStages];
+  uint64_t u_full[kDSlots], u_empty[kDSlots];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t st_ready[2];  // a group's rows are in shared memory, ready to store
+  uint64_t mma_done;
+  uint32_t tmem_base;
+};
+static_assert(sizeof(DraftBars) <= 256, "barrier block");
+
+struct DraftStepArgs {
+  int32_t B, V, r, gamma, k;
+  int32_t n_tiles;  // vocabulary tiles
+  int32_t n_m;      // request tiles
+  int32_t per_m;    // CTAs per request tile
+  ExpParams ep;
+  DraftStat* stats;  // [B][n_tiles]
+  int32_t* status;
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+// two floats -> packed bf16x2 (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Wait with a bound; on timeout record DSPARK_ERR_TIMEOUT and report failure.
+__device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, int32_t* status) {
+  if (mbar_wait(bar, parity)) return true;
+  set_status(status, DSPARK_ERR_TIMEOUT);
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// k_draft_step: bias GEMM + U + bf16 rounding + tile statistics, one position
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kDThreads, 1)
+    k_draft_step(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ CUtensorMap mapW,
+                 const __grid_constant__ CUtensorMap mapU, const __grid_constant__ CUtensorMap mapL,
+                 const DraftStepArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  DraftBars* bars = reinterpret_cast<DraftBars*>(smem + kOffBar);
+  const uint32_t sbase = smem_addr(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tile = blockIdx.x % a.n_m;
+  const int p = blockIdx.x / a.n_m;
+  const int n_local = p < a.n_tiles ? (a.n_tiles - p + a.per_m - 1) / a.per_m : 0;
+  const int KC = a.r / kDK;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->a_full, 1);
+    for (int s = 0; s < kDStages; ++s) {
+      mbar_init(&bars->w_full[s], 1);
+      mbar_init(&bars->w_empty[s], 1);
+    }
+    for (int s = 0; s < kDSlots; ++s) {
+      mbar_init(&bars->u_full[s], 1);
+      mbar_init(&bars->u_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->acc_full[i], 1);
+      mbar_init(&bars->acc_empty[i], 4);
+      mbar_init(&bars->st_ready[i], 4);
+    }
+    mbar_init(&bars->mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ---------------- producer: one thread issues every TMA load ----------------
+    if (lane == 0) {
+      tma_prefetch_map(&mapW);
+      tma_prefetch_map(&mapU);
+      tma_prefetch_map(&mapG);
+      const uint64_t pol_keep = policy_evict_last();    // W2 (other request tiles, steps)
+      const uint64_t pol_stream = policy_evict_first();  // U (read once)
+      const int total = n_local * KC;
+      auto issue_w = [&](int q) {
+        const int t = q / KC, c = q % KC, s = q % kDStages;
+        mbar_arrive_expect_tx(&bars->w_full[s], kBox);
+        tma_load_2d(smem + kOffW + s * kBox, &mapW, c * kDK, (p + t * a.per_m) * kDN,
+                    &bars->w_full[s], pol_keep);
+      };
+      auto issue_u = [&](int t) {
+        const int slot = t % kDSlots;
+        const int v0 = (p + t * a.per_m) * kDN;
+        uint8_t* dst = smem + kOffU + slot * 2 * kBox;
+        mbar_arrive_expect_tx(&bars->u_full[slot], 2 * kBox);
+        tma_load_3d(dst, &mapU, v0, a.k, m_tile * kDM, &bars->u_full[slot], pol_stream);
+        tma_load_3d(dst + kBox, &mapU, v0 + kDK, a.k, m_tile * kDM, &bars->u_full[slot],
+                    pol_stream);
+      };
+      // before the dependency wait: W2 and U do not depend on the previous kernels
+      const int q0 = total < kDStages ? total : kDStages;
+      const int u0 = n_local < kDSlots ? n_local : kDSlots;
+      for (int q = 0; q < q0; ++q) issue_w(q);
+      for (int t = 0; t < u0; ++t) issue_u(t);
+      pdl_wait();
+      pdl_trigger();
+      if (n_local > 0) {
+        mbar_arrive_expect_tx(&bars->a_full, KC * kBox);
+        for (int c = 0; c < KC; ++c)
+          tma_load_2d(smem + kOffA + c * kBox, &mapG, c * kDK, m_tile * kDM, &bars->a_full,
+                      pol_keep);
+      }
+      bool ok = true;
+      int nq = q0, nu = u0;  // copies issued so far
+      for (int t = 0; t < n_local && ok; ++t) {
+        if (t >= kDSlots) {
+          const int slot = t % kDSlots;
+          ok = wait_or_flag(&bars->u_empty[slot], ((t / kDSlots) - 1) & 1, a.status);
+          if (!ok) break;
+          issue_u(t);
+          nu = t + 1;
+        }
+        for (int c = 0; c < KC; ++c) {
+          const int q = t * KC + c;
+          if (q < q0) continue;
+          ok = wait_or_flag(&bars->w_empty[q % kDStages], ((q / kDStages) - 1) & 1, a.status);
+          if (!ok) break;
+          issue_w(q);
+          nq = q + 1;
+        }
+      }
+      if (!ok) {
+        // give each copy still in flight a bounded chance to land before exit:
+        // the last phase issued on each stage and slot
+        for (int q = nq - kDStages > 0 ? nq - kDStages : 0; q < nq; ++q)
+          mbar_wait(&bars->w_full[q % kDStages], (q / kDStages) & 1);
+        for (int t = nu - kDSlots > 0 ? nu - kDSlots : 0; t < nu; ++t)
+          mbar_wait(&bars->u_full[t % kDSlots], (t / kDSlots) & 1);
+        if (n_local > 0) mbar_wait(&bars->a_full, 0);
+      }
+    } else {
+      pdl_wait();
+      pdl_trigger();
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: one thread ----------------
+    pdl_wait();
+    pdl_trigger();
+    if (lane == 0) {
+      bool ok = n_local == 0 || wait_or_flag(&bars->a_full, 0, a.status);
+      tc_fence_after();
+      for (int t = 0; t < n_local && ok; ++t) {
+        const int acc = t & 1;
+        if (t >= 2) {
+          ok = wait_or_flag(&bars->acc_empty[acc], ((t >> 1) - 1) & 1, a.status);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const uint32_t d = tmem + acc * kDN;
+        for (int c = 0; c < KC && ok; ++c) {
+          const int q = t * KC + c, s = q % kDStages;
+          ok = wait_or_flag(&bars->w_full[s], (q / kDStages) & 1, a.status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a_base = sbase + kOffA + c * kBox;
+          const uint32_t w_base = sbase + kOffW + s * kBox;
+#pragma unroll
+          for (int j = 0; j < kDK / 16; ++j)
+            tc_mma(d, sdesc_sw128(a_base + 32 * j), sdesc_sw128(w_base + 32 * j), kIdesc,
+                   (c | j) != 0);
+          tc_commit(&bars->w_empty[s]);
+        }
+        if (ok) tc_commit(&bars->acc_full[acc]);
+      }
+      // every MMA issued has completed before tensor memory is released
+      tc_commit(&bars->mma_done);
+      wait_or_flag(&bars->mma_done, 0, a.status);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: two groups of four warps, alternate tiles ----------------
+    pdl_wait();
+    pdl_trigger();
+    const int grp = (warp - 2) >> 2;
+    const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
+    const int m = quarter * 32 + lane;
+    const int b = m_tile * kDM + m;
+    const bool row_ok = b < a.B;
+    const bool leader = (warp == 2 + 4 * grp) && lane == 0;
+    const uint64_t pol_out = policy_evict_first();
+    const float c_hi = a.ep.c_hi;
+    for (int t = grp; t < n_local; t += 2) {
+      const int n = p + t * a.per_m;
+      const int v0 = n * kDN;
+      const int slot = t % kDSlots;
+      const uint32_t ubase = sbase + kOffU + slot * 2 * kBox;
+      // every lane waits (and so acquires); the warp then decides as one, so
+      // that the aligned tensor-memory loads below run converged
+      bool ok = wait_or_flag(&bars->acc_full[grp], (t >> 1) & 1, a.status);
+      ok = ok && wait_or_flag(&bars->u_full[slot], (t / kDSlots) & 1, a.status);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      // pass 1: L = bf16(acc + U) written over U in shared memory; tile maximum
+      float mx = -INFINITY;
+      bool bad = false;
+#pragma unroll 1
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float acc[32];
+        __syncwarp();
+        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * kDN + c4 * 32, acc);
+        const uint32_t row = ubase + (c4 >> 1) * kBox + m * 128;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int chunk = (c4 & 1) * 4 + jj;
+          const uint32_t addr = row + ((chunk ^ (m & 7)) << 4);
+          const uint4 u = lds128(addr);
+          const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+          uint32_t ow[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float s0 = acc[8 * jj + 2 * e] + bf16_lo(uw[e]);
+            const float s1 = acc[8 * jj + 2 * e + 1] + bf16_hi(uw[e]);
+            ow[e] = pack_bf16x2(s0, s1);
+            const int v = v0 + c4 * 32 + 8 * jj + 2 * e;
+            const float z0 = bf16_lo(ow[e]), z1 = bf16_hi(ow[e]);
+            if (v < a.V) {
+              mx = fmaxf(mx, z0);
+              bad |= (z0 != z0) || z0 == INFINITY;
+            }
+            if (v + 1 < a.V) {
+              mx = fmaxf(mx, z1);
+              bad |= (z1 != z1) || z1 == INFINITY;
+            }
+          }
+          sts128(addr, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+        }
+      }
+      // accumulator read out: release it to the MMA warp
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->acc_empty[grp]);
+      // pass 2: sum of 2^(L*c - R) over the tile, pairwise, one reference R
+      int32_t R = INT_MIN;
+      float total = 0.f;
+      if (mx > -INFINITY && !bad) {
+        R = static_cast<int32_t>(ceilf(mx * c_hi));
+        const float nK = -static_cast<float>(R);
+        float part[4];
+#pragma unroll 1
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const uint32_t row = ubase + (c4 >> 1) * kBox + m * 128;
+          float e[32];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int chunk = (c4 & 1) * 4 + jj;
+            const uint4 w = lds128(row + ((chunk ^ (m & 7)) << 4));
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int v = v0 + c4 * 32 + 8 * jj + 2 * q;
+              e[8 * jj + 2 * q] = v < a.V ? exp_term(bf16_lo(ww[q]), nK, a.ep) : 0.f;
+              e[8 * jj + 2 * q + 1] = v + 1 < a.V ? exp_term(bf16_hi(ww[q]), nK, a.ep) : 0.f;
+            }
+          }
+#pragma unroll
+          for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) e[i] += e[i + w];
+          part[c4] = e[0];
+        }
+        total = (part[0] + part[1]) + (part[2] + part[3]);
+      }
+      if (bad && row_ok) set_status(a.status, DSPARK_ERR_BAD_DATA);
+      if (row_ok) a.stats[static_cast<size_t>(b) * a.n_tiles + n] = DraftStat{total, R};
+      // the emitted rows go out by TMA once the group's writes are visible to
+      // the asynchronous proxy (each writer fences, then arrives)
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->st_ready[grp]);
+      if (leader && wait_or_flag(&bars->st_ready[grp], (t >> 1) & 1, a.status)) {
+        tma_store_3d(&mapL, smem + kOffU + slot * 2 * kBox, v0, a.k, m_tile * kDM, pol_out);
+        if (v0 + kDK < a.V)
+          tma_store_3d(&mapL, smem + kOffU + slot * 2 * kBox + kBox, v0 + kDK, a.k,
+                       m_tile * kDM, pol_out);
+        bulk_commit();
+        bulk_wait_read<0>();
+        mbar_arrive(&bars->u_empty[slot]);
+      }
+      __syncwarp();
+    }
+    if (leader) bulk_wait<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// k_draft_gather: G[b] = W1[x_0(b)] before the first position
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void copy_row(const uint16_t* __restrict__ W1, uint16_t* __restrict__ G,
+                                         int x, int b, int r, int lane) {
+  const uint4* src = reinterpret_cast<const uint4*>(W1 + static_cast<size_t>(x) * r);
+  uint4* dst = reinterpret_cast<uint4*>(G + static_cast<size_t>(b) * r);
+  for (int i = lane; i < r / 8; i += 32) dst[i] = src[i];
+}
+
+__global__ void __launch_bounds__(32) k_draft_gather(const int32_t* __restrict__ anchors,
+                                                     const uint16_t* __restrict__ W1,
+                                                     uint16_t* __restrict__ G, int B, int V, int r,
+                                                     int32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x;
+  if (b >= B) return;
+  int x = anchors[b];
+  if (x < 0 || x >= V) {
+    if (threadIdx.x == 0) set_status(status, DSPARK_ERR_BAD_DATA);
+    x = 0;
+  }
+  copy_row(W1, G, x, b, r, threadIdx.x);
+}
+
+// ---------------------------------------------------------------------------
+// k_draft_pick: inverse-CDF draw of position k for one request
+// ---------------------------------------------------------------------------
+struct DraftPickArgs {
+  int32_t B, V, r, gamma, k, n_tiles;
+  ExpParams ep;
+  const DraftStat* stats;    // [B][n_tiles]
+  const uint16_t* L;         // emitted rows [B][gamma][V]
+  const float* uniforms;     // [B][gamma]
+  const uint16_t* W1;        // [V][r]
+  uint16_t* G;               // [B][r]
+  int32_t* tokens;           // [B][gamma]
+  int32_t* status;
+};
+
+constexpr int kPickThreads = 128;
+
+__global__ void __launch_bounds__(kPickThreads) k_draft_pick(const DraftPickArgs a) {
+  __shared__ int32_t s_red[kPickThreads / 32];
+  __shared__ double s_tot[kPickThreads / 32];
+  __shared__ int32_t s_tile;
+  __shared__ double s_before;
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const DraftStat* st = a.stats + static_cast<size_t>(b) * a.n_tiles;
+  const int per = (a.n_tiles + kPickThreads - 1) / kPickThreads;
+  const int g0 = t * per;
+  const int g1 = g0 + per < a.n_tiles ? g0 + per : a.n_tiles;
+
+  // common exponent reference: the largest tile reference
+  int32_t Rm = INT_MIN;
+  for (int g = g0; g < g1; ++g) {
+    const DraftStat d = st[g];
+    if (d.s > 0.f && d.R > Rm) Rm = d.R;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Rm = max(Rm, __shfl_xor_sync(0xFFFFFFFFu, Rm, o));
+  if (lane == 0) s_red[warp] = Rm;
+  if (t == 0) s_tile = -1;
+  __syncthreads();
+  int32_t Rmax = s_red[0];
+  for (int w = 1; w < kPickThreads / 32; ++w) Rmax = max(Rmax, s_red[w]);
+
+  const float u = a.uniforms[static_cast<size_t>(b) * a.gamma + a.k];
+  const bool u_ok = u >= 0.f && u < 1.f;
+  int y = 0;
+  if (Rmax == INT_MIN || !u_ok) {
+    if (t == 0) set_status(a.status, DSPARK_ERR_BAD_DATA);
+  } else {
+    // this thread's tile mass, then an inclusive scan over threads in
+    // ascending tile order; the next thread's exclusive prefix is bitwise this
+    // thread's inclusive one, so the threads partition [0, Z)
+    double S = 0.0;
+    for (int g = g0; g < g1; ++g) {
+      const DraftStat d = st[g];
+      if (d.s > 0.f) S += ldexp(static_cast<double>(d.s), d.R - Rmax);
+    }
+    double inc = S;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    if (lane == 31) s_tot[warp] = inc;
+    __syncthreads();
+    double off = 0.0, Z = 0.0;
+    for (int w = 0; w < kPickThreads / 32; ++w) {
+      if (w < warp) off += s_tot[w];
+      Z += s_tot[w];
+    }
+    // exclusive prefix = the previous lane's inclusive one (same expression)
+    const double prev = __shfl_up_sync(0xFFFFFFFFu, inc, 1);
+    const double excl = off + (lane > 0 ? prev : 0.0);
+    const double incl = off + inc;
+    const double target = static_cast<double>(u) * Z;
+    if (S > 0.0 && excl <= target && target < incl) {
+      double C = excl;
+      int gs = -1, glast = -1;
+      double Clast = excl;
+      for (int g = g0; g < g1; ++g) {
+        const DraftStat d = st[g];
+        if (!(d.s > 0.f)) continue;
+        const double w = ldexp(static_cast<double>(d.s), d.R - Rmax);
+        if (C + w > target) {
+          gs = g;
+          break;
+        }
+        glast = g;
+        Clast = C;
+        C += w;
+      }
+      if (gs < 0) {  // rounding left the target past the last tile: take it
+        gs = glast;
+        C = Clast;
+      }
+      s_tile = gs;
+      s_before = C;
+    }
+    __syncthreads();
+    const int g = s_tile;
+    if (warp == 0 && g >= 0) {
+      // the crossing tile: recompute its 128 terms exactly as the step kernel did
+      const DraftStat d = st[g];
+      const float nK = -static_cast<float>(d.R);
+      const double scale = ldexp(1.0, d.R - Rmax);
+      const int v = g * kDN + 4 * lane;
+      double w[4] = {0.0, 0.0, 0.0, 0.0};
+      if (v < a.V) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(
+            a.L + (static_cast<size_t>(b) * a.gamma + a.k) * a.V + v);
+        w[0] = exp_term(bf16_lo(raw.x), nK, a.ep) * scale;
+        w[1] = exp_term(bf16_hi(raw.x), nK, a.ep) * scale;
+        w[2] = exp_term(bf16_lo(raw.y), nK, a.ep) * scale;
+        w[3] = exp_term(bf16_hi(raw.y), nK, a.ep) * scale;
+      }
+      double inc_l = ((w[0] + w[1]) + w[2]) + w[3];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double vv = __shfl_up_sync(0xFFFFFFFFu, inc_l, o);
+        if (lane >= o) inc_l += vv;
+      }
+      const double pre = __shfl_up_sync(0xFFFFFFFFu, inc_l, 1);
+      const double base = s_before + (lane > 0 ? pre : 0.0);
+      const uint32_t cross = __ballot_sync(0xFFFFFFFFu, s_before + inc_l > target);
+      int pick = -1;
+      if (cross) {
+        const int L0 = __ffs(cross) - 1;
+        if (lane == L0) {
+          double c = base;
+          int last = -1;
+          for (int e = 0; e < 4; ++e) {
+            if (w[e] > 0.0) last = e;
+            if (c + w[e] > target) {
+              pick = v + e;
+              break;
+            }
+            c += w[e];
+          }
+          if (pick < 0) pick = v + (last >= 0 ? last : 0);
+        }
+        pick = __shfl_sync(0xFFFFFFFFu, pick, L0);
+      } else {  // rounding: the last token of the tile with positive weight
+        const int lpos = (w[3] > 0.0) ? 3 : (w[2] > 0.0) ? 2 : (w[1] > 0.0) ? 1 : (w[0] > 0.0) ? 0 : -1;
+        const uint32_t any = __ballot_sync(0xFFFFFFFFu, lpos >= 0);
+        const int Lh = any ? 31 - __clz(any) : 0;
+        const int e = __shfl_sync(0xFFFFFFFFu, lpos, Lh);
+        pick = g * kDN + 4 * Lh + (e >= 0 ? e : 0);
+      }
+      y = pick;
+    }
+  }
+  if (warp == 0) {
+    if (lane == 0) a.tokens[static_cast<size_t>(b) * a.gamma + a.k] = y;
+    if (a.k + 1 < a.gamma) copy_row(a.W1, a.G, y, b, a.r, lane);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+struct DraftDevice {
+  bool ready = false;
+  int sms = 0;
+};
+std::mutex g_draft_mutex;
+DraftDevice g_draft_dev[128];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int draft_setup(int& sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return DSPARK_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_draft_mutex);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return DSPARK_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  DraftDevice& d = g_draft_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    if (cudaFuncSetAttribute(k_draft_step, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kDraftSmem)) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    d.ready = true;
+  }
+  sms = d.sms;
+  return DSPARK_OK;
+}
+
+// A bf16 tensor map in the 128-byte swizzled layout: dims[0] innermost.
+bool encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims,
+                const cuuint64_t* strides_bytes, const cuuint32_t* box) {
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                  const_cast<void*>(base), dims, strides_bytes, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ExpParams draft_exp_params(float temperature) {
+  ExpParams ep;
+  ep.c_d = 1.4426950408889634 / static_cast<double>(temperature);  // log2(e) / T
+  float hi = static_cast<float>(ep.c_d);
+  if (static_cast<double>(hi) > ep.c_d) hi = std::nextafter(hi, 0.0f);
+  ep.c_hi = hi;
+  ep.c_lo = static_cast<float>(ep.c_d - static_cast<double>(hi));
+  if (!(ep.c_lo > 0.0f)) ep.c_lo = 1e-30f;  // keeps c_lo * (-inf) = -inf
+  return ep;
+}
+
+int draft_entry(const void* base_logits, const void* w1, const void* w2t, const int32_t* anchors,
+                const float* uniforms, float temperature, int32_t B, int32_t gamma, int64_t V,
+                int32_t r, void* draft_logits, int32_t* draft_tokens, int32_t* device_status,
+                void* workspace, size_t workspace_bytes, cudaStream_t stream, cudaEvent_t* ev) {
+  if (B < 0 || gamma < 1 || gamma > DSPARK_MAX_GAMMA || V < 8 || V % 8 != 0 ||
+      V > (int64_t)INT32_MAX - kDN || r < kDK || r > DSPARK_DRAFT_MAX_RANK || r % kDK != 0 ||
+      !(temperature > 0.0f) || !std::isfinite(temperature))
+    return DSPARK_ERR_INVALID_ARG;
+  if (B == 0) return DSPARK_OK;
+  if (!base_logits || !w1 || !w2t || !anchors || !uniforms || !draft_logits || !draft_tokens ||
+      !device_status || !workspace)
+    return DSPARK_ERR_INVALID_ARG;
+  if (!aligned16(base_logits) || !aligned16(w1) || !aligned16(w2t) || !aligned16(draft_logits) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return DSPARK_ERR_INVALID_ARG;
+  if (workspace_bytes < DSPARK_DRAFT_WS_BYTES(B, r, V)) return DSPARK_ERR_WORKSPACE;
+  int sms = 0;
+  if (int rc = draft_setup(sms)) return rc;
+
+  const int Vi = static_cast<int>(V);
+  const int n_tiles = (Vi + kDN - 1) / kDN;
+  const int n_m = (B + kDM - 1) / kDM;
+  int per_m = sms / n_m;
+  if (per_m < 1) per_m = 1;
+  if (per_m > n_tiles) per_m = n_tiles;
+  uint16_t* G = static_cast<uint16_t*>(workspace);
+  DraftStat* stats = reinterpret_cast<DraftStat*>(
+      static_cast<char*>(workspace) + DSPARK_ALIGN256(static_cast<size_t>(B) * r * 2));
+
+  CUtensorMap mapG, mapW, mapU, mapL;
+  {
+    const cuuint64_t dg[2] = {static_cast<cuuint64_t>(r), static_cast<cuuint64_t>(B)};
+    const cuuint64_t sg[1] = {static_cast<cuuint64_t>(r) * 2};
+    const cuuint32_t bx[2] = {kDK, kDM};
+    const cuuint64_t dw[2] = {static_cast<cuuint64_t>(r), static_cast<cuuint64_t>(V)};
+    const cuuint64_t du[3] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(gamma),
+                              static_cast<cuuint64_t>(B)};
+    const cuuint64_t su[2] = {static_cast<cuuint64_t>(V) * 2,
+                              static_cast<cuuint64_t>(V) * 2 * static_cast<cuuint64_t>(gamma)};
+    const cuuint32_t bu[3] = {kDK, 1, kDM};
+    if (!encode_map(&mapG, G, 2, dg, sg, bx) || !encode_map(&mapW, w2t, 2, dw, sg, bx) ||
+        !encode_map(&mapU, base_logits, 3, du, su, bu) ||
+        !encode_map(&mapL, draft_logits, 3, du, su, bu))
+      return DSPARK_ERR_CUDA;
+  }
+
+  const ExpParams ep = draft_exp_params(temperature);
+  const uint16_t* W1 = static_cast<const uint16_t*>(w1);
+  if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (launch_pdl(k_draft_gather, B, 32, 0, stream, anchors, W1, G, B, Vi, r, device_status) !=
+      cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  for (int k = 0; k < gamma; ++k) {
+    DraftStepArgs sa{B, Vi, r, gamma, k, n_tiles, n_m, per_m, ep, stats, device_status};
+    if (launch_pdl(k_draft_step, n_m * per_m, kDThreads, kDraftSmem, stream, mapG, mapW, mapU,
+                   mapL, sa) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    if (ev && cudaEventRecord(ev[2 + 2 * k], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+    DraftPickArgs pa{B,     Vi,       r, gamma, k,  n_tiles, ep, stats,
+                     static_cast<const uint16_t*>(draft_logits), uniforms, W1, G, draft_tokens,
+                     device_status};
+    if (launch_pdl(k_draft_pick, B, kPickThreads, 0, stream, pa) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    if (ev && cudaEventRecord(ev[3 + 2 * k], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  }
+  return DSPARK_OK;
+}
+
+}  // namespace
+}  // namespace dspark
+
+extern "C" int dspark_draft_markov(const void* base_logits, const void* w1, const void* w2t,
+                                   const int32_t* anchors, const float* uniforms,
+                                   float temperature, int32_t B, int32_t gamma, int64_t V,
+                                   int32_t r, void* draft_logits, int32_t* draft_tokens,
+                                   int32_t* device_status, void* workspace,
+                                   size_t workspace_bytes, struct CUstream_st* stream) {
+  return dspark::draft_entry(base_logits, w1, w2t, anchors, uniforms, temperature, B, gamma, V, r,
+                             draft_logits, draft_tokens, device_status, workspace,
+                             workspace_bytes, stream, nullptr);
+}
+
+extern "C" int dspark_draft_markov_timed(const void* base_logits, const void* w1, const void* w2t,
+                                         const int32_t* anchors, const float* uniforms,
+                                         float temperature, int32_t B, int32_t gamma, int64_t V,
+                                         int32_t r, void* draft_logits, int32_t* draft_tokens,
+                                         int32_t* device_status, void* workspace,
+                                         size_t workspace_bytes, struct CUstream_st* stream,
+                                         struct CUevent_st** events) {
+  if (!events || gamma < 1 || gamma > DSPARK_MAX_GAMMA) return DSPARK_ERR_INVALID_ARG;
+  for (int i = 0; i < 2 * gamma + 2; ++i)
+    if (!events[i]) return DSPARK_ERR_INVALID_ARG;
+  return dspark::draft_entry(base_logits, w1, w2t, anchors, uniforms, temperature, B, gamma, V, r,
+                             draft_logits, draft_tokens, device_status, workspace,
+                             workspace_bytes, stream, events);
+}

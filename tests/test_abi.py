@@ -48,6 +48,9 @@ def test_header_compiles_as_c_and_macros_match_binding(tmp_path):
         src.append(f'  printf("%zu %zu %zu\\n", DSPARK_VERIFY_WS_BYTES({B}, {g}, {V}), '
                    f'DSPARK_SCHEDULE_WS_BYTES({max(B, 1)}, {g}), '
                    f'DSPARK_ACCEPTANCE_WS_BYTES({B}, {g}, {V}));')
+    draft_shapes = [(1, 64, 8), (5, 128, 1000), (256, 256, 129280), (1000, 192, 151936)]
+    for B, r, V in draft_shapes:
+        src.append(f'  printf("%zu\\n", DSPARK_DRAFT_WS_BYTES({B}, {r}, {V}));')
     src.append("  return 0; }")
     c = tmp_path / "probe.c"
     c.write_text("\n".join(src))
@@ -60,6 +63,8 @@ def test_header_compiles_as_c_and_macros_match_binding(tmp_path):
         assert v == binding.verify_workspace_bytes(B, g, V)
         assert s == binding.schedule_workspace_bytes(max(B, 1), g)
         assert a == binding.acceptance_workspace_bytes(B, g, V)
+    for (B, r, V), line in zip(draft_shapes, lines[len(shapes):]):
+        assert int(line) == binding.draft_workspace_bytes(B, r, V)
 
 
 def _verify_call(lib, **kw):
@@ -159,3 +164,39 @@ def test_acceptance_rejects_bad_arguments_on_host(lib):
     assert call(toff=64) == 1
     assert call(ws=None) == 3
     assert call(wsb=100) == 3
+
+
+def _draft_call(lib, timed=False, events=None, **kw):
+    a = dict(U=256, w1=256, w2t=256, x0=256, uni=256, T=1.0, B=4, g=4, V=1024, r=256, L=256,
+             tok=256, st=256, ws=256, wsb=1 << 30)
+    a.update(kw)
+    q = lambda x: None if x is None else ctypes.c_void_p(x)
+    args = (q(a["U"]), q(a["w1"]), q(a["w2t"]), q(a["x0"]), q(a["uni"]), a["T"], a["B"], a["g"],
+            a["V"], a["r"], q(a["L"]), q(a["tok"]), q(a["st"]), q(a["ws"]), a["wsb"], None)
+    if timed:
+        return lib.dspark_draft_markov_timed(*args, events)
+    return lib.dspark_draft_markov(*args)
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(g=0), 1), (dict(g=33), 1), (dict(V=4), 1), (dict(V=1001), 1), (dict(B=-1), 1),
+    (dict(r=0), 1), (dict(r=100), 1), (dict(r=320), 1), (dict(T=0.0), 1),
+    (dict(T=float("nan")), 1), (dict(T=float("inf")), 1), (dict(U=None), 1), (dict(w2t=None), 1),
+    (dict(L=None), 1), (dict(tok=None), 1), (dict(st=None), 1), (dict(ws=None), 1),
+    (dict(U=264), 1), (dict(w1=8), 1), (dict(L=1032), 1), (dict(ws=128), 1),
+    (dict(wsb=1000), 3),
+])
+def test_draft_rejects_bad_arguments_on_host(lib, bad, code):
+    """Every check runs before the first CUDA call (no device is needed)."""
+    assert _draft_call(lib, **bad) == code
+
+
+def test_draft_with_no_requests_does_nothing(lib):
+    assert _draft_call(lib, B=0, U=None, w1=None, w2t=None, x0=None, uni=None, L=None, tok=None,
+                       st=None, ws=None, wsb=0) == 0
+
+
+def test_timed_draft_rejects_missing_events_on_host(lib):
+    assert _draft_call(lib, timed=True, events=None) == 1
+    ev = (ctypes.c_void_p * 10)(*([ctypes.c_void_p(64)] * 9 + [None]))
+    assert _draft_call(lib, timed=True, events=ev) == 1      # one of 2*4 + 2 is NULL
