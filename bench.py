@@ -47,6 +47,12 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--cpu-sample", type=int, default=256, help="requests in the oracle's sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-drafter", action="store_true",
+                   help="skip the drafter's sequential stage (dspark_draft_markov)")
+    p.add_argument("--drafter-only", action="store_true",
+                   help="measure only the drafter's sequential stage (the ncu capture case)")
+    p.add_argument("--draft-batch", type=int, default=None,
+                   help="requests of the drafter measurement (default 256)")
     p.add_argument("--batch", type=int, default=None,
                    help="requests per step (default: the headline 256); a smaller batch of the "
                         "same recipe serves the ncu capture case")
@@ -233,6 +239,11 @@ def native_arm(args):
         cuda_build.build()
     barrier(dist, dev)
     binding.load()
+    if args.drafter_only:
+        res = drafter_measure(args, dev, torch.cuda.current_stream(dev), rank, ws)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
 
     if args.batch is None and rank == 0:
         vi = workloads.make_config(WORKLOAD, device=dev)
@@ -318,6 +329,8 @@ def native_arm(args):
         if i > 0:
             acc_ms.append(a0.elapsed_time(a1))
     del acc_ws
+
+    drafter = None if args.no_drafter else drafter_measure(args, dev, stream, rank, ws)
 
     # end to end: pinned host buffers -> device, both calls, results back
     e2e = None
@@ -419,8 +432,106 @@ def native_arm(args):
         "clocks": clk,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "drafter": drafter,
     }
+    if drafter is not None and drafter.get("roofline"):
+        drafter["roofline"]["peak"] = peak
+        drafter["roofline"]["frac"] = drafter["roofline"]["achieved"] / peak
+        drafter["roofline"]["peak_source"] = peak_src
     print(json.dumps(line), flush=True)
+
+
+DRAFT_SHAPE = dict(B=256, gamma=16, V=129280, r=256, temperature=0.7)
+
+
+def draft_algorithmic_bytes(B, gamma, V, r) -> int:
+    """Compulsory DRAM bytes of one k_draft_step launch: U_k read and L_k written
+    (bf16), one statistic per (request, 128-token tile) written, the batch's
+    W1 rows read, and W2 once per call spread over its gamma launches."""
+    tiles = -(-V // 128)
+    return 2 * B * V * 2 + B * tiles * 8 + B * r * 2 + V * r * 2 // gamma
+
+
+def drafter_measure(args, dev, stream, rank, ws):
+    """The drafter's sequential stage with the Markov head (dspark_draft_markov)
+    on 256 requests x 16 positions x 129,280 tokens, rank 256: its own median
+    call time (separate from the verification step), per-kernel medians through
+    dspark_draft_markov_timed, and the oracle on a host sample."""
+    from speculative_decoding_verification_41_gb300 import binding, workloads
+    sh = dict(DRAFT_SHAPE, B=args.draft_batch or DRAFT_SHAPE["B"])
+    d = workloads.make_markov_draft(sh["B"], sh["gamma"], sh["V"], sh["r"],
+                                    temperature=sh["temperature"], seed=shard_seed(rank),
+                                    device=dev)
+    out_L = torch.empty_like(d.base_logits)
+    out_x = torch.empty(sh["B"], sh["gamma"], dtype=torch.int32, device=dev)
+    wsp = torch.empty(binding.draft_workspace_bytes(sh["B"], sh["r"], sh["V"]), dtype=torch.uint8,
+                      device=dev)
+
+    def call(events=None):
+        return binding.dspark_draft_markov(d.base_logits, d.w1, d.w2t, d.anchors, d.uniforms,
+                                           d.temperature, draft_logits=out_L, draft_tokens=out_x,
+                                           workspace=wsp, events=events)
+
+    for _ in range(3):
+        o = call()
+    torch.cuda.synchronize(dev)
+    if int(o["device_status"].item()) != 0:
+        raise SystemExit("drafter device status not OK during warm-up")
+    n = max(5, min(args.steps, 20))
+    ms = []
+    for _ in range(n):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        call()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms.append(a0.elapsed_time(a1))
+    g = sh["gamma"]
+    step_ms, pick_ms = [], []
+    for _ in range(3):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * g + 2)]
+        call(events=ev)
+        torch.cuda.synchronize(dev)
+        step_ms += [ev[1 + 2 * k].elapsed_time(ev[2 + 2 * k]) for k in range(g)]
+        pick_ms += [ev[2 + 2 * k].elapsed_time(ev[3 + 2 * k]) for k in range(g)]
+    t_call = statistics.median(ms)
+    t_step = statistics.median(step_ms)
+    positions = sh["B"] * g
+    alg = draft_algorithmic_bytes(sh["B"], g, sh["V"], sh["r"])
+    flops = 2.0 * sh["B"] * sh["V"] * sh["r"]
+    res = {
+        "metric": "draft_positions_per_s", "value": positions * ws / (t_call * 1e-3),
+        "unit": "positions/s", "ms_per_call": t_call,
+        "config": {"workload": f"draft_b{sh['B']}_g{g}_v{sh['V']}_r{sh['r']}_bf16",
+                   "weights": "random on the 2^-8 grid", "temperature": sh["temperature"],
+                   "l2": "base logits (1.06 GB) larger than L2, no flush"},
+        "timing_ms": {"call_median": t_call, "call_p90": float(np.percentile(ms, 90)),
+                      "k_draft_step_median": t_step, "k_draft_pick_median":
+                          statistics.median(pick_ms)},
+        "roofline": {"bound": "hbm", "achieved": alg / (t_step * 1e-3) / 1e9, "unit": "GB/s",
+                     "traffic": None, "algorithmic_bytes_per_launch": alg,
+                     "kernel": "k_draft_step (median CUDA-event interval around each of the 16 "
+                               "launches, dspark_draft_markov_timed)",
+                     "tensor_tflops": flops / (t_step * 1e-3) / 1e12},
+        "gpu_launches_per_call": 1 + 2 * g,
+        "cpu_baseline": None,
+    }
+    del out_L
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        cores = oracle.max_threads()
+        nreq = max(1, min(cores, 16))
+        U = workloads.bf16_bits(d.base_logits[:nreq])
+        W1, W2t = workloads.bf16_bits(d.w1), workloads.bf16_bits(d.w2t)
+        x0, u = d.anchors[:nreq].cpu().numpy(), d.uniforms[:nreq].cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.markov_draft(U, W1, W2t, x0, u, d.temperature, nthreads=cores)
+        t = time.perf_counter() - t0
+        res["cpu_baseline"] = {"value": nreq * g / t, "unit": "positions/s", "cores": cores,
+                               "kind": "oracle",
+                               "sample": f"{nreq} of 256 requests, all 16 positions, "
+                                         f"{t:.2f} s wall, OpenMP over requests"}
+    return res
 
 
 # DRAM traffic of the streaming kernel from one ncu capture (dram__bytes_read.sum +
