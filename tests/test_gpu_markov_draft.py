@@ -62,9 +62,10 @@ def compare_chains(L_gpu, x_gpu, ref, requests):
 
 @pytest.mark.parametrize("B,gamma,V,r,T", [
     (1, 1, 8, 64, 1.0),          # one token tile, mostly out of bounds
-    (5, 4, 1000, 64, 0.7),       # ragged vocabulary tail inside the second half-tile
-    (130, 3, 1064, 128, 1.0),    # two request tiles; the last tile's second half is empty
-    (200, 6, 4096, 256, 0.7),
+    (5, 4, 1000, 64, 0.7),       # ragged vocabulary tail: the last tile holds 40 tokens
+    (130, 3, 1064, 128, 1.0),    # two request tiles; the last tile holds 40 tokens
+    (200, 6, 4096, 256, 0.7),    # whole tiles only
+    (3, 2, 1032, 64, 1.0),       # the last tile holds 8 tokens
     (257, 2, 2048, 192, 2.0),    # three request tiles, rank 192
     (40, 16, 20000, 256, 0.7),   # the full block length
 ])
