@@ -101,7 +101,7 @@ typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
 
 /* Vocabulary entries per tensor-core tile and per softmax statistic of the
    drafter, and the largest Markov-head rank it takes. */
-#define DSPARK_DRAFT_TILE 64
+#define DSPARK_DRAFT_TILE 128
 #define DSPARK_DRAFT_MAX_RANK 256
 /* Workspace of dspark_draft_markov, in bytes: the gathered embedding rows
    W1[x_{k-1}] of the batch, then one statistic per (request, tile). */

@@ -8,22 +8,25 @@
 //
 //   k_draft_step  (tensor cores) D = G W2 for the batch, G[b] = W1[x_{k-1}(b)]:
 //                 an M = requests x N = vocabulary x K = r product by
-//                 tcgen05.mma (bf16 in, f32 accumulators in tensor memory),
-//                 operands brought in by tiled TMA in the 128-byte swizzled
-//                 layout. The epilogue adds U_k, rounds to bf16 (the emitted
+//                 tcgen05.mma (bf16 in, f32 accumulators in tensor memory).
+//                 G stays in tensor memory for the whole launch (the MMA's
+//                 A operand), so shared memory holds only the W2 stream,
+//                 brought in by tiled TMA in the 128-byte swizzled layout,
+//                 and the U / L tiles. The epilogue adds U_k, rounds to bf16 (the emitted
 //                 draft row that the verifier reads), stores it by TMA and
-//                 writes one softmax statistic per (request, 64-token tile).
-//   k_draft_pick  (one CTA per request) merges the tile statistics, finds the
+//                 writes one softmax statistic per (request, 128-token tile).
+//   k_draft_pick  (one warp per request) merges the tile statistics, finds the
 //                 tile where the running sum crosses u*Z, re-reads that tile's
-//                 64 emitted logits and returns the token: an inverse-CDF
+//                 128 emitted logits and returns the token: an inverse-CDF
 //                 draw of softmax(L_k / T) in ascending token order. It then
 //                 copies W1[x_k] into G for the next position.
 //
 // W2 is stored transposed, w2t[v][j] = W2[j][v], so both operands are K-major.
-// The tile is 128 requests x 64 tokens: small enough that a ring of 12 W2
-// chunks keeps three tiles of rank 256 in flight beside 4 U / L slots and the
-// batch's 64 KB of W1 rows, so that the stream of W2 is not serialised on one
-// memory latency per tile.
+// The tile is 128 requests x 128 tokens. With G in tensor memory (where the
+// MMA reads it without touching shared memory), a ring of 8 W2 chunks keeps two
+// tiles of rank 256 in flight beside 3 U / L slots, so the W2 stream is not
+// serialised on one memory latency per tile, and each MMA reads only its 4 KB
+// W2 slice from shared memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -40,22 +43,24 @@ namespace {
 constexpr int kDM = 128;                             // requests per tile (MMA M)
 constexpr int kDN = DSPARK_DRAFT_TILE;               // vocabulary per tile (MMA N)
 constexpr int kDK = 64;                              // K per chunk: one 128-byte row of bf16
-constexpr int kDMaxKC = DSPARK_DRAFT_MAX_RANK / kDK;  // chunks of the largest rank
-constexpr int kDStages = 12;  // W2 ring: 64 x 64 chunks, three tiles of rank 256 in flight
-constexpr int kDSlots = 4;    // U / L tile slots
-constexpr int kDEpiWarps = 8;                        // two groups of four
-constexpr int kDThreads = 64 + kDEpiWarps * 32;      // producer, MMA, epilogue
-constexpr uint32_t kBoxA = kDM * 128u;  // G chunk: 128 request rows x 128 bytes
-constexpr uint32_t kBoxW = kDN * 128u;  // W2 chunk: 64 vocabulary rows x 128 bytes
-constexpr uint32_t kBoxU = kDM * 128u;  // U / L tile: 128 request rows x 64 bf16
-constexpr uint32_t kOffA = 0;
-constexpr uint32_t kOffW = kOffA + kDMaxKC * kBoxA;
+constexpr int kDStages = 8;  // W2 ring: 128 x 64 chunks, two tiles of rank 256 in flight
+constexpr int kDSlots = 3;   // U / L tile slots
+constexpr int kDEpiWarps = 8;                        // two groups of four (warps 2..9)
+constexpr int kDThreads = 96 + kDEpiWarps * 32;      // W2 producer, MMA, epilogue, U producer
+constexpr int kDWarpU = 2 + kDEpiWarps;              // the U producer's warp
+constexpr uint32_t kBoxW = kDN * 128u;               // W2 chunk: 128 vocabulary rows x 128 B
+constexpr uint32_t kBoxU = kDM * 128u;               // half a U / L tile: 128 rows x 64 bf16
+constexpr uint32_t kOffW = 0;
 constexpr uint32_t kOffU = kOffW + kDStages * kBoxW;
-constexpr uint32_t kOffBar = kOffU + kDSlots * kBoxU;
+constexpr uint32_t kOffBar = kOffU + kDSlots * 2 * kBoxU;
 constexpr uint32_t kDraftSmem = kOffBar + 512 + 1024;  // barriers, 1024-byte alignment slack
-constexpr uint32_t kTmemCols = 2 * kDN;              // two accumulators
+// Tensor memory: two f32 accumulators of kDN columns, then G = W1[x_{k-1}] of
+// the request tile (row m in lane m, two bf16 per column: r / 2 columns).
+constexpr uint32_t kColG = 2 * kDN;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_bf16_f32(kDM, kDN);
-static_assert(kDN == 64 && kDK == 64, "epilogue and statistics assume 64-token tiles");
+static_assert(kDN == 128 && kDK == 64, "epilogue and statistics assume 128-token tiles");
+static_assert(kColG + DSPARK_DRAFT_MAX_RANK / 2 <= kTmemCols, "tensor memory columns");
 static_assert(kDraftSmem <= 232448, "shared memory of k_draft_step");
 
 struct DraftStat {  // one (request, tile): sum over the tile of 2^(L_v * c - R)
@@ -64,7 +69,7 @@ struct DraftStat {  // one (request, tile): sum over the tile of 2^(L_v * c - R)
 };
 
 struct DraftBars {
-  uint64_t a_full;
+  uint64_t a_full;  // G is in tensor memory (one arrival per epilogue warp)
   uint64_t w_full[kDStages], w_empty[kDStages];
   uint64_t u_full[kDSlots], u_empty[kDSlots];
   uint64_t acc_full[2], acc_empty[2];
@@ -80,7 +85,7 @@ struct DraftStepArgs {
   int32_t n_m;      // request tiles
   int32_t per_m;    // CTAs per request tile
   ExpParams ep;
-  DraftStat* stats;  // [n_tiles][B]
+  DraftStat* stats;  // [B][n_tiles]
   int32_t* status;
 };
 
@@ -116,14 +121,14 @@ __device__ __forceinline__ int32_t chunk_reference(float cm, float c_hi) {
   return cm > -INFINITY && cm < INFINITY ? static_cast<int32_t>(ceilf(cm * c_hi)) : INT_MIN;
 }
 
-// One epilogue tile of one thread: its request row m, 64 columns from tensor
-// memory (taddr) and from the U slot (ubase, 128-byte swizzled rows).
-// Writes the rounded row over U. Each 32-column chunk c gets its own reference
-// R_c and the pairwise sum S_c of 2^(L*c - R_c); the tile statistic is
-// (R, S) with R = max R_c and S = sum_c S_c 2^(R_c - R), the chunks folded in
-// order by exact power-of-two scaling. FULL: every column is inside the
-// vocabulary (no masks). Releases the accumulator (acc_empty) once its last
-// columns are in registers.
+// One epilogue tile of one thread: its request row m, 128 columns from
+// tensor memory (taddr) and from the U slot (ubase: two boxes of 64 columns,
+// 128-byte swizzled rows). Writes the rounded row over U. Each 32-column chunk
+// c gets its own reference R_c and the pairwise sum S_c of 2^(L*c - R_c); the
+// tile statistic is (R, S) with R = max R_c and S = sum_c S_c 2^(R_c - R), the
+// chunks folded in order by exact power-of-two scaling. FULL: every column is
+// inside the vocabulary (no masks). Releases the accumulator (acc_empty) once
+// its last columns are in registers.
 template <bool FULL>
 __device__ __forceinline__ void epi_tile(uint32_t taddr, uint32_t ubase, int m, int v0, int V,
                                          const ExpParams& ep, int32_t& R_out, float& S_out,
@@ -131,20 +136,20 @@ __device__ __forceinline__ void epi_tile(uint32_t taddr, uint32_t ubase, int m, 
   int32_t Rt = INT_MIN;
   float St = 0.f;
 #pragma unroll 1
-  for (int c4 = 0; c4 < 2; ++c4) {
+  for (int c4 = 0; c4 < 4; ++c4) {
     float acc[32];
     __syncwarp();
     tmem_ld32(taddr + c4 * 32, acc);
-    if (c4 == 1) {
+    if (c4 == 3) {
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
     }
-    const uint32_t row = ubase + m * 128;
+    const uint32_t row = ubase + (c4 >> 1) * kBoxU + m * 128;
     uint32_t lw[16];
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-      const uint32_t addr = row + (((c4 * 4 + jj) ^ (m & 7)) << 4);
+      const uint32_t addr = row + (((((c4 & 1) * 4) + jj) ^ (m & 7)) << 4);
       const uint4 u = lds128(addr);
       lw[4 * jj + 0] = pack_bf16x2(acc[8 * jj + 0] + bf16_lo(u.x), acc[8 * jj + 1] + bf16_hi(u.x));
       lw[4 * jj + 1] = pack_bf16x2(acc[8 * jj + 2] + bf16_lo(u.y), acc[8 * jj + 3] + bf16_hi(u.y));
@@ -208,8 +213,8 @@ __device__ __forceinline__ void epi_tile(uint32_t taddr, uint32_t ubase, int m, 
 // k_draft_step: bias GEMM + U + bf16 rounding + tile statistics, one position
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kDThreads, 1)
-    k_draft_step(const __grid_constant__ CUtensorMap mapG, const __grid_constant__ CUtensorMap mapW,
-                 const __grid_constant__ CUtensorMap mapU, const __grid_constant__ CUtensorMap mapL,
+    k_draft_step(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapU,
+                 const __grid_constant__ CUtensorMap mapL, const uint16_t* __restrict__ G,
                  const DraftStepArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -221,9 +226,17 @@ __global__ void __launch_bounds__(kDThreads, 1)
   const int p = blockIdx.x / a.n_m;
   const int n_local = p < a.n_tiles ? (a.n_tiles - p + a.per_m - 1) / a.per_m : 0;
   const int KC = a.r / kDK;
+  // this CTA's t-th vocabulary tile: every other position walks the vocabulary
+  // backwards, so that it starts on the W2 tiles the previous position read
+  // last (the ones most likely still in L2)
+  const bool backwards = a.k & 1;
+  auto tile_of = [&](int t) {
+    const int n = p + t * a.per_m;
+    return backwards ? a.n_tiles - 1 - n : n;
+  };
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars->a_full, 1);
+    mbar_init(&bars->a_full, kDEpiWarps);
     for (int s = 0; s < kDStages; ++s) {
       mbar_init(&bars->w_full[s], 1);
       mbar_init(&bars->w_empty[s], 1);
@@ -250,65 +263,52 @@ __global__ void __launch_bounds__(kDThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == 0) {
-    // ---------------- producer: one thread issues every TMA load ----------------
+    // ---------------- W2 producer: one thread streams the W2 chunks ----------------
     if (lane == 0) {
       tma_prefetch_map(&mapW);
-      tma_prefetch_map(&mapU);
-      tma_prefetch_map(&mapG);
-      const uint64_t pol_keep = policy_evict_last();    // W2 (other request tiles, steps)
-      const uint64_t pol_stream = policy_evict_first();  // U (read once)
+      const uint64_t pol_keep = policy_evict_last();  // W2 (other request tiles, steps)
       const int total = n_local * KC;
-      auto issue_w = [&](int q) {
-        const int t = q / KC, c = q % KC, s = q % kDStages;
-        mbar_arrive_expect_tx(&bars->w_full[s], kBoxW);
-        tma_load_2d(smem + kOffW + s * kBoxW, &mapW, c * kDK, (p + t * a.per_m) * kDN,
-                    &bars->w_full[s], pol_keep);
-      };
-      auto issue_u = [&](int t) {
-        const int slot = t % kDSlots;
-        const int v0 = (p + t * a.per_m) * kDN;
-        mbar_arrive_expect_tx(&bars->u_full[slot], kBoxU);
-        tma_load_3d(smem + kOffU + slot * kBoxU, &mapU, v0, a.k, m_tile * kDM,
-                    &bars->u_full[slot], pol_stream);
-      };
-      const int q0 = total < kDStages ? total : kDStages;
-      const int u0 = n_local < kDSlots ? n_local : kDSlots;
-      for (int q = 0; q < q0; ++q) issue_w(q);
-      for (int t = 0; t < u0; ++t) issue_u(t);
-      if (n_local > 0) {
-        mbar_arrive_expect_tx(&bars->a_full, KC * kBoxA);
-        for (int c = 0; c < KC; ++c)
-          tma_load_2d(smem + kOffA + c * kBoxA, &mapG, c * kDK, m_tile * kDM, &bars->a_full,
-                      pol_keep);
-      }
       bool ok = true;
-      int nq = q0, nu = u0;  // copies issued so far
-      for (int t = 0; t < n_local && ok; ++t) {
-        if (t >= kDSlots) {
-          const int slot = t % kDSlots;
-          ok = wait_or_flag(&bars->u_empty[slot], ((t / kDSlots) - 1) & 1, a.status);
+      int nq = 0;  // chunks issued so far
+      for (int q = 0; q < total; ++q) {
+        const int t = q / KC, c = q % KC, s = q % kDStages;
+        if (q >= kDStages) {
+          ok = wait_or_flag(&bars->w_empty[s], ((q / kDStages) - 1) & 1, a.status);
           if (!ok) break;
-          issue_u(t);
-          nu = t + 1;
         }
-        for (int c = 0; c < KC; ++c) {
-          const int q = t * KC + c;
-          if (q < q0) continue;
-          ok = wait_or_flag(&bars->w_empty[q % kDStages], ((q / kDStages) - 1) & 1, a.status);
-          if (!ok) break;
-          issue_w(q);
-          nq = q + 1;
-        }
+        mbar_arrive_expect_tx(&bars->w_full[s], kBoxW);
+        tma_load_2d(smem + kOffW + s * kBoxW, &mapW, c * kDK, tile_of(t) * kDN, &bars->w_full[s],
+                    pol_keep);
+        nq = q + 1;
       }
-      if (!ok) {
-        // give each copy still in flight a bounded chance to land before exit:
-        // the last phase issued on each stage and slot
+      if (!ok)  // give each copy still in flight a bounded chance to land before exit
         for (int q = nq - kDStages > 0 ? nq - kDStages : 0; q < nq; ++q)
           mbar_wait(&bars->w_full[q % kDStages], (q / kDStages) & 1);
+    }
+  } else if (warp == kDWarpU) {
+    // ---------------- U producer: one thread streams the U tiles ----------------
+    if (lane == 0) {
+      tma_prefetch_map(&mapU);
+      const uint64_t pol_stream = policy_evict_first();  // U (read once)
+      bool ok = true;
+      int nu = 0;  // tiles issued so far
+      for (int t = 0; t < n_local; ++t) {
+        const int slot = t % kDSlots;
+        if (t >= kDSlots) {
+          ok = wait_or_flag(&bars->u_empty[slot], ((t / kDSlots) - 1) & 1, a.status);
+          if (!ok) break;
+        }
+        const int v0 = tile_of(t) * kDN;
+        uint8_t* dst = smem + kOffU + slot * 2 * kBoxU;
+        mbar_arrive_expect_tx(&bars->u_full[slot], 2 * kBoxU);
+        tma_load_3d(dst, &mapU, v0, a.k, m_tile * kDM, &bars->u_full[slot], pol_stream);
+        tma_load_3d(dst + kBoxU, &mapU, v0 + kDK, a.k, m_tile * kDM, &bars->u_full[slot],
+                    pol_stream);
+        nu = t + 1;
+      }
+      if (!ok)
         for (int t = nu - kDSlots > 0 ? nu - kDSlots : 0; t < nu; ++t)
           mbar_wait(&bars->u_full[t % kDSlots], (t / kDSlots) & 1);
-        if (n_local > 0) mbar_wait(&bars->a_full, 0);
-      }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: one thread ----------------
@@ -328,12 +328,11 @@ __global__ void __launch_bounds__(kDThreads, 1)
           ok = wait_or_flag(&bars->w_full[s], (q / kDStages) & 1, a.status);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t a_base = sbase + kOffA + c * kBoxA;
           const uint32_t w_base = sbase + kOffW + s * kBoxW;
 #pragma unroll
           for (int j = 0; j < kDK / 16; ++j)
-            tc_mma(d, sdesc_sw128(a_base + 32 * j), sdesc_sw128(w_base + 32 * j), kIdesc,
-                   (c | j) != 0);
+            tc_mma_ts(d, tmem + kColG + c * (kDK / 2) + j * 8, sdesc_sw128(w_base + 32 * j),
+                      kIdesc, (c | j) != 0);
           tc_commit(&bars->w_empty[s]);
         }
         if (ok) tc_commit(&bars->acc_full[acc]);
@@ -352,19 +351,47 @@ __global__ void __launch_bounds__(kDThreads, 1)
     const bool row_ok = b < a.B;
     const bool leader = (warp == 2 + 4 * grp) && lane == 0;
     const uint64_t pol_out = policy_evict_first();
+    // G = W1[x_{k-1}] of this request tile into tensor memory (the MMA's A
+    // operand): group g writes K elements [128 g, 128 g + 128) of row m, as
+    // 32-bit columns of two bf16 each; rows past the batch get zeros
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(G + static_cast<size_t>(b) * a.r);
+      const int c0 = grp * 2;
+      const int nc = KC - c0 < 0 ? 0 : (KC - c0 > 2 ? 2 : KC - c0);
+      uint32_t w[2][32];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = row_ok && cc < nc ? __ldg(src + (c0 + cc) * 8 + i)
+                                            : make_uint4(0u, 0u, 0u, 0u);
+          w[cc][4 * i] = v.x;
+          w[cc][4 * i + 1] = v.y;
+          w[cc][4 * i + 2] = v.z;
+          w[cc][4 * i + 3] = v.w;
+        }
+      __syncwarp();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc)
+        if (cc < nc)
+          tmem_st32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kColG + (c0 + cc) * 32,
+                    w[cc]);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->a_full);
+    }
     for (int t = grp; t < n_local; t += 2) {
-      const int n = p + t * a.per_m;
+      const int n = tile_of(t);
       const int v0 = n * kDN;
       const int slot = t % kDSlots;
-      const uint32_t ubase = sbase + kOffU + slot * kBoxU;
+      const uint32_t ubase = sbase + kOffU + slot * 2 * kBoxU;
       // every lane waits (and so acquires); the warp then decides as one, so
       // that the aligned tensor-memory loads below run converged
       bool ok = wait_or_flag(&bars->acc_full[grp], (t >> 1) & 1, a.status);
       ok = ok && wait_or_flag(&bars->u_full[slot], (t / kDSlots) & 1, a.status);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
-      // four chunks of 32 columns: L = bf16(acc + U) over U in shared memory,
-      // and each chunk's sum of 2^(L*c - R_c) with its own reference R_c
       const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * kDN;
       int32_t R;
       float total;
@@ -378,7 +405,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       const bool bad = inf_seen || total != total;
       if (row_ok) {
         if (bad) set_status(a.status, DSPARK_ERR_BAD_DATA);
-        a.stats[static_cast<size_t>(n) * a.B + b] = DraftStat{bad ? 0.f : total, bad ? INT_MIN : R};
+        a.stats[static_cast<size_t>(b) * a.n_tiles + n] = DraftStat{bad ? 0.f : total, bad ? INT_MIN : R};
       }
       // the emitted rows go out by TMA once the group's writes are visible to
       // the asynchronous proxy (each writer fences, then arrives)
@@ -386,7 +413,10 @@ __global__ void __launch_bounds__(kDThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->st_ready[grp]);
       if (leader && wait_or_flag(&bars->st_ready[grp], (t >> 1) & 1, a.status)) {
-        tma_store_3d(&mapL, smem + kOffU + slot * kBoxU, v0, a.k, m_tile * kDM, pol_out);
+        tma_store_3d(&mapL, smem + kOffU + slot * 2 * kBoxU, v0, a.k, m_tile * kDM, pol_out);
+        if (v0 + kDK < a.V)
+          tma_store_3d(&mapL, smem + kOffU + slot * 2 * kBoxU + kBoxU, v0 + kDK, a.k,
+                       m_tile * kDM, pol_out);
         bulk_commit();
         bulk_wait_read<0>();
         mbar_arrive(&bars->u_empty[slot]);
@@ -434,7 +464,7 @@ __global__ void __launch_bounds__(32) k_draft_gather(const int32_t* __restrict__
 struct DraftPickArgs {
   int32_t B, V, r, gamma, k, n_tiles;
   ExpParams ep;
-  const DraftStat* stats;    // [n_tiles][B]
+  const DraftStat* stats;    // [B][n_tiles]
   const uint16_t* L;         // emitted rows [B][gamma][V]
   const float* uniforms;     // [B][gamma]
   const uint16_t* W1;        // [V][r]
@@ -443,146 +473,178 @@ struct DraftPickArgs {
   int32_t* status;
 };
 
-constexpr int kPickThreads = 128;
+constexpr int kPickWarps = 4;   // one request per warp
+constexpr int kPickBatch = 16;  // statistics loaded per round trip by a lane
 
-__global__ void __launch_bounds__(kPickThreads) k_draft_pick(const DraftPickArgs a) {
-  __shared__ int32_t s_red[kPickThreads / 32];
-  __shared__ double s_tot[kPickThreads / 32];
-  __shared__ int32_t s_tile;
-  __shared__ double s_before;
-  const int b = blockIdx.x;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const DraftStat* st = a.stats + b;  // tile g of request b at st[g * B]
-  const int per = (a.n_tiles + kPickThreads - 1) / kPickThreads;
-  const int g0 = t * per;
+__device__ __forceinline__ DraftStat ld_stat(const DraftStat* p) {
+  const int2 v = __ldg(reinterpret_cast<const int2*>(p));
+  return DraftStat{__int_as_float(v.x), v.y};
+}
+
+// 2^d for d <= 0 as a float, built from its exponent bits (0 below the
+// normal range, where a term is far below any mass that can decide a draw).
+__device__ __forceinline__ float pow2_nonpos(int d) {
+  return d < -126 ? 0.f : __int_as_float((d + 127) << 23);
+}
+
+__device__ __forceinline__ ff ff_scale(ff v, float p2) { return ff{v.hi * p2, v.lo * p2}; }
+
+__device__ __forceinline__ ff warp_incl_scan_ff(ff v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const ff u = shfl_up_ff(v, o);
+    if (lane >= o) v = ff_add(v, u);
+  }
+  return v;
+}
+
+// One warp draws position k of one request, in float-float arithmetic (about
+// 48 significant bits; this GPU's FP64 rate is far too low for it): lane l
+// owns the contiguous tiles [l * per, (l + 1) * per) of the request's
+// statistics, the warp scans their masses (the next lane's exclusive prefix is
+// bitwise this lane's inclusive one, so the lanes partition [0, Z)), the
+// owning lane walks its tiles to the crossing one, and the warp recomputes
+// that tile's 128 terms.
+__global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kPickWarps + (threadIdx.x >> 5);
+  if (b >= a.B) return;  // whole warps only
+  const DraftStat* st = a.stats + static_cast<size_t>(b) * a.n_tiles;
+  const int per = (a.n_tiles + 31) / 32;
+  const int g0 = lane * per;
   const int g1 = g0 + per < a.n_tiles ? g0 + per : a.n_tiles;
 
-  // common exponent reference: the largest tile reference
-  int32_t Rm = INT_MIN;
-  for (int g = g0; g < g1; ++g) {
-    const DraftStat d = st[static_cast<size_t>(g) * a.B];
-    if (d.s > 0.f && d.R > Rm) Rm = d.R;
-  }
+  // one pass over the lane's tiles, loads issued 16 at a time: the lane's
+  // largest reference Rl and its mass Sl = sum s 2^(R - Rl), rescaled exactly
+  // whenever Rl grows
+  int32_t Rl = INT_MIN;
+  ff Sl{0.f, 0.f};
+  for (int gb = g0; gb < g1; gb += kPickBatch) {
+    DraftStat d[kPickBatch];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) Rm = max(Rm, __shfl_xor_sync(0xFFFFFFFFu, Rm, o));
-  if (lane == 0) s_red[warp] = Rm;
-  if (t == 0) s_tile = -1;
-  __syncthreads();
-  int32_t Rmax = s_red[0];
-  for (int w = 1; w < kPickThreads / 32; ++w) Rmax = max(Rmax, s_red[w]);
-
-  const float u = a.uniforms[static_cast<size_t>(b) * a.gamma + a.k];
-  const bool u_ok = u >= 0.f && u < 1.f;
-  int y = 0;
-  if (Rmax == INT_MIN || !u_ok) {
-    if (t == 0) set_status(a.status, DSPARK_ERR_BAD_DATA);
-  } else {
-    // this thread's tile mass, then an inclusive scan over threads in
-    // ascending tile order; the next thread's exclusive prefix is bitwise this
-    // thread's inclusive one, so the threads partition [0, Z)
-    double S = 0.0;
-    for (int g = g0; g < g1; ++g) {
-      const DraftStat d = st[static_cast<size_t>(g) * a.B];
-      if (d.s > 0.f) S += ldexp(static_cast<double>(d.s), d.R - Rmax);
-    }
-    double inc = S;
+    for (int i = 0; i < kPickBatch; ++i)
+      d[i] = gb + i < g1 ? ld_stat(st + gb + i) : DraftStat{0.f, INT_MIN};
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-      if (lane >= o) inc += v;
-    }
-    if (lane == 31) s_tot[warp] = inc;
-    __syncthreads();
-    double off = 0.0, Z = 0.0;
-    for (int w = 0; w < kPickThreads / 32; ++w) {
-      if (w < warp) off += s_tot[w];
-      Z += s_tot[w];
-    }
-    // exclusive prefix = the previous lane's inclusive one (same expression)
-    const double prev = __shfl_up_sync(0xFFFFFFFFu, inc, 1);
-    const double excl = off + (lane > 0 ? prev : 0.0);
-    const double incl = off + inc;
-    const double target = static_cast<double>(u) * Z;
-    if (S > 0.0 && excl <= target && target < incl) {
-      double C = excl;
-      int gs = -1, glast = -1;
-      double Clast = excl;
-      for (int g = g0; g < g1; ++g) {
-        const DraftStat d = st[static_cast<size_t>(g) * a.B];
-        if (!(d.s > 0.f)) continue;
-        const double w = ldexp(static_cast<double>(d.s), d.R - Rmax);
-        if (C + w > target) {
-          gs = g;
-          break;
-        }
-        glast = g;
-        Clast = C;
-        C += w;
+    for (int i = 0; i < kPickBatch; ++i) {
+      if (!(d[i].s > 0.f)) continue;
+      if (d[i].R > Rl) {
+        Sl = Rl == INT_MIN ? ff{0.f, 0.f} : ff_scale(Sl, pow2_nonpos(Rl - d[i].R));
+        Rl = d[i].R;
       }
-      if (gs < 0) {  // rounding left the target past the last tile: take it
+      Sl = ff_add(Sl, ff{d[i].s * pow2_nonpos(d[i].R - Rl), 0.f});
+    }
+  }
+  int32_t Rmax = Rl;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Rmax = max(Rmax, __shfl_xor_sync(0xFFFFFFFFu, Rmax, o));
+  const float u = a.uniforms[static_cast<size_t>(b) * a.gamma + a.k];
+  int y = 0;
+  if (Rmax == INT_MIN || !(u >= 0.f && u < 1.f)) {
+    if (lane == 0) set_status(a.status, DSPARK_ERR_BAD_DATA);
+  } else {
+    const ff S = Rl == INT_MIN ? ff{0.f, 0.f} : ff_scale(Sl, pow2_nonpos(Rl - Rmax));
+    const bool has = S.hi > 0.f;
+    const ff incl = warp_incl_scan_ff(S, lane);
+    const ff prev = shfl_up_ff(incl, 1);
+    const ff excl = lane > 0 ? prev : ff{0.f, 0.f};
+    const ff Z = shfl_ff(incl, 31);
+    const ff target = ff_mul(ff{u, 0.f}, Z);
+    uint32_t own =
+        __ballot_sync(0xFFFFFFFFu, has && ff_cmp(excl, target) <= 0 && ff_cmp(target, incl) < 0);
+    if (!own) own = 1u << (31 - __clz(__ballot_sync(0xFFFFFFFFu, has)));  // rounding
+    const int ol = __ffs(own) - 1;
+    int gs = -1;
+    ff before{0.f, 0.f};
+    if (lane == ol) {  // walk this lane's tiles (cached since the pass above)
+      ff C = excl, Clast = excl;
+      int glast = -1;
+      for (int gb = g0; gb < g1 && gs < 0; gb += kPickBatch) {
+        DraftStat d[kPickBatch];
+#pragma unroll
+        for (int i = 0; i < kPickBatch; ++i)
+          d[i] = gb + i < g1 ? ld_stat(st + gb + i) : DraftStat{0.f, INT_MIN};
+#pragma unroll
+        for (int i = 0; i < kPickBatch; ++i) {
+          if (gs >= 0 || !(d[i].s > 0.f)) continue;
+          const ff next = ff_add(C, ff{d[i].s * pow2_nonpos(d[i].R - Rmax), 0.f});
+          if (ff_cmp(next, target) > 0) {
+            gs = gb + i;
+          } else {
+            glast = gb + i;
+            Clast = C;
+            C = next;
+          }
+        }
+      }
+      if (gs < 0) {  // rounding left the target past this lane's last tile: take it
         gs = glast;
         C = Clast;
       }
-      s_tile = gs;
-      s_before = C;
+      before = C;
     }
-    __syncthreads();
-    const int g = s_tile;
-    if (warp == 0 && g >= 0) {
-      // the crossing tile: recompute its 64 terms exactly as the step kernel
-      // did, each 32-column chunk (16 lanes) with its own reference
-      const int v = g * kDN + 2 * lane;
-      float z[2] = {-INFINITY, -INFINITY};
-      if (v < a.V) {  // V is a multiple of 8: v + 1 < V too
-        const uint32_t raw = *reinterpret_cast<const uint32_t*>(
+    const int g = __shfl_sync(0xFFFFFFFFu, gs, ol);
+    const ff s_before = shfl_ff(before, ol);
+    if (g >= 0) {
+      // the crossing tile: recompute its 128 terms exactly as the step kernel
+      // did, each 32-column chunk (8 lanes) with its own reference
+      const int v = g * kDN + 4 * lane;
+      float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (v < a.V) {  // V is a multiple of 8: v + 3 < V too
+        const uint2 raw = *reinterpret_cast<const uint2*>(
             a.L + (static_cast<size_t>(b) * a.gamma + a.k) * a.V + v);
-        z[0] = bf16_lo(raw);
-        z[1] = bf16_hi(raw);
+        z[0] = bf16_lo(raw.x);
+        z[1] = bf16_hi(raw.x);
+        z[2] = bf16_lo(raw.y);
+        z[3] = bf16_hi(raw.y);
       }
-      float cm = fmaxf(z[0], z[1]);
+      float cm = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
 #pragma unroll
-      for (int o = 1; o < 16; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, o));
+      for (int o = 1; o < 8; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, o));
       const int32_t Rc = chunk_reference(cm, a.ep.c_hi);
-      double w[2] = {0.0, 0.0};
+      float w[4] = {0.f, 0.f, 0.f, 0.f};
       if (Rc != INT_MIN && v < a.V) {
         const float nK = -static_cast<float>(Rc);
-        const double scale = ldexp(1.0, Rc - Rmax);
-        w[0] = static_cast<double>(exp_term(z[0], nK, a.ep)) * scale;
-        w[1] = static_cast<double>(exp_term(z[1], nK, a.ep)) * scale;
-      }
-      double inc_l = w[0] + w[1];
+        const float scale = pow2_nonpos(Rc - Rmax);
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double vv = __shfl_up_sync(0xFFFFFFFFu, inc_l, o);
-        if (lane >= o) inc_l += vv;
+        for (int e = 0; e < 4; ++e) w[e] = exp_term(z[e], nK, a.ep) * scale;
       }
-      const double pre = __shfl_up_sync(0xFFFFFFFFu, inc_l, 1);
-      const double base = s_before + (lane > 0 ? pre : 0.0);
-      const uint32_t cross = __ballot_sync(0xFFFFFFFFu, s_before + inc_l > target);
+      ff lsum{0.f, 0.f};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) lsum = ff_add(lsum, ff{w[e], 0.f});
+      const ff inc_l = warp_incl_scan_ff(lsum, lane);
+      const ff pre = shfl_up_ff(inc_l, 1);
+      const ff base = ff_add(s_before, lane > 0 ? pre : ff{0.f, 0.f});
+      const uint32_t cross = __ballot_sync(0xFFFFFFFFu, ff_cmp(ff_add(s_before, inc_l), target) > 0);
       int pick = -1;
       if (cross) {
         const int L0 = __ffs(cross) - 1;
         if (lane == L0) {
-          if (base + w[0] > target && w[0] > 0.0)
-            pick = v;
-          else
-            pick = w[1] > 0.0 ? v + 1 : v;
+          ff c = base;
+          int last = -1;
+          for (int e = 0; e < 4; ++e) {
+            if (w[e] > 0.f) last = e;
+            const ff nc = ff_add(c, ff{w[e], 0.f});
+            if (w[e] > 0.f && ff_cmp(nc, target) > 0) {
+              pick = v + e;
+              break;
+            }
+            c = nc;
+          }
+          if (pick < 0) pick = v + (last >= 0 ? last : 0);
         }
         pick = __shfl_sync(0xFFFFFFFFu, pick, L0);
       } else {  // rounding: the last token of the tile with positive weight
-        const int lpos = (w[1] > 0.0) ? 1 : (w[0] > 0.0) ? 0 : -1;
+        const int lpos = (w[3] > 0.f) ? 3 : (w[2] > 0.f) ? 2 : (w[1] > 0.f) ? 1 : (w[0] > 0.f) ? 0 : -1;
         const uint32_t any = __ballot_sync(0xFFFFFFFFu, lpos >= 0);
         const int Lh = any ? 31 - __clz(any) : 0;
         const int e = __shfl_sync(0xFFFFFFFFu, lpos, Lh);
-        pick = g * kDN + 2 * Lh + (e >= 0 ? e : 0);
+        pick = g * kDN + 4 * Lh + (e >= 0 ? e : 0);
       }
       y = pick;
     }
   }
-  if (warp == 0) {
-    if (lane == 0) a.tokens[static_cast<size_t>(b) * a.gamma + a.k] = y;
-    if (a.k + 1 < a.gamma) copy_row(a.W1, a.G, y, b, a.r, lane);
-  }
+  if (lane == 0) a.tokens[static_cast<size_t>(b) * a.gamma + a.k] = y;
+  if (a.k + 1 < a.gamma) copy_row(a.W1, a.G, y, b, a.r, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -691,11 +753,9 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
   DraftStat* stats = reinterpret_cast<DraftStat*>(
       static_cast<char*>(workspace) + DSPARK_ALIGN256(static_cast<size_t>(B) * r * 2));
 
-  CUtensorMap mapG, mapW, mapU, mapL;
+  CUtensorMap mapW, mapU, mapL;
   {
-    const cuuint64_t dg[2] = {static_cast<cuuint64_t>(r), static_cast<cuuint64_t>(B)};
     const cuuint64_t sg[1] = {static_cast<cuuint64_t>(r) * 2};
-    const cuuint32_t bx[2] = {kDK, kDM};
     const cuuint32_t bw[2] = {kDK, kDN};
     const cuuint64_t dw[2] = {static_cast<cuuint64_t>(r), static_cast<cuuint64_t>(V)};
     const cuuint64_t du[3] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(gamma),
@@ -703,7 +763,7 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
     const cuuint64_t su[2] = {static_cast<cuuint64_t>(V) * 2,
                               static_cast<cuuint64_t>(V) * 2 * static_cast<cuuint64_t>(gamma)};
     const cuuint32_t bu[3] = {kDK, 1, kDM};
-    if (!encode_map(&mapG, G, 2, dg, sg, bx) || !encode_map(&mapW, w2t, 2, dw, sg, bw) ||
+    if (!encode_map(&mapW, w2t, 2, dw, sg, bw) ||
         !encode_map(&mapU, base_logits, 3, du, su, bu) ||
         !encode_map(&mapL, draft_logits, 3, du, su, bu))
       return DSPARK_ERR_CUDA;
@@ -718,14 +778,15 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
   if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   for (int k = 0; k < gamma; ++k) {
     DraftStepArgs sa{B, Vi, r, gamma, k, n_tiles, n_m, per_m, ep, stats, device_status};
-    if (launch_plain(k_draft_step, n_m * per_m, kDThreads, kDraftSmem, stream, mapG, mapW, mapU,
-                   mapL, sa) != cudaSuccess)
+    if (launch_plain(k_draft_step, n_m * per_m, kDThreads, kDraftSmem, stream, mapW, mapU, mapL,
+                     static_cast<const uint16_t*>(G), sa) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     if (ev && cudaEventRecord(ev[2 + 2 * k], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
     DraftPickArgs pa{B,     Vi,       r, gamma, k,  n_tiles, ep, stats,
                      static_cast<const uint16_t*>(draft_logits), uniforms, W1, G, draft_tokens,
                      device_status};
-    if (launch_plain(k_draft_pick, B, kPickThreads, 0, stream, pa) != cudaSuccess)
+    if (launch_plain(k_draft_pick, (B + kPickWarps - 1) / kPickWarps, kPickWarps * 32, 0, stream,
+                     pa) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     if (ev && cudaEventRecord(ev[3 + 2 * k], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   }
