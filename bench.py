@@ -486,6 +486,20 @@ def drafter_measure(args, dev, stream, rank, ws):
         a1.record(stream)
         torch.cuda.synchronize(dev)
         ms.append(a0.elapsed_time(a1))
+    # a soak of back-to-back calls with the clocks sampled during it
+    clocks = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                          int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    time.sleep(0.3)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_soak = max(20, int(1.2 / max(statistics.median(ms) * 1e-3, 1e-4)))
+    s0.record(stream)
+    for _ in range(n_soak):
+        call()
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    soak_ms = s0.elapsed_time(s1) / n_soak
     g = sh["gamma"]
     step_ms, pick_ms = [], []
     for _ in range(3):
@@ -505,7 +519,9 @@ def drafter_measure(args, dev, stream, rank, ws):
         "config": {"workload": f"draft_b{sh['B']}_g{g}_v{sh['V']}_r{sh['r']}_bf16",
                    "weights": "random on the 2^-8 grid", "temperature": sh["temperature"],
                    "l2": "base logits (1.06 GB) larger than L2, no flush"},
+        "clocks": clk,
         "timing_ms": {"call_median": t_call, "call_p90": float(np.percentile(ms, 90)),
+                      "call_soak_mean": soak_ms,
                       "k_draft_step_median": t_step, "k_draft_pick_median":
                           statistics.median(pick_ms)},
         "roofline": {"bound": "hbm", "achieved": alg / (t_step * 1e-3) / 1e9, "unit": "GB/s",

@@ -104,10 +104,12 @@ typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
 #define DSPARK_DRAFT_TILE 128
 #define DSPARK_DRAFT_MAX_RANK 256
 /* Workspace of dspark_draft_markov, in bytes: the gathered embedding rows
-   W1[x_{k-1}] of the batch, then one statistic per (request, tile). */
+   W1[x_{k-1}] of the batch, two buffers of one statistic per (request, tile),
+   the grid-barrier words and one ready flag per request. */
 #define DSPARK_DRAFT_WS_BYTES(B, r, V)                                        \
   (DSPARK_ALIGN256((size_t)(B) * (size_t)(r) * 2u) +                          \
-   DSPARK_ALIGN256((size_t)(B) * DSPARK_CEILDIV((V), DSPARK_DRAFT_TILE) * 8u))
+   2u * DSPARK_ALIGN256((size_t)(B) * DSPARK_CEILDIV((V), DSPARK_DRAFT_TILE) * 8u) + \
+   256u + DSPARK_ALIGN256((size_t)(B) * 8u))
 
 /* Workspace of dspark_schedule, in bytes: two (key, index) buffers for the
    sort, per-request lengths and a header. */

@@ -75,6 +75,8 @@ struct DraftBars {
   uint64_t acc_full[2], acc_empty[2];
   uint64_t st_ready[2];  // a group's rows are in shared memory, ready to store
   uint64_t mma_done;
+  uint64_t epi_done;     // k_draft_block: the CTA's epilogue warps reached a grid barrier
+  uint64_t step_go;      // k_draft_block: the grid barrier was crossed
   uint32_t tmem_base;
 };
 static_assert(sizeof(DraftBars) <= 512, "barrier block");
@@ -471,14 +473,57 @@ struct DraftPickArgs {
   uint16_t* G;               // [B][r]
   int32_t* tokens;           // [B][gamma]
   int32_t* status;
+  unsigned long long* ready;  // k_draft_block: [B], (k + 1) << 32 | x_k once drawn
 };
 
-constexpr int kPickWarps = 4;   // one request per warp
-constexpr int kPickBatch = 16;  // statistics loaded per round trip by a lane
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_gpu64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
 
+constexpr int kPickWarps = 4;   // one request per warp
+constexpr int kPickBatch = 32;  // statistics loaded per round trip by a lane
+
+// A statistic through the read-only path (kCoherent false: written by an
+// earlier kernel) or through L2 only (written earlier in this kernel, at an
+// address reused every position).
+template <bool kCoherent>
 __device__ __forceinline__ DraftStat ld_stat(const DraftStat* p) {
-  const int2 v = __ldg(reinterpret_cast<const int2*>(p));
+  int2 v;
+  if constexpr (kCoherent)
+    asm volatile("ld.global.cg.v2.s32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+  else
+    v = __ldg(reinterpret_cast<const int2*>(p));
   return DraftStat{__int_as_float(v.x), v.y};
+}
+template <bool kCoherent>
+__device__ __forceinline__ uint2 ld_u2(const uint16_t* p) {
+  uint2 v;
+  if constexpr (kCoherent)
+    asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+  else
+    v = *reinterpret_cast<const uint2*>(p);
+  return v;
 }
 
 // 2^d for d <= 0 as a float, built from its exponent bits (0 below the
@@ -498,32 +543,32 @@ __device__ __forceinline__ ff warp_incl_scan_ff(ff v, int lane) {
   return v;
 }
 
-// One warp draws position k of one request, in float-float arithmetic (about
+// One warp draws position k of request b, in float-float arithmetic (about
 // 48 significant bits; this GPU's FP64 rate is far too low for it): lane l
 // owns the contiguous tiles [l * per, (l + 1) * per) of the request's
 // statistics, the warp scans their masses (the next lane's exclusive prefix is
 // bitwise this lane's inclusive one, so the lanes partition [0, Z)), the
 // owning lane walks its tiles to the crossing one, and the warp recomputes
 // that tile's 128 terms.
-__global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kPickWarps + (threadIdx.x >> 5);
-  if (b >= a.B) return;  // whole warps only
+template <bool kCoherent>
+__device__ __forceinline__ void draw_request(const DraftPickArgs& a, int b, int lane) {
   const DraftStat* st = a.stats + static_cast<size_t>(b) * a.n_tiles;
   const int per = (a.n_tiles + 31) / 32;
   const int g0 = lane * per;
   const int g1 = g0 + per < a.n_tiles ? g0 + per : a.n_tiles;
 
-  // one pass over the lane's tiles, loads issued 16 at a time: the lane's
-  // largest reference Rl and its mass Sl = sum s 2^(R - Rl), rescaled exactly
-  // whenever Rl grows
+  // one pass over the lane's tiles, loads issued kPickBatch at a time (all at
+  // once, and kept for the walk below, when they fit): the lane's largest
+  // reference Rl and its mass Sl = sum s 2^(R - Rl), rescaled exactly whenever
+  // Rl grows
   int32_t Rl = INT_MIN;
   ff Sl{0.f, 0.f};
+  DraftStat d[kPickBatch];
+  const bool held = per <= kPickBatch;
   for (int gb = g0; gb < g1; gb += kPickBatch) {
-    DraftStat d[kPickBatch];
 #pragma unroll
     for (int i = 0; i < kPickBatch; ++i)
-      d[i] = gb + i < g1 ? ld_stat(st + gb + i) : DraftStat{0.f, INT_MIN};
+      d[i] = gb + i < g1 ? ld_stat<kCoherent>(st + gb + i) : DraftStat{0.f, INT_MIN};
 #pragma unroll
     for (int i = 0; i < kPickBatch; ++i) {
       if (!(d[i].s > 0.f)) continue;
@@ -555,14 +600,15 @@ __global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickA
     const int ol = __ffs(own) - 1;
     int gs = -1;
     ff before{0.f, 0.f};
-    if (lane == ol) {  // walk this lane's tiles (cached since the pass above)
+    if (lane == ol) {  // walk this lane's tiles (still in registers when they fit)
       ff C = excl, Clast = excl;
       int glast = -1;
       for (int gb = g0; gb < g1 && gs < 0; gb += kPickBatch) {
-        DraftStat d[kPickBatch];
+        if (!held) {
 #pragma unroll
-        for (int i = 0; i < kPickBatch; ++i)
-          d[i] = gb + i < g1 ? ld_stat(st + gb + i) : DraftStat{0.f, INT_MIN};
+          for (int i = 0; i < kPickBatch; ++i)
+            d[i] = gb + i < g1 ? ld_stat<kCoherent>(st + gb + i) : DraftStat{0.f, INT_MIN};
+        }
 #pragma unroll
         for (int i = 0; i < kPickBatch; ++i) {
           if (gs >= 0 || !(d[i].s > 0.f)) continue;
@@ -590,8 +636,8 @@ __global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickA
       const int v = g * kDN + 4 * lane;
       float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (v < a.V) {  // V is a multiple of 8: v + 3 < V too
-        const uint2 raw = *reinterpret_cast<const uint2*>(
-            a.L + (static_cast<size_t>(b) * a.gamma + a.k) * a.V + v);
+        const uint2 raw =
+            ld_u2<kCoherent>(a.L + (static_cast<size_t>(b) * a.gamma + a.k) * a.V + v);
         z[0] = bf16_lo(raw.x);
         z[1] = bf16_hi(raw.x);
         z[2] = bf16_lo(raw.y);
@@ -644,7 +690,370 @@ __global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickA
     }
   }
   if (lane == 0) a.tokens[static_cast<size_t>(b) * a.gamma + a.k] = y;
-  if (a.k + 1 < a.gamma) copy_row(a.W1, a.G, y, b, a.r, lane);
+  if (a.ready) {  // publish the token: the next position's CTAs read W1[x_k] themselves
+    if (lane == 0 && a.k + 1 < a.gamma)
+      st_release_gpu64(&a.ready[b], (static_cast<unsigned long long>(a.k + 1) << 32) |
+                                        static_cast<uint32_t>(y));
+  } else if (a.k + 1 < a.gamma) {
+    copy_row(a.W1, a.G, y, b, a.r, lane);
+  }
+}
+
+__global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickArgs a) {
+  const int b = blockIdx.x * kPickWarps + (threadIdx.x >> 5);
+  if (b >= a.B) return;  // whole warps only
+  draw_request<false>(a, b, threadIdx.x & 31);
+}
+
+
+// ---------------------------------------------------------------------------
+// k_draft_block: the whole block of gamma positions in one persistent kernel
+// ---------------------------------------------------------------------------
+// The same roles as k_draft_step, kept alive across the positions of a block:
+// the producers stream W2 and U for position after position (the next
+// position's tiles load while the current one draws), the tensor memory and
+// the barriers stay set up, and the draws run inside the kernel between two
+// grid barriers (every CTA's statistics and rows of position k are written
+// before any warp draws; every G row of position k+1 is written before any CTA
+// loads it: each drawing warp publishes its request's row with a flag, and a
+// CTA waits only for its own rows; the statistics alternate between two
+// buffers, so a CTA already writing position k+1's may not overwrite what a
+// slower one still reads). Launched cooperatively (every CTA resident, one per
+// SM), so no wait can be on a CTA that is not running; every spin is bounded.
+constexpr uint32_t kGridSpinLimit = 1u << 22;
+
+// One thread per CTA. sync[0] counts arrivals and is 0 between uses (zeroed
+// before the launch, reset by the last arrival); sync[1] is a generation that
+// every CTA reads before its first arrival. Returns false if the wait gave up.
+__device__ bool grid_barrier(uint32_t* sync, uint32_t nctas, uint32_t& gen) {
+  const uint32_t g = gen;
+  __threadfence();
+  if (atom_add_acq_rel_gpu(&sync[0], 1u) == nctas - 1) {
+    atomicExch(&sync[0], 0u);
+    __threadfence();
+    st_release_gpu(&sync[1], g + 1u);
+  } else {
+    uint32_t i = 0;
+    while (ld_acquire_gpu(&sync[1]) == g) {
+      if (++i > kGridSpinLimit) return false;
+      __nanosleep(128);
+    }
+  }
+  gen = g + 1u;
+  __threadfence();
+  return true;
+}
+
+struct DraftBlockArgs {
+  DraftStepArgs s;     // s.k unused; s.stats: the statistics of even positions
+  DraftPickArgs p;     // p.k and p.stats set per position
+  DraftStat* stats1;   // the statistics of odd positions
+  const int32_t* anchors;       // x_0
+  uint32_t* sync;               // [2]
+  unsigned long long* ready;    // [B]
+};
+
+__global__ void __launch_bounds__(kDThreads, 1)
+    k_draft_block(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapU,
+                  const __grid_constant__ CUtensorMap mapL, const DraftBlockArgs ba) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  DraftBars* bars = reinterpret_cast<DraftBars*>(smem + kOffBar);
+  const DraftStepArgs& a = ba.s;
+  const uint32_t sbase = smem_addr(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tile = blockIdx.x % a.n_m;
+  const int p = blockIdx.x / a.n_m;
+  const int n_local = p < a.n_tiles ? (a.n_tiles - p + a.per_m - 1) / a.per_m : 0;
+  const int KC = a.r / kDK;
+  const int gamma = a.gamma;
+  // position k's t-th vocabulary tile of this CTA (odd positions walk backwards)
+  auto tile_of = [&](int k, int t) {
+    const int n = p + t * a.per_m;
+    return (k & 1) ? a.n_tiles - 1 - n : n;
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->a_full, kDEpiWarps);
+    for (int s = 0; s < kDStages; ++s) {
+      mbar_init(&bars->w_full[s], 1);
+      mbar_init(&bars->w_empty[s], 1);
+    }
+    for (int s = 0; s < kDSlots; ++s) {
+      mbar_init(&bars->u_full[s], 1);
+      mbar_init(&bars->u_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->acc_full[i], 1);
+      mbar_init(&bars->acc_empty[i], 4);
+      mbar_init(&bars->st_ready[i], 4);
+    }
+    mbar_init(&bars->mma_done, 1);
+    mbar_init(&bars->epi_done, kDEpiWarps);
+    mbar_init(&bars->step_go, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ---------------- W2 producer: every position's chunks, in order ----------------
+    if (lane == 0) {
+      tma_prefetch_map(&mapW);
+      const uint64_t pol_keep = policy_evict_last();
+      const int total = gamma * n_local * KC;
+      bool ok = true;
+      int nq = 0;
+      for (int q = 0; q < total; ++q) {
+        const int tg = q / KC, c = q % KC, s = q % kDStages;
+        if (q >= kDStages) {
+          ok = wait_or_flag(&bars->w_empty[s], ((q / kDStages) - 1) & 1, a.status);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(&bars->w_full[s], kBoxW);
+        tma_load_2d(smem + kOffW + s * kBoxW, &mapW, c * kDK,
+                    tile_of(tg / n_local, tg % n_local) * kDN, &bars->w_full[s], pol_keep);
+        nq = q + 1;
+      }
+      if (!ok)
+        for (int q = nq - kDStages > 0 ? nq - kDStages : 0; q < nq; ++q)
+          mbar_wait(&bars->w_full[q % kDStages], (q / kDStages) & 1);
+    }
+  } else if (warp == kDWarpU) {
+    // ---------------- U producer: every position's tiles, in order ----------------
+    if (lane == 0) {
+      tma_prefetch_map(&mapU);
+      const uint64_t pol_stream = policy_evict_first();
+      const int total = gamma * n_local;
+      bool ok = true;
+      int nu = 0;
+      for (int tg = 0; tg < total; ++tg) {
+        const int slot = tg % kDSlots;
+        if (tg >= kDSlots) {
+          ok = wait_or_flag(&bars->u_empty[slot], ((tg / kDSlots) - 1) & 1, a.status);
+          if (!ok) break;
+        }
+        const int k = tg / n_local;
+        const int v0 = tile_of(k, tg % n_local) * kDN;
+        uint8_t* dst = smem + kOffU + slot * 2 * kBoxU;
+        mbar_arrive_expect_tx(&bars->u_full[slot], 2 * kBoxU);
+        tma_load_3d(dst, &mapU, v0, k, m_tile * kDM, &bars->u_full[slot], pol_stream);
+        tma_load_3d(dst + kBoxU, &mapU, v0 + kDK, k, m_tile * kDM, &bars->u_full[slot],
+                    pol_stream);
+        nu = tg + 1;
+      }
+      if (!ok)
+        for (int t = nu - kDSlots > 0 ? nu - kDSlots : 0; t < nu; ++t)
+          mbar_wait(&bars->u_full[t % kDSlots], (t / kDSlots) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = true;
+      for (int k = 0; k < gamma && ok && n_local > 0; ++k) {
+        ok = wait_or_flag(&bars->a_full, k & 1, a.status);  // G of position k in tensor memory
+        if (!ok) break;
+        tc_fence_after();
+        for (int t = 0; t < n_local && ok; ++t) {
+          const int tg = k * n_local + t;
+          const int acc = tg & 1;
+          if (tg >= 2) {
+            ok = wait_or_flag(&bars->acc_empty[acc], ((tg >> 1) - 1) & 1, a.status);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          const uint32_t d = tmem + acc * kDN;
+          for (int c = 0; c < KC && ok; ++c) {
+            const int q = tg * KC + c, s = q % kDStages;
+            ok = wait_or_flag(&bars->w_full[s], (q / kDStages) & 1, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t w_base = sbase + kOffW + s * kBoxW;
+#pragma unroll
+            for (int j = 0; j < kDK / 16; ++j)
+              tc_mma_ts(d, tmem + kColG + c * (kDK / 2) + j * 8, sdesc_sw128(w_base + 32 * j),
+                        kIdesc, (c | j) != 0);
+            tc_commit(&bars->w_empty[s]);
+          }
+          if (ok) tc_commit(&bars->acc_full[acc]);
+        }
+      }
+      tc_commit(&bars->mma_done);
+      wait_or_flag(&bars->mma_done, 0, a.status);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue + draw warps ----------------
+    const int ew = warp - 2;          // 0..7
+    const int grp = ew >> 2;
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;
+    const int b = m_tile * kDM + m;
+    const bool row_ok = b < a.B;
+    const bool leader = (warp == 2 + 4 * grp) && lane == 0;
+    const bool syncer = warp == 2 && lane == 0;  // takes part in the grid barriers
+    const uint64_t pol_out = policy_evict_first();
+    uint32_t gen = 0;
+    if (syncer) gen = ld_acquire_gpu(&ba.sync[1]);
+    int jg = 0;        // tiles this group has finished (all positions)
+    int uses = 0;      // epi_done / step_go phases used so far
+    bool ok = true;
+    // a grid barrier: the CTA's eight warps report, one thread crosses, all go on
+    auto cta_grid_sync = [&]() {
+      if (lane == 0) mbar_arrive(&bars->epi_done);
+      bool good = true;
+      if (syncer) {
+        good = wait_or_flag(&bars->epi_done, uses & 1, a.status) &&
+               grid_barrier(ba.sync, gridDim.x, gen);
+        if (!good) set_status(a.status, DSPARK_ERR_TIMEOUT);
+        mbar_arrive(&bars->step_go);
+      }
+      good = wait_or_flag(&bars->step_go, uses & 1, a.status) && good;
+      ++uses;
+      return __all_sync(0xFFFFFFFFu, good);
+    };
+    for (int k = 0; k < gamma && ok; ++k) {
+      // G = W1[x_{k-1}] of this request tile into tensor memory: group g
+      // writes K elements [128 g, 128 g + 128) of row m (rows past the batch:
+      // 0). x_0 is the anchor; x_{k-1} comes with the flag its drawing warp
+      // published
+      int x = 0;
+      {
+        bool r_ok = true;
+        if (row_ok) {
+          if (k == 0) {
+            x = ba.anchors[b];
+            if (x < 0 || x >= a.V) {
+              set_status(a.status, DSPARK_ERR_BAD_DATA);
+              x = 0;
+            }
+          } else {
+            uint32_t i = 0;
+            unsigned long long f;
+            while (((f = ld_acquire_gpu64(&ba.ready[b])) >> 32) < static_cast<unsigned>(k)) {
+              if (++i > kGridSpinLimit) {
+                r_ok = false;
+                break;
+              }
+              __nanosleep(32);
+            }
+            x = static_cast<int>(static_cast<uint32_t>(f));
+          }
+        }
+        if (!__all_sync(0xFFFFFFFFu, r_ok)) {
+          set_status(a.status, DSPARK_ERR_TIMEOUT);
+          break;
+        }
+      }
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(ba.p.W1 + static_cast<size_t>(x) * a.r);
+        const int c0 = grp * 2;
+        const int nc = KC - c0 < 0 ? 0 : (KC - c0 > 2 ? 2 : KC - c0);
+        uint32_t w[2][32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint4 v = row_ok && cc < nc ? __ldg(src + (c0 + cc) * 8 + i)
+                                              : make_uint4(0u, 0u, 0u, 0u);
+            w[cc][4 * i] = v.x;
+            w[cc][4 * i + 1] = v.y;
+            w[cc][4 * i + 2] = v.z;
+            w[cc][4 * i + 3] = v.w;
+          }
+        __syncwarp();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc)
+          if (cc < nc)
+            tmem_st32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kColG + (c0 + cc) * 32,
+                      w[cc]);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->a_full);
+      }
+      // this position's tiles: tile tg of the block goes to group tg & 1
+      for (int t = 0; t < n_local; ++t) {
+        const int tg = k * n_local + t;
+        if ((tg & 1) != grp) continue;
+        const int n = tile_of(k, t);
+        const int v0 = n * kDN;
+        const int slot = tg % kDSlots;
+        const uint32_t ubase = sbase + kOffU + slot * 2 * kBoxU;
+        bool w_ok = wait_or_flag(&bars->acc_full[grp], (tg >> 1) & 1, a.status);
+        w_ok = w_ok && wait_or_flag(&bars->u_full[slot], (tg / kDSlots) & 1, a.status);
+        if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * kDN;
+        int32_t R;
+        float total;
+        bool inf_seen = false;
+        if (v0 + kDN <= a.V)
+          epi_tile<true>(taddr, ubase, m, v0, a.V, a.ep, R, total, inf_seen,
+                         &bars->acc_empty[grp], lane);
+        else
+          epi_tile<false>(taddr, ubase, m, v0, a.V, a.ep, R, total, inf_seen,
+                          &bars->acc_empty[grp], lane);
+        const bool bad = inf_seen || total != total;
+        if (row_ok) {
+          if (bad) set_status(a.status, DSPARK_ERR_BAD_DATA);
+          ((k & 1) ? ba.stats1 : a.stats)[static_cast<size_t>(b) * a.n_tiles + n] =
+              DraftStat{bad ? 0.f : total, bad ? INT_MIN : R};
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->st_ready[grp]);
+        if (leader && wait_or_flag(&bars->st_ready[grp], jg & 1, a.status)) {
+          tma_store_3d(&mapL, smem + kOffU + slot * 2 * kBoxU, v0, k, m_tile * kDM, pol_out);
+          if (v0 + kDK < a.V)
+            tma_store_3d(&mapL, smem + kOffU + slot * 2 * kBoxU + kBoxU, v0 + kDK, k,
+                         m_tile * kDM, pol_out);
+          bulk_commit();
+          bulk_wait_read<0>();
+          mbar_arrive(&bars->u_empty[slot]);
+        }
+        ++jg;
+        __syncwarp();
+      }
+      if (!ok) break;
+      // the rows of this position are in memory (stores complete, visible to
+      // the generic proxy of every CTA) and so are the statistics
+      if (leader) {
+        bulk_wait<0>();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      __threadfence();
+      if (!cta_grid_sync()) {
+        ok = false;
+        break;
+      }
+      // the draws: one warp per request, spread over every CTA
+      DraftPickArgs pa = ba.p;
+      pa.k = k;
+      pa.stats = (k & 1) ? ba.stats1 : a.stats;
+      pa.ready = ba.ready;
+      for (int rq = ew * gridDim.x + blockIdx.x; rq < a.B; rq += kDEpiWarps * gridDim.x)
+        draw_request<true>(pa, rq, lane);
+    }
+    if (leader) bulk_wait<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -652,6 +1061,7 @@ __global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickA
 // ---------------------------------------------------------------------------
 struct DraftDevice {
   bool ready = false;
+  bool coop = false;
   int sms = 0;
 };
 std::mutex g_draft_mutex;
@@ -674,7 +1084,7 @@ cudaError_t launch_plain(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t
 DraftDevice g_draft_dev[128];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-int draft_setup(int& sms) {
+int draft_setup(int& sms, bool& coop) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return DSPARK_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_draft_mutex);
@@ -692,11 +1102,18 @@ int draft_setup(int& sms) {
     if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     if (cudaFuncSetAttribute(k_draft_step, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kDraftSmem)) != cudaSuccess ||
+        cudaFuncSetAttribute(k_draft_block, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kDraftSmem)) != cudaSuccess)
       return DSPARK_ERR_CUDA;
+    int coop = 0;
+    if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    d.coop = coop != 0;
     d.ready = true;
   }
   sms = d.sms;
+  coop = d.coop;
   return DSPARK_OK;
 }
 
@@ -741,7 +1158,8 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
     return DSPARK_ERR_INVALID_ARG;
   if (workspace_bytes < DSPARK_DRAFT_WS_BYTES(B, r, V)) return DSPARK_ERR_WORKSPACE;
   int sms = 0;
-  if (int rc = draft_setup(sms)) return rc;
+  bool coop = false;
+  if (int rc = draft_setup(sms, coop)) return rc;
 
   const int Vi = static_cast<int>(V);
   const int n_tiles = (Vi + kDN - 1) / kDN;
@@ -752,6 +1170,12 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
   uint16_t* G = static_cast<uint16_t*>(workspace);
   DraftStat* stats = reinterpret_cast<DraftStat*>(
       static_cast<char*>(workspace) + DSPARK_ALIGN256(static_cast<size_t>(B) * r * 2));
+  DraftStat* stats1 = stats + DSPARK_ALIGN256(static_cast<size_t>(B) * n_tiles * 8) / 8;
+  uint32_t* sync = reinterpret_cast<uint32_t*>(
+      static_cast<char*>(workspace) + DSPARK_ALIGN256(static_cast<size_t>(B) * r * 2) +
+      2 * DSPARK_ALIGN256(static_cast<size_t>(B) * n_tiles * 8));
+  unsigned long long* ready =
+      reinterpret_cast<unsigned long long*>(sync + 64);  // 256 bytes after the barrier words
 
   CUtensorMap mapW, mapU, mapL;
   {
@@ -772,6 +1196,34 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
   const ExpParams ep = draft_exp_params(temperature);
   const uint16_t* W1 = static_cast<const uint16_t*>(w1);
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
+  const int grid = n_m * per_m;
+  if (!ev && coop && grid <= sms) {
+    // the whole block in one cooperative launch (every CTA resident, one per SM)
+    if (cudaMemsetAsync(sync, 0, 256 + static_cast<size_t>(B) * 8, stream) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    DraftBlockArgs ba;
+    ba.s = DraftStepArgs{B, Vi, r, gamma, 0, n_tiles, n_m, per_m, ep, stats, device_status};
+    ba.p = DraftPickArgs{B,     Vi,       r, gamma, 0,  n_tiles, ep, stats,
+                         static_cast<const uint16_t*>(draft_logits), uniforms, W1, G,
+                         draft_tokens, device_status, nullptr};
+    ba.stats1 = stats1;
+    ba.anchors = anchors;
+    ba.sync = sync;
+    ba.ready = ready;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = kDThreads;
+    cfg.dynamicSmemBytes = kDraftSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_draft_block, mapW, mapU, mapL, ba) == cudaSuccess)
+      return DSPARK_OK;
+    (void)cudaGetLastError();  // not resident as one grid: fall back to one launch per step
+  }
   if (launch_plain(k_draft_gather, B, 32, 0, stream, anchors, W1, G, B, Vi, r, device_status) !=
       cudaSuccess)
     return DSPARK_ERR_CUDA;
@@ -784,7 +1236,7 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
     if (ev && cudaEventRecord(ev[2 + 2 * k], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
     DraftPickArgs pa{B,     Vi,       r, gamma, k,  n_tiles, ep, stats,
                      static_cast<const uint16_t*>(draft_logits), uniforms, W1, G, draft_tokens,
-                     device_status};
+                     device_status, nullptr};
     if (launch_plain(k_draft_pick, (B + kPickWarps - 1) / kPickWarps, kPickWarps * 32, 0, stream,
                      pa) != cudaSuccess)
       return DSPARK_ERR_CUDA;

@@ -73,6 +73,21 @@ def test_named_and_large(dev, R, g):
     assert ell.sum() == ref["n_admitted"] or ref["near_ties"]
 
 
+@pytest.mark.parametrize("R,g", [(256, 16), (4096, 1), (1, 32), (4097, 1),
+                                 (257, 16), (255, 16), (129, 31)])
+def test_shapes_and_ties(dev, R, g):
+    """The headline 256 x 16 and shapes around it: gamma = 1 (runs of one
+    candidate), one request of 32, request counts that are not powers of two,
+    with ties from repeated confidences and certain tokens (c = 1)."""
+    rng = np.random.default_rng(R * 31 + g)
+    conf = workloads.make_confidences(R, g, seed=R + g)
+    conf[rng.uniform(size=(R, g)) < 0.2] = 1.0
+    conf[:, :] = np.where(rng.uniform(size=(R, g)) < 0.1, conf[0, 0], conf)
+    N = np.arange(R * (g + 1) + 1, dtype=np.float64)
+    for T in (workloads.step_time_profile(R * (g + 1) + 1), 2.0 + 0.01 * N + 0.4 * (N % 7 == 0)):
+        check(conf, T, dev)
+
+
 def test_flat_profile_admits_everything(dev):
     conf = workloads.make_confidences(256, 16, seed=1)
     ell, _ = check(conf, np.full(256 * 17 + 1, 4.0), dev)
