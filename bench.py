@@ -529,7 +529,8 @@ def drafter_measure(args, dev, stream, rank, ws):
                      "kernel": "k_draft_step (median CUDA-event interval around each of the 16 "
                                "launches, dspark_draft_markov_timed)",
                      "tensor_tflops": flops / (t_step * 1e-3) / 1e12},
-        "gpu_launches_per_call": 1 + 2 * g,
+        "gpu_launches_per_call": 1,  # k_draft_block (cooperative), after one 2 KB memset
+        "gpu_launches_per_call_timed_path": 1 + 2 * g,
         "cpu_baseline": None,
     }
     del out_L
