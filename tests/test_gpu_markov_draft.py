@@ -77,6 +77,18 @@ def test_matches_oracle(dev, B, gamma, V, r, T):
     assert excused <= max(1, B // 100)
 
 
+def test_batch_too_large_for_one_resident_grid(dev):
+    """B = 20,000 needs 157 request tiles, more than one CTA per SM can hold at
+    once, so the call takes the per-launch path (gather, then a step and a
+    draw kernel per position); results as on the single-launch path."""
+    B, gamma, V, r = 20000, 2, 64, 64
+    d = workloads.make_markov_draft(B, gamma, V, r, temperature=1.0, seed=21, device="cpu")
+    L, x = run_gpu(d, dev)
+    ref = run_oracle(d)
+    excused = compare_chains(L, x, ref, range(B))
+    assert excused <= B // 100
+
+
 def test_in_place(dev):
     d = workloads.make_markov_draft(33, 5, 3000, 256, seed=3, device="cpu")
     g = d.to(dev)
