@@ -272,6 +272,19 @@ def native_arm(args):
     ell = sbuf.verify_len.cpu().numpy()
     positions = int(ell.sum())
     logit_bytes = vi.logit_bytes(ell)
+    # bytes beyond the algorithmic ones: the draw re-reads two rows per
+    # rejected request (target and draft at k* = m + 1) and the bonus target row
+    # otherwise; B_min is what a left-to-right early-exit design would read
+    m_acc = vbuf.accepted_len.cpu().numpy().astype(np.int64)
+    rej = m_acc < ell
+    row_bytes = vi.V * vi.target_logits.element_size()
+    resample_bytes = int((np.where(rej, 2, 1)).sum()) * row_bytes
+    b_min_bytes = int(np.where(rej, 2 * (m_acc + 1), 2 * ell + 1).sum()) * row_bytes
+    # a checksum of the inputs (64-bit sums of their bit patterns)
+    ck = [int(t.contiguous().view(torch.int16 if t.element_size() == 2 else torch.int32)
+              .to(torch.int64).sum().item()) & 0xFFFFFFFFFFFFFFFF
+          for t in (vi.target_logits, vi.draft_logits, vi.draft_tokens, vi.uniforms)]
+    input_checksum = "-".join(f"{c:016x}" for c in ck)
 
     # timed region: the serving loop, pipelined as section 5.2's asynchronous
     # scheduler is -- step i+1's schedule runs on a side stream beside step i's
@@ -418,10 +431,16 @@ def native_arm(args):
         svi = cpu_sample_inputs(n_req)
         ts = [run_oracle_sample(svi, cores) for _ in range(3)]
         t = statistics.median(ts)
+        # one thread, on a smaller sample of the same recipe
+        n1 = max(1, min(16, n_req))
+        s1 = cpu_sample_inputs(n1, seed=8)
+        t1 = run_oracle_sample(s1, 1)
         cpu = {"value": int(svi.verify_len.sum()) / t, "unit": UNIT, "cores": cores,
                "kind": "oracle",
                "sample": f"{n_req} of 256 requests of {WORKLOAD} (host-generated, same recipe), "
                          f"median of 3 passes, {t:.2f} s wall each, OpenMP over requests",
+               "single_thread_value": int(s1.verify_len.sum()) / t1,
+               "single_thread_sample": f"{n1} requests, one pass, {t1:.2f} s wall",
                "cpu": cpu_model()}
 
     if rank != 0:
@@ -445,14 +464,18 @@ def native_arm(args):
         "config": {"workload": WORKLOAD, "B": vi.B, "gamma": vi.gamma, "V": vi.V,
                    "temperature": vi.temperature, "positions_per_step": positions,
                    "logit_bytes_per_step": logit_bytes,
+                   "input_checksum": input_checksum,
                    "l2": "inputs (2.18 GB) larger than L2, no flush",
                    "step": "dspark_schedule (flat profile) + dspark_verify; step i+1's "
                            "schedule on a side stream beside step i's verify"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
+                     "nominal_peak": 7900.0, "frac_of_nominal": achieved / 7900.0,
                      "kernel": "k_rowstats_tma (streaming pass; median CUDA-event interval "
                                "around its launch, dspark_verify_timed)",
                      "peak_source": peak_src},
+        "bytes_per_step": {"algorithmic": logit_bytes, "resample_reread": resample_bytes,
+                           "actual": logit_bytes + resample_bytes, "b_min_early_exit": b_min_bytes},
         "roofline_call": {"bound": "hbm", "achieved": achieved_call, "peak": peak,
                           "unit": "GB/s", "frac": achieved_call / peak,
                           "scope": "whole dspark_verify call (k_plan, k_rowstats_tma, k_desc, "
