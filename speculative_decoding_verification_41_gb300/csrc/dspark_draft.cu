@@ -212,231 +212,6 @@ __device__ __forceinline__ void epi_tile(uint32_t taddr, uint32_t ubase, int m, 
 }
 
 // ---------------------------------------------------------------------------
-// k_draft_step: bias GEMM + U + bf16 rounding + tile statistics, one position
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kDThreads, 1)
-    k_draft_step(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapU,
-                 const __grid_constant__ CUtensorMap mapL, const uint16_t* __restrict__ G,
-                 const DraftStepArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  DraftBars* bars = reinterpret_cast<DraftBars*>(smem + kOffBar);
-  const uint32_t sbase = smem_addr(smem);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tile = blockIdx.x % a.n_m;
-  const int p = blockIdx.x / a.n_m;
-  const int n_local = p < a.n_tiles ? (a.n_tiles - p + a.per_m - 1) / a.per_m : 0;
-  const int KC = a.r / kDK;
-  // this CTA's t-th vocabulary tile: every other position walks the vocabulary
-  // backwards, so that it starts on the W2 tiles the previous position read
-  // last (the ones most likely still in L2)
-  const bool backwards = a.k & 1;
-  auto tile_of = [&](int t) {
-    const int n = p + t * a.per_m;
-    return backwards ? a.n_tiles - 1 - n : n;
-  };
-
-  if (threadIdx.x == 0) {
-    mbar_init(&bars->a_full, kDEpiWarps);
-    for (int s = 0; s < kDStages; ++s) {
-      mbar_init(&bars->w_full[s], 1);
-      mbar_init(&bars->w_empty[s], 1);
-    }
-    for (int s = 0; s < kDSlots; ++s) {
-      mbar_init(&bars->u_full[s], 1);
-      mbar_init(&bars->u_empty[s], 1);
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->acc_full[i], 1);
-      mbar_init(&bars->acc_empty[i], 4);
-      mbar_init(&bars->st_ready[i], 4);
-    }
-    mbar_init(&bars->mma_done, 1);
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
-
-  if (warp == 0) {
-    // ---------------- W2 producer: one thread streams the W2 chunks ----------------
-    if (lane == 0) {
-      tma_prefetch_map(&mapW);
-      const uint64_t pol_keep = policy_evict_last();  // W2 (other request tiles, steps)
-      const int total = n_local * KC;
-      bool ok = true;
-      int nq = 0;  // chunks issued so far
-      for (int q = 0; q < total; ++q) {
-        const int t = q / KC, c = q % KC, s = q % kDStages;
-        if (q >= kDStages) {
-          ok = wait_or_flag(&bars->w_empty[s], ((q / kDStages) - 1) & 1, a.status);
-          if (!ok) break;
-        }
-        mbar_arrive_expect_tx(&bars->w_full[s], kBoxW);
-        tma_load_2d(smem + kOffW + s * kBoxW, &mapW, c * kDK, tile_of(t) * kDN, &bars->w_full[s],
-                    pol_keep);
-        nq = q + 1;
-      }
-      if (!ok)  // give each copy still in flight a bounded chance to land before exit
-        for (int q = nq - kDStages > 0 ? nq - kDStages : 0; q < nq; ++q)
-          mbar_wait(&bars->w_full[q % kDStages], (q / kDStages) & 1);
-    }
-  } else if (warp == kDWarpU) {
-    // ---------------- U producer: one thread streams the U tiles ----------------
-    if (lane == 0) {
-      tma_prefetch_map(&mapU);
-      const uint64_t pol_stream = policy_evict_first();  // U (read once)
-      bool ok = true;
-      int nu = 0;  // tiles issued so far
-      for (int t = 0; t < n_local; ++t) {
-        const int slot = t % kDSlots;
-        if (t >= kDSlots) {
-          ok = wait_or_flag(&bars->u_empty[slot], ((t / kDSlots) - 1) & 1, a.status);
-          if (!ok) break;
-        }
-        const int v0 = tile_of(t) * kDN;
-        uint8_t* dst = smem + kOffU + slot * 2 * kBoxU;
-        mbar_arrive_expect_tx(&bars->u_full[slot], 2 * kBoxU);
-        tma_load_3d(dst, &mapU, v0, a.k, m_tile * kDM, &bars->u_full[slot], pol_stream);
-        tma_load_3d(dst + kBoxU, &mapU, v0 + kDK, a.k, m_tile * kDM, &bars->u_full[slot],
-                    pol_stream);
-        nu = t + 1;
-      }
-      if (!ok)
-        for (int t = nu - kDSlots > 0 ? nu - kDSlots : 0; t < nu; ++t)
-          mbar_wait(&bars->u_full[t % kDSlots], (t / kDSlots) & 1);
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer: one thread ----------------
-    if (lane == 0) {
-      bool ok = n_local == 0 || wait_or_flag(&bars->a_full, 0, a.status);
-      tc_fence_after();
-      for (int t = 0; t < n_local && ok; ++t) {
-        const int acc = t & 1;
-        if (t >= 2) {
-          ok = wait_or_flag(&bars->acc_empty[acc], ((t >> 1) - 1) & 1, a.status);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        const uint32_t d = tmem + acc * kDN;
-        for (int c = 0; c < KC && ok; ++c) {
-          const int q = t * KC + c, s = q % kDStages;
-          ok = wait_or_flag(&bars->w_full[s], (q / kDStages) & 1, a.status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t w_base = sbase + kOffW + s * kBoxW;
-#pragma unroll
-          for (int j = 0; j < kDK / 16; ++j)
-            tc_mma_ts(d, tmem + kColG + c * (kDK / 2) + j * 8, sdesc_sw128(w_base + 32 * j),
-                      kIdesc, (c | j) != 0);
-          tc_commit(&bars->w_empty[s]);
-        }
-        if (ok) tc_commit(&bars->acc_full[acc]);
-      }
-      // every MMA issued has completed before tensor memory is released
-      tc_commit(&bars->mma_done);
-      wait_or_flag(&bars->mma_done, 0, a.status);
-    }
-    __syncwarp();
-  } else {
-    // ---------------- epilogue: two groups of four warps, alternate tiles ----------------
-    const int grp = (warp - 2) >> 2;
-    const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
-    const int m = quarter * 32 + lane;
-    const int b = m_tile * kDM + m;
-    const bool row_ok = b < a.B;
-    const bool leader = (warp == 2 + 4 * grp) && lane == 0;
-    const uint64_t pol_out = policy_evict_first();
-    // G = W1[x_{k-1}] of this request tile into tensor memory (the MMA's A
-    // operand): group g writes K elements [128 g, 128 g + 128) of row m, as
-    // 32-bit columns of two bf16 each; rows past the batch get zeros
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(G + static_cast<size_t>(b) * a.r);
-      const int c0 = grp * 2;
-      const int nc = KC - c0 < 0 ? 0 : (KC - c0 > 2 ? 2 : KC - c0);
-      uint32_t w[2][32];
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = row_ok && cc < nc ? __ldg(src + (c0 + cc) * 8 + i)
-                                            : make_uint4(0u, 0u, 0u, 0u);
-          w[cc][4 * i] = v.x;
-          w[cc][4 * i + 1] = v.y;
-          w[cc][4 * i + 2] = v.z;
-          w[cc][4 * i + 3] = v.w;
-        }
-      __syncwarp();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc)
-        if (cc < nc)
-          tmem_st32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kColG + (c0 + cc) * 32,
-                    w[cc]);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->a_full);
-    }
-    for (int t = grp; t < n_local; t += 2) {
-      const int n = tile_of(t);
-      const int v0 = n * kDN;
-      const int slot = t % kDSlots;
-      const uint32_t ubase = sbase + kOffU + slot * 2 * kBoxU;
-      // every lane waits (and so acquires); the warp then decides as one, so
-      // that the aligned tensor-memory loads below run converged
-      bool ok = wait_or_flag(&bars->acc_full[grp], (t >> 1) & 1, a.status);
-      ok = ok && wait_or_flag(&bars->u_full[slot], (t / kDSlots) & 1, a.status);
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * kDN;
-      int32_t R;
-      float total;
-      bool inf_seen = false;
-      if (v0 + kDN <= a.V)
-        epi_tile<true>(taddr, ubase, m, v0, a.V, a.ep, R, total, inf_seen, &bars->acc_empty[grp],
-                       lane);
-      else
-        epi_tile<false>(taddr, ubase, m, v0, a.V, a.ep, R, total, inf_seen,
-                        &bars->acc_empty[grp], lane);
-      const bool bad = inf_seen || total != total;
-      if (row_ok) {
-        if (bad) set_status(a.status, DSPARK_ERR_BAD_DATA);
-        a.stats[static_cast<size_t>(b) * a.n_tiles + n] = DraftStat{bad ? 0.f : total, bad ? INT_MIN : R};
-      }
-      // the emitted rows go out by TMA once the group's writes are visible to
-      // the asynchronous proxy (each writer fences, then arrives)
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->st_ready[grp]);
-      if (leader && wait_or_flag(&bars->st_ready[grp], (t >> 1) & 1, a.status)) {
-        tma_store_3d(&mapL, smem + kOffU + slot * 2 * kBoxU, v0, a.k, m_tile * kDM, pol_out);
-        if (v0 + kDK < a.V)
-          tma_store_3d(&mapL, smem + kOffU + slot * 2 * kBoxU + kBoxU, v0 + kDK, a.k,
-                       m_tile * kDM, pol_out);
-        bulk_commit();
-        bulk_wait_read<0>();
-        mbar_arrive(&bars->u_empty[slot]);
-      }
-      __syncwarp();
-    }
-    if (leader) bulk_wait<0>();
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-// ---------------------------------------------------------------------------
 // k_draft_gather: G[b] = W1[x_0(b)] before the first position
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void copy_row(const uint16_t* __restrict__ W1, uint16_t* __restrict__ G,
@@ -760,9 +535,12 @@ __global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickA
 
 
 // ---------------------------------------------------------------------------
-// k_draft_block: the whole block of gamma positions in one persistent kernel
+// draft_tiles: the tile stage of positions [k_begin, k_end)
 // ---------------------------------------------------------------------------
-// The same roles as k_draft_step, kept alive across the positions of a block:
+// Two instantiations. k_draft_step runs one position per launch and leaves the
+// draw to k_draft_pick (G comes from the buffer the previous draw wrote).
+// k_draft_block runs the whole block of gamma positions in one persistent
+// kernel: the roles stay alive across the positions, so
 // the producers stream W2 and U for position after position (the next
 // position's tiles load while the current one draws), the tensor memory and
 // the barriers stay set up, and the draws run inside the kernel between two
@@ -798,17 +576,19 @@ __device__ bool grid_barrier(uint32_t* sync, uint32_t nctas, uint32_t& gen) {
 }
 
 struct DraftBlockArgs {
-  DraftStepArgs s;     // s.k unused; s.stats: the statistics of even positions
+  DraftStepArgs s;     // s.k unused; s.stats: the statistics (of even positions)
   DraftPickArgs p;     // p.k and p.stats set per position
-  DraftStat* stats1;   // the statistics of odd positions
+  int32_t k_begin, k_end;       // the positions this launch runs
+  const uint16_t* G;            // per-launch path: G = W1[x_{k-1}] written by the previous draw
+  DraftStat* stats1;            // single launch: the statistics of odd positions
   const int32_t* anchors;       // x_0
   uint32_t* sync;               // [2]
   unsigned long long* ready;    // [B]
 };
 
-__global__ void __launch_bounds__(kDThreads, 1)
-    k_draft_block(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapU,
-                  const __grid_constant__ CUtensorMap mapL, const DraftBlockArgs ba) {
+template <bool kBlock>
+__device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUtensorMap& mapU,
+                                            const CUtensorMap& mapL, const DraftBlockArgs& ba) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -820,7 +600,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
   const int p = blockIdx.x / a.n_m;
   const int n_local = p < a.n_tiles ? (a.n_tiles - p + a.per_m - 1) / a.per_m : 0;
   const int KC = a.r / kDK;
-  const int gamma = a.gamma;
+  const int k0 = ba.k_begin;
+  const int npos = ba.k_end - ba.k_begin;  // positions of this launch
   // position k's t-th vocabulary tile of this CTA (odd positions walk backwards)
   auto tile_of = [&](int k, int t) {
     const int n = p + t * a.per_m;
@@ -861,7 +642,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     if (lane == 0) {
       tma_prefetch_map(&mapW);
       const uint64_t pol_keep = policy_evict_last();
-      const int total = gamma * n_local * KC;
+      const int total = npos * n_local * KC;
       bool ok = true;
       int nq = 0;
       for (int q = 0; q < total; ++q) {
@@ -872,7 +653,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         }
         mbar_arrive_expect_tx(&bars->w_full[s], kBoxW);
         tma_load_2d(smem + kOffW + s * kBoxW, &mapW, c * kDK,
-                    tile_of(tg / n_local, tg % n_local) * kDN, &bars->w_full[s], pol_keep);
+                    tile_of(k0 + tg / n_local, tg % n_local) * kDN, &bars->w_full[s], pol_keep);
         nq = q + 1;
       }
       if (!ok)
@@ -884,7 +665,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     if (lane == 0) {
       tma_prefetch_map(&mapU);
       const uint64_t pol_stream = policy_evict_first();
-      const int total = gamma * n_local;
+      const int total = npos * n_local;
       bool ok = true;
       int nu = 0;
       for (int tg = 0; tg < total; ++tg) {
@@ -893,7 +674,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
           ok = wait_or_flag(&bars->u_empty[slot], ((tg / kDSlots) - 1) & 1, a.status);
           if (!ok) break;
         }
-        const int k = tg / n_local;
+        const int k = k0 + tg / n_local;
         const int v0 = tile_of(k, tg % n_local) * kDN;
         uint8_t* dst = smem + kOffU + slot * 2 * kBoxU;
         mbar_arrive_expect_tx(&bars->u_full[slot], 2 * kBoxU);
@@ -910,12 +691,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       bool ok = true;
-      for (int k = 0; k < gamma && ok && n_local > 0; ++k) {
-        ok = wait_or_flag(&bars->a_full, k & 1, a.status);  // G of position k in tensor memory
+      for (int j = 0; j < npos && ok && n_local > 0; ++j) {
+        ok = wait_or_flag(&bars->a_full, j & 1, a.status);  // G of position k0 + j in tensor memory
         if (!ok) break;
         tc_fence_after();
         for (int t = 0; t < n_local && ok; ++t) {
-          const int tg = k * n_local + t;
+          const int tg = j * n_local + t;
           const int acc = tg & 1;
           if (tg >= 2) {
             ok = wait_or_flag(&bars->acc_empty[acc], ((tg >> 1) - 1) & 1, a.status);
@@ -930,9 +711,9 @@ __global__ void __launch_bounds__(kDThreads, 1)
             tc_fence_after();
             const uint32_t w_base = sbase + kOffW + s * kBoxW;
 #pragma unroll
-            for (int j = 0; j < kDK / 16; ++j)
-              tc_mma_ts(d, tmem + kColG + c * (kDK / 2) + j * 8, sdesc_sw128(w_base + 32 * j),
-                        kIdesc, (c | j) != 0);
+            for (int kk = 0; kk < kDK / 16; ++kk)
+              tc_mma_ts(d, tmem + kColG + c * (kDK / 2) + kk * 8, sdesc_sw128(w_base + 32 * kk),
+                        kIdesc, (c | kk) != 0);
             tc_commit(&bars->w_empty[s]);
           }
           if (ok) tc_commit(&bars->acc_full[acc]);
@@ -973,13 +754,14 @@ __global__ void __launch_bounds__(kDThreads, 1)
       ++uses;
       return __all_sync(0xFFFFFFFFu, good);
     };
-    for (int k = 0; k < gamma && ok; ++k) {
+    for (int j = 0; j < npos && ok; ++j) {
+      const int k = k0 + j;
       // G = W1[x_{k-1}] of this request tile into tensor memory: group g
       // writes K elements [128 g, 128 g + 128) of row m (rows past the batch:
-      // 0). x_0 is the anchor; x_{k-1} comes with the flag its drawing warp
-      // published
+      // 0). Single launch: x_0 is the anchor and x_{k-1} comes with the flag its
+      // drawing warp published; per launch: the row the previous kernel wrote
       int x = 0;
-      {
+      if constexpr (kBlock) {
         bool r_ok = true;
         if (row_ok) {
           if (k == 0) {
@@ -1007,7 +789,9 @@ __global__ void __launch_bounds__(kDThreads, 1)
         }
       }
       {
-        const uint4* src = reinterpret_cast<const uint4*>(ba.p.W1 + static_cast<size_t>(x) * a.r);
+        const uint16_t* row = kBlock ? ba.p.W1 + static_cast<size_t>(x) * a.r
+                                     : ba.G + static_cast<size_t>(b) * a.r;
+        const uint4* src = reinterpret_cast<const uint4*>(row);
         const int c0 = grp * 2;
         const int nc = KC - c0 < 0 ? 0 : (KC - c0 > 2 ? 2 : KC - c0);
         uint32_t w[2][32];
@@ -1035,7 +819,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       }
       // this position's tiles: tile tg of the block goes to group tg & 1
       for (int t = 0; t < n_local; ++t) {
-        const int tg = k * n_local + t;
+        const int tg = j * n_local + t;
         if ((tg & 1) != grp) continue;
         const int n = tile_of(k, t);
         const int v0 = n * kDN;
@@ -1061,7 +845,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         const bool bad = inf_seen || total != total;
         if (row_ok) {
           if (bad) set_status(a.status, DSPARK_ERR_BAD_DATA);
-          ((k & 1) ? ba.stats1 : a.stats)[static_cast<size_t>(b) * a.n_tiles + n] =
+          ((kBlock && (k & 1)) ? ba.stats1 : a.stats)[static_cast<size_t>(b) * a.n_tiles + n] =
               DraftStat{bad ? 0.f : total, bad ? INT_MIN : R};
         }
         fence_proxy_async();
@@ -1080,6 +864,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         __syncwarp();
       }
       if (!ok) break;
+      if constexpr (!kBlock) break;  // one position; the draw is the next kernel
       // the rows of this position are in memory (stores complete, visible to
       // the generic proxy of every CTA) and so are the statistics
       if (leader) {
@@ -1109,6 +894,21 @@ __global__ void __launch_bounds__(kDThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// One position per launch (the per-launch path: grids that cannot be resident
+// at once, and the timed entry point); the draw is k_draft_pick.
+__global__ void __launch_bounds__(kDThreads, 1)
+    k_draft_step(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapU,
+                 const __grid_constant__ CUtensorMap mapL, const DraftBlockArgs ba) {
+  draft_tiles<false>(mapW, mapU, mapL, ba);
+}
+
+// The whole block in one cooperative launch, draws included.
+__global__ void __launch_bounds__(kDThreads, 1)
+    k_draft_block(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapU,
+                  const __grid_constant__ CUtensorMap mapL, const DraftBlockArgs ba) {
+  draft_tiles<true>(mapW, mapU, mapL, ba);
 }
 
 // ---------------------------------------------------------------------------
@@ -1256,11 +1056,14 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
     // the whole block in one cooperative launch (every CTA resident, one per SM)
     if (cudaMemsetAsync(sync, 0, 256 + static_cast<size_t>(B) * 8, stream) != cudaSuccess)
       return DSPARK_ERR_CUDA;
-    DraftBlockArgs ba;
+    DraftBlockArgs ba{};
     ba.s = DraftStepArgs{B, Vi, r, gamma, 0, n_tiles, n_m, per_m, ep, stats, device_status};
     ba.p = DraftPickArgs{B,     Vi,       r, gamma, 0,  n_tiles, ep, stats,
                          static_cast<const uint16_t*>(draft_logits), uniforms, W1, G,
                          draft_tokens, device_status, nullptr};
+    ba.k_begin = 0;
+    ba.k_end = gamma;
+    ba.G = nullptr;
     ba.stats1 = stats1;
     ba.anchors = anchors;
     ba.sync = sync;
@@ -1284,9 +1087,16 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
     return DSPARK_ERR_CUDA;
   if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   for (int k = 0; k < gamma; ++k) {
-    DraftStepArgs sa{B, Vi, r, gamma, k, n_tiles, n_m, per_m, ep, stats, device_status};
+    DraftBlockArgs sa{};
+    sa.s = DraftStepArgs{B, Vi, r, gamma, k, n_tiles, n_m, per_m, ep, stats, device_status};
+    sa.p = DraftPickArgs{B,     Vi,       r, gamma, k,  n_tiles, ep, stats,
+                         static_cast<const uint16_t*>(draft_logits), uniforms, W1, G,
+                         draft_tokens, device_status, nullptr};
+    sa.k_begin = k;
+    sa.k_end = k + 1;
+    sa.G = G;
     if (launch_plain(k_draft_step, n_m * per_m, kDThreads, kDraftSmem, stream, mapW, mapU, mapL,
-                     static_cast<const uint16_t*>(G), sa) != cudaSuccess)
+                     sa) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     if (ev && cudaEventRecord(ev[2 + 2 * k], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
     DraftPickArgs pa{B,     Vi,       r, gamma, k,  n_tiles, ep, stats,
