@@ -907,28 +907,31 @@ __global__ void __launch_bounds__(kDecideWarps * 32) k_desc(
 // row pair each): for dspark_verify the residual (or bonus) weights of every
 // request's draw, for dspark_acceptance the minima of every verified position.
 // Persistent, W warps per CTA and one CTA per SM, like the streaming pass:
-// warp w takes items w, w + GW, ...
-// (item = s * B + r for segment s of request r) through its own ring of 4 KB stages,
-// each holding 2 KB of the target row and 2 KB of the draft row (only the
-// target row for a bonus draw), fed by bulk copies; the ring runs on across
-// items. k_pick then draws each request's token from the segment sums.
-
+// warp w takes items w, w + GW, ... (item = s * n_jobs + j for segment s of
+// job j: a warp's items fall in different segments, so that the segments rich
+// in heavy tokens do not all land on the same warps) through its own ring of
+// stages, each holding kRowPart bytes of the target row and kRowPart bytes of
+// the draft row (only the target row for a bonus draw), fed by bulk copies;
+// the ring runs on across items. The descriptors of a warp's next 32 items are
+// loaded together, one per lane, so that setting up an item costs shuffles,
+// not a dependent load. k_pick then draws each request's token from the
+// segment sums.
 struct __align__(16) StageInfo {  // what a ring stage holds; written by lane 0
   float nK, E_hi, E_lo, D_hi, D_lo;
-  int32_t mode;   // kModeResidual or kModeTarget
-  int32_t bytes;  // bytes of each row in the stage
-  int32_t last;   // the item's last stage
-  int32_t r, s;   // request and segment
-  int32_t pad[2];
+  int32_t mode;    // kModeResidual, kModeTarget or kModeMin
+  int32_t bytes;   // bytes of each row in the stage
+  int32_t out;     // the item's last stage: index of its sum; otherwise -1
 };
-static_assert(sizeof(StageInfo) == 48, "StageInfo layout");
+static_assert(sizeof(StageInfo) == 32, "StageInfo layout");
 
-struct __align__(16) ResidCursor {  // a warp's producer position; lane 0's, in shared memory
-  StageInfo item;                   // parameters of the item being copied
-  long long pi;                     // the item
-  const char* p_t;                  // its target-row segment
-  const char* p_d;                  // its draft-row segment
-  int pc, n_st, ib, have;           // next stage, stages, bytes per row, an item is set up
+// One lane's share of a batch of 32 items: the descriptor of item base + lane.
+struct ItemRegs {
+  const char* p_t;  // target-row segment
+  const char* p_d;  // draft-row segment
+  float nK, E_hi, E_lo, D_hi, D_lo;
+  int32_t mode;     // kModeNone: nothing to sum
+  int32_t bytes;    // bytes of each row in the segment
+  int32_t out;      // index of the segment's sum
 };
 
 template <typename Tin, int W, int STAGES, int kRowPart>
@@ -936,12 +939,12 @@ __global__ void __launch_bounds__(W * 32, 1)
     k_resid(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int n_jobs, int V, int n_seg,
             ExpParams ep, const ResampleDesc* __restrict__ jobs, ff* __restrict__ sums,
             int32_t* status) {
-  const int B = n_jobs;
   constexpr int RPL = kRowPart / 16 / 32;  // 16-byte vectors per lane and row part
   constexpr int kSegBytes = kSeg * static_cast<int>(sizeof(Tin));
+  constexpr int kStage = 2 * kRowPart;  // target part, then draft part
+  constexpr unsigned kFull = 0xFFFFFFFFu;
   extern __shared__ __align__(1024) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kStage = 2 * kRowPart;  // target part, then draft part
   unsigned char* buf = smem + static_cast<size_t>(warp) * STAGES * kStage;
   uint64_t* bars =
       reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(W) * STAGES * kStage) +
@@ -949,8 +952,6 @@ __global__ void __launch_bounds__(W * 32, 1)
   StageInfo* info =
       reinterpret_cast<StageInfo*>(smem + static_cast<size_t>(W) * STAGES * (kStage + 8)) +
       warp * STAGES;
-  ResidCursor* curs = reinterpret_cast<ResidCursor*>(
-      smem + static_cast<size_t>(W) * STAGES * (kStage + 8 + sizeof(StageInfo)));
   if (lane == 0) {
     for (int st = 0; st < STAGES; ++st) mbar_init(&bars[st], 1);
     fence_barrier_init();
@@ -960,71 +961,108 @@ __global__ void __launch_bounds__(W * 32, 1)
   pdl_trigger();
 
   const long long row_bytes = static_cast<long long>(V) * sizeof(Tin);
-  const long long N = static_cast<long long>(B) * n_seg;
+  const long long N = static_cast<long long>(n_jobs) * n_seg;
   const long long GW = static_cast<long long>(gridDim.x) * W;
+  const long long g0 = static_cast<long long>(blockIdx.x) * W + warp;
+  const int n_items = g0 < N ? static_cast<int>((N - 1 - g0) / GW + 1) : 0;
 
-  // producer cursor (lane 0): the item being copied and its next stage
-  ResidCursor& cu = curs[warp];
-  auto locate = [&]() {  // next item with something to draw, if any
-    cu.have = 0;
-    for (; cu.pi < N; cu.pi += GW) {
-      // segment-major: a warp's items fall in different segments, so that the
-      // segments rich in heavy tokens do not all land on the same warps
-      const int sg = static_cast<int>(cu.pi / B);
-      const int r = static_cast<int>(cu.pi - static_cast<long long>(sg) * B);
-      const ResampleDesc d = jobs[r];  // written by the previous kernel
-      if (d.mode != kModeResidual && d.mode != kModeTarget && d.mode != kModeMin) continue;
-      const long long left = row_bytes - static_cast<long long>(sg) * kSegBytes;
-      cu.ib = static_cast<int>(left < kSegBytes ? left : kSegBytes);
-      cu.n_st = (cu.ib + kRowPart - 1) / kRowPart;
-      const long long off = static_cast<long long>(sg) * kSegBytes;
-      cu.p_t = reinterpret_cast<const char*>(tl) + d.t_row * row_bytes + off;
-      cu.p_d = reinterpret_cast<const char*>(dl) + d.d_row * row_bytes + off;
-      cu.item.nK = -static_cast<float>(d.K_t);
-      cu.item.E_hi = d.E_hi;
-      cu.item.E_lo = d.E_lo;
-      cu.item.D_hi = d.D_hi;
-      cu.item.D_lo = d.D_lo;
-      cu.item.mode = d.mode;
-      cu.item.r = r;
-      cu.item.s = sg;
-      cu.pc = 0;
-      cu.have = 1;
+  ItemRegs mine{};
+  auto load_batch = [&](int base) {  // lane l: the descriptor of item base + l
+    mine.mode = kModeNone;
+    const int k = base + lane;
+    if (k < n_items) {
+      const long long i = g0 + static_cast<long long>(k) * GW;
+      const int sg = static_cast<int>(i / n_jobs);
+      const int j = static_cast<int>(i - static_cast<long long>(sg) * n_jobs);
+      const ResampleDesc d = jobs[j];  // written by the previous kernel
+      if (d.mode == kModeResidual || d.mode == kModeTarget || d.mode == kModeMin) {
+        const long long off = static_cast<long long>(sg) * kSegBytes;
+        const long long left = row_bytes - off;
+        mine.bytes = static_cast<int>(left < kSegBytes ? left : kSegBytes);
+        mine.p_t = reinterpret_cast<const char*>(tl) + d.t_row * row_bytes + off;
+        mine.p_d = reinterpret_cast<const char*>(dl) + d.d_row * row_bytes + off;
+        mine.nK = -static_cast<float>(d.K_t);
+        mine.E_hi = d.E_hi;
+        mine.E_lo = d.E_lo;
+        mine.D_hi = d.D_hi;
+        mine.D_lo = d.D_lo;
+        mine.out = j * n_seg + sg;
+        mine.mode = d.mode;
+      }
+    }
+  };
+
+  // producer (warp-uniform state; lane 0 issues): item kp, its next stage pc
+  int kp = 0, pc = 0, batch = -1;
+  ItemRegs cur{};
+  bool have = false;
+  auto next_item = [&]() {  // sets up the next item with something to sum, if any
+    have = false;
+    for (; kp < n_items; ++kp) {
+      if ((kp >> 5) != batch) {
+        batch = kp >> 5;
+        load_batch(batch << 5);
+      }
+      const int l = kp & 31;
+      const int mode = __shfl_sync(kFull, mine.mode, l);
+      if (mode == kModeNone) continue;
+      cur.mode = mode;
+      cur.p_t = reinterpret_cast<const char*>(
+          __shfl_sync(kFull, reinterpret_cast<unsigned long long>(mine.p_t), l));
+      cur.p_d = reinterpret_cast<const char*>(
+          __shfl_sync(kFull, reinterpret_cast<unsigned long long>(mine.p_d), l));
+      cur.nK = __shfl_sync(kFull, mine.nK, l);
+      cur.E_hi = __shfl_sync(kFull, mine.E_hi, l);
+      cur.E_lo = __shfl_sync(kFull, mine.E_lo, l);
+      cur.D_hi = __shfl_sync(kFull, mine.D_hi, l);
+      cur.D_lo = __shfl_sync(kFull, mine.D_lo, l);
+      cur.bytes = __shfl_sync(kFull, mine.bytes, l);
+      cur.out = __shfl_sync(kFull, mine.out, l);
+      pc = 0;
+      have = true;
       return;
     }
   };
-  auto issue = [&](int st) {  // lane 0, cu.have
-    const int bytes = min(kRowPart, cu.ib - cu.pc * kRowPart);
-    StageInfo& in = info[st];
-    in = cu.item;
-    in.bytes = bytes;
-    in.last = cu.pc == cu.n_st - 1;
-    const bool two = cu.item.mode != kModeTarget;
-    mbar_arrive_expect_tx(&bars[st], static_cast<uint32_t>(two ? 2 * bytes : bytes));
-    bulk_g2s(buf + st * kStage, cu.p_t + static_cast<long long>(cu.pc) * kRowPart,
-             static_cast<uint32_t>(bytes), &bars[st]);
-    if (two)
-      bulk_g2s(buf + st * kStage + kRowPart, cu.p_d + static_cast<long long>(cu.pc) * kRowPart,
-               static_cast<uint32_t>(bytes), &bars[st]);
-    if (++cu.pc == cu.n_st) {
-      cu.pi += GW;
-      locate();
+  auto issue = [&](int st) {  // one stage of the current item
+    const int left = cur.bytes - pc * kRowPart;
+    const uint32_t bytes = static_cast<uint32_t>(left < kRowPart ? left : kRowPart);
+    const bool last = left <= kRowPart;
+    if (lane == 0) {
+      StageInfo in;
+      in.nK = cur.nK;
+      in.E_hi = cur.E_hi;
+      in.E_lo = cur.E_lo;
+      in.D_hi = cur.D_hi;
+      in.D_lo = cur.D_lo;
+      in.mode = cur.mode;
+      in.bytes = static_cast<int>(bytes);
+      in.out = last ? cur.out : -1;
+      info[st] = in;
+      const bool two = cur.mode != kModeTarget;
+      mbar_arrive_expect_tx(&bars[st], two ? 2 * bytes : bytes);
+      bulk_g2s(buf + st * kStage, cur.p_t + static_cast<long long>(pc) * kRowPart, bytes,
+               &bars[st]);
+      if (two)
+        bulk_g2s(buf + st * kStage + kRowPart, cur.p_d + static_cast<long long>(pc) * kRowPart,
+                 bytes, &bars[st]);
+    }
+    ++pc;
+    if (last) {
+      ++kp;
+      next_item();
     }
   };
+
   int inflight = 0;
-  if (lane == 0) {
-    cu.pi = static_cast<long long>(blockIdx.x) * W + warp;
-    locate();
-    while (inflight < STAGES && cu.have) issue(inflight++);
-  }
-  inflight = __shfl_sync(0xFFFFFFFFu, inflight, 0);
+  next_item();
+  while (inflight < STAGES && have) issue(inflight++);
 
   int stage = 0;
   uint32_t phase = 0;
   LaneAcc acc;
   while (inflight > 0) {
     // every lane waits (each gets the barrier's acquire); the give-up decision is warp-uniform
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[stage], phase))) {
+    if (!__all_sync(kFull, mbar_wait(&bars[stage], phase))) {
       if (lane == 0) set_status(status, DSPARK_ERR_TIMEOUT);
       for (int q = 0; q < inflight; ++q) {  // let the copies in flight land before leaving
         int s2 = stage + q;
@@ -1041,10 +1079,11 @@ __global__ void __launch_bounds__(W * 32, 1)
     const bool two = in.mode != kModeTarget;
     uint4 v[2 * RPL];
     const uint4* sp = reinterpret_cast<const uint4*>(buf + stage * kStage);
+    const int n_vec = in.bytes == kRowPart ? RPL : (in.bytes / 16 - lane + 31) / 32;
 #pragma unroll
     for (int q = 0; q < RPL; ++q) {
       const int idx = q * 32 + lane;
-      const bool ok = idx * 16 < in.bytes;
+      const bool ok = q < n_vec;
       v[q] = ok ? sp[idx] : make_uint4(0u, 0u, 0u, 0u);
       v[RPL + q] = (ok && two) ? sp[kRowPart / 16 + idx] : v[q];
     }
@@ -1055,15 +1094,13 @@ __global__ void __launch_bounds__(W * 32, 1)
       phase ^= 1u;
     }
     --inflight;
-    if (lane == 0 && cu.have) {  // the ring was full: the freed stage is the next one to fill
-      fence_proxy_async();
+    if (have) {  // the ring was full: the freed stage is the next one to fill
+      if (lane == 0) fence_proxy_async();
       issue(freed);
       ++inflight;
     }
-    inflight = __shfl_sync(0xFFFFFFFFu, inflight, 0);
 
     const WeightParams wp{in.mode, in.nK, in.D_hi, in.D_lo, in.E_hi, in.E_lo};
-    const int n_vec = in.bytes == kRowPart ? RPL : (in.bytes / 16 - lane + 31) / 32;
 #pragma unroll
     for (int q = 0; q < RPL; ++q) {
       if (q >= n_vec) break;
@@ -1078,11 +1115,11 @@ __global__ void __launch_bounds__(W * 32, 1)
       if (!light) sum = heavy_vec_sum<Tin>(v[q], v[RPL + q], wp, ep);
       kahan_add(acc, sum);
     }
-    if (in.last) {
+    if (in.out >= 0) {
       float hi = acc.s, lo = -acc.comp;
       warp_two_sum(hi, lo);
       acc = LaneAcc();
-      if (lane == 0) sums[static_cast<long long>(in.r) * n_seg + in.s] = ff_norm(hi, lo);
+      if (lane == 0) sums[in.out] = ff_norm(hi, lo);
     }
   }
 }
@@ -1174,24 +1211,36 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// k_rate_finish: one thread per position adds its segment sums in order and
-// divides by S_t; -1 where there is no job.
-__global__ void __launch_bounds__(256)
+// k_rate_finish: one warp per position adds its segment sums (lanes take
+// every 32nd sum, then a butterfly, all in float pairs) and divides by S_t;
+// -1 where there is no job.
+constexpr int kFinishWarps = 8;
+__global__ void __launch_bounds__(kFinishWarps * 32)
     k_rate_finish(int n_jobs, int n_seg, const ResampleDesc* __restrict__ jobs,
                   const ff* __restrict__ sums, float* __restrict__ rates) {
   pdl_wait();  // predecessor grid complete, its writes visible
   pdl_trigger();
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= n_jobs) return;
+  const int lane = threadIdx.x & 31;
+  const int j = blockIdx.x * kFinishWarps + (threadIdx.x >> 5);
+  if (j >= n_jobs) return;  // whole warps only
   const ResampleDesc d = jobs[j];
   if (d.mode != kModeMin) {
-    rates[j] = -1.f;
+    if (lane == 0) rates[j] = -1.f;
     return;
   }
+  const ff* s = sums + static_cast<long long>(j) * n_seg;
   ff t{0.f, 0.f};
-  for (int sg = 0; sg < n_seg; ++sg) t = ff_add(t, sums[static_cast<long long>(j) * n_seg + sg]);
-  const double rate = (static_cast<double>(t.hi) + t.lo) / (static_cast<double>(d.S_hi) + d.S_lo);
-  rates[j] = static_cast<float>(rate);
+  for (int sg = lane; sg < n_seg; sg += 32) t = ff_add(t, s[sg]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const ff u{__shfl_xor_sync(0xFFFFFFFFu, t.hi, o), __shfl_xor_sync(0xFFFFFFFFu, t.lo, o)};
+    t = ff_add(t, u);
+  }
+  if (lane == 0) {
+    const double rate =
+        (static_cast<double>(t.hi) + t.lo) / (static_cast<double>(d.S_hi) + d.S_lo);
+    rates[j] = static_cast<float>(rate);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1220,8 +1269,7 @@ constexpr int kResidStages = 3;
 constexpr int kResidPart = 2048;
 constexpr size_t resid_smem_bytes() {
   return static_cast<size_t>(kResidWarps) * kResidStages *
-             (2 * kResidPart + sizeof(uint64_t) + sizeof(StageInfo)) +
-         static_cast<size_t>(kResidWarps) * sizeof(ResidCursor);
+         (2 * kResidPart + sizeof(uint64_t) + sizeof(StageInfo));
 }
 static_assert(resid_smem_bytes() <= 227 * 1024, "shared memory of k_resid");
 
@@ -1554,7 +1602,8 @@ int launch_acceptance(const Tin* tl, const Tin* dl, const int32_t* vlen, float t
                    static_cast<const ResampleDesc*>(jobs), sums);
   }
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
-  if (launch_pdl(k_rate_finish, (n_jobs + 255) / 256, 256, 0, stream, n_jobs, n_seg,
+  if (launch_pdl(k_rate_finish, (n_jobs + kFinishWarps - 1) / kFinishWarps, kFinishWarps * 32, 0,
+                 stream, n_jobs, n_seg,
                  static_cast<const ResampleDesc*>(jobs), static_cast<const ff*>(sums),
                  rates) != cudaSuccess)
     return DSPARK_ERR_CUDA;
