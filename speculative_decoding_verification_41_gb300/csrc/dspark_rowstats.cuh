@@ -120,7 +120,25 @@ __device__ __forceinline__ void unit_finish(const LaneAcc& a, TileStat* out, int
 }
 
 // Streaming pass through the TMA engine. Row byte length and both buffers
-// must be 16-byte aligned. Shared memory: W warps x STAGES x 4 KB + barriers.
+// must be 16-byte aligned. Shared memory: W warps x STAGES x (4 KB + barrier +
+// 16-byte chunk record).
+//
+// Work assignment: warp gw takes units gw, gw + GW, ... for the first n_static
+// rounds (all but about 1/kDynamicDiv of the units), then claims the remaining
+// units one at a time from a counter (reset by k_plan). A CTA that starts late
+// -- its SM still held by another kernel, e.g. a scheduler running on another
+// stream -- then takes fewer of the last units instead of finishing late. The
+// producer (lane 0) records which unit and bytes each stage holds, so the
+// consumer follows whatever the claims gave.
+constexpr int kDynamicDiv = 8;
+
+struct __align__(16) ChunkRec {  // what a ring stage holds; written by lane 0
+  long long u;    // unit (row-list row * n_units + part)
+  int32_t bytes;  // bytes of the chunk
+  int32_t last;   // the unit's last chunk
+};
+static_assert(sizeof(ChunkRec) == 16, "ChunkRec layout");
+
 template <typename Tin, int W, int STAGES>
 __global__ void __launch_bounds__(W * 32, 1)
     k_rowstats_tma(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int V, int n_units,
@@ -134,6 +152,9 @@ __global__ void __launch_bounds__(W * 32, 1)
   uint64_t* bars =
       reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(W) * STAGES * kChunkBytes) +
       warp * STAGES;
+  ChunkRec* recs =
+      reinterpret_cast<ChunkRec*>(smem + static_cast<size_t>(W) * STAGES * (kChunkBytes + 8)) +
+      warp * STAGES;
   if (lane == 0) {
     for (int s = 0; s < STAGES; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
@@ -144,73 +165,101 @@ __global__ void __launch_bounds__(W * 32, 1)
   const long long gw = static_cast<long long>(blockIdx.x) * W + warp;
   const long long GW = static_cast<long long>(gridDim.x) * W;
   const long long row_bytes = static_cast<long long>(V) * sizeof(Tin);
+  const long long n_static = (U - U / kDynamicDiv) / GW;  // rounds taken statically
+  const long long dyn0 = n_static * GW;                    // first unit of the claims
 
-  auto unit_bytes = [&](long long u) -> int {
-    const long long part = u % n_units;
-    const long long left = row_bytes - part * kUnitBytes;
-    return static_cast<int>(left < kUnitBytes ? left : kUnitBytes);
+  // producer cursor (lane 0): the unit being copied and its next chunk
+  long long k_st = 0;
+  auto next_unit = [&]() -> long long {
+    if (k_st < n_static) return gw + (k_st++) * GW;
+    return dyn0 + static_cast<long long>(atomicAdd(&ws.hdr->next_unit, 1ull));
   };
-
-  // producer cursor (lane 0): next chunk to copy
-  long long pu = gw;
-  int pc = 0;
+  long long pu = 0;
+  int pc = 0, pub = 0;
+  bool have = false;
   const char* pbase = nullptr;
-  auto issue_next = [&](int s) {  // lane 0 only; pu < U
-    const int ub = unit_bytes(pu);
+  auto issue_next = [&](int s) {  // lane 0 only; have
     if (pc == 0) {
       const long long row = pu / n_units;
+      const long long part = pu - row * n_units;
       const long long e = ws.row_list[row];
       pbase = reinterpret_cast<const char*>((e & 1) ? dl : tl) + (e >> 1) * row_bytes +
-              (pu - row * n_units) * static_cast<long long>(kUnitBytes);
+              part * static_cast<long long>(kUnitBytes);
+      const long long left = row_bytes - part * kUnitBytes;
+      pub = static_cast<int>(left < kUnitBytes ? left : kUnitBytes);
     }
-    const int left = ub - pc * kChunkBytes;
+    const int left = pub - pc * kChunkBytes;
     const uint32_t bytes = static_cast<uint32_t>(left < kChunkBytes ? left : kChunkBytes);
+    ChunkRec rc;
+    rc.u = pu;
+    rc.bytes = static_cast<int>(bytes);
+    rc.last = left <= kChunkBytes;
+    recs[s] = rc;
     mbar_arrive_expect_tx(&bars[s], bytes);
     bulk_g2s(buf + s * kChunkBytes, pbase + static_cast<long long>(pc) * kChunkBytes, bytes,
              &bars[s]);
-    if ((++pc) * kChunkBytes >= ub) {
+    if (rc.last) {
       pc = 0;
-      pu += GW;
+      pu = next_unit();
+      have = pu < U;
+    } else {
+      ++pc;
     }
   };
-  if (lane == 0)
-    for (int s = 0; s < STAGES && pu < U; ++s) issue_next(s);
+  int inflight = 0;
+  if (lane == 0) {
+    pu = next_unit();
+    have = pu < U;
+    while (inflight < STAGES && have) issue_next(inflight++);
+  }
+  inflight = __shfl_sync(0xFFFFFFFFu, inflight, 0);
 
   int stage = 0;
   uint32_t phase = 0;
   uint4 neg_inf;
   neg_inf.x = neg_inf.y = neg_inf.z = neg_inf.w = (sizeof(Tin) == 2) ? 0xFF80FF80u : 0xFF800000u;
-  for (long long u = gw; u < U; u += GW) {
-    const int ub = unit_bytes(u);
-    const int nc = (ub + kChunkBytes - 1) / kChunkBytes;
-    LaneAcc acc;
-    for (int c = 0; c < nc; ++c) {
-      // every lane waits (each gets the barrier's acquire); the give-up decision is warp-uniform
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[stage], phase))) {
-        if (lane == 0) set_status(status, DSPARK_ERR_TIMEOUT);
-        for (int s = 0; s < STAGES; ++s) (void)mbar_wait(&bars[s], phase ^ (s < stage ? 1u : 0u));
-        return;
+  LaneAcc acc;
+  while (inflight > 0) {
+    // every lane waits (each gets the barrier's acquire); the give-up decision is warp-uniform
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bars[stage], phase))) {
+      if (lane == 0) set_status(status, DSPARK_ERR_TIMEOUT);
+      for (int q = 0; q < inflight; ++q) {  // let the copies in flight land before leaving
+        int s2 = stage + q;
+        uint32_t p2 = phase;
+        if (s2 >= STAGES) {
+          s2 -= STAGES;
+          p2 ^= 1u;
+        }
+        (void)mbar_wait(&bars[s2], p2);
       }
-      const int bytes = min(kChunkBytes, ub - c * kChunkBytes);
-      uint4 v[VPL];
-      const uint4* sp = reinterpret_cast<const uint4*>(buf + stage * kChunkBytes);
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const int idx = j * 32 + lane;
-        v[j] = (idx * 16 < bytes) ? sp[idx] : neg_inf;
-      }
-      __syncwarp();
-      if (lane == 0 && pu < U) {
-        fence_proxy_async();
-        issue_next(stage);
-      }
-      if (++stage == STAGES) {
-        stage = 0;
-        phase ^= 1u;
-      }
-      chunk_accumulate<Tin, VPL>(v, acc, ep);
+      return;
     }
-    unit_finish(acc, ws.tiles + u, lane, status);
+    const ChunkRec rc = recs[stage];
+    uint4 v[VPL];
+    const uint4* sp = reinterpret_cast<const uint4*>(buf + stage * kChunkBytes);
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int idx = j * 32 + lane;
+      v[j] = (idx * 16 < rc.bytes) ? sp[idx] : neg_inf;
+    }
+    __syncwarp();
+    const int freed = stage;
+    if (++stage == STAGES) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    --inflight;
+    if (lane == 0 && have) {  // the ring was full: the freed stage is the next one to fill
+      fence_proxy_async();
+      issue_next(freed);
+      ++inflight;
+    }
+    inflight = __shfl_sync(0xFFFFFFFFu, inflight, 0);
+    chunk_accumulate<Tin, VPL>(v, acc, ep);
+    if (rc.last) {
+      unit_finish(acc, ws.tiles + rc.u, lane, status);
+      acc = LaneAcc();
+    }
   }
 }
 

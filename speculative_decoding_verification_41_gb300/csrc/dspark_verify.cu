@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verif
   if (tid == 0) {
     *status = DSPARK_OK;
     *ties = 0;
+    ws.hdr->next_unit = 0ull;
     carry = 0;
   }
   __syncthreads();
@@ -1258,8 +1259,8 @@ std::mutex g_mutex;
 DeviceState g_devices[128];
 
 constexpr size_t tma_smem_bytes() {
-  return static_cast<size_t>(kStreamWarps) * kStages * kChunkBytes +
-         static_cast<size_t>(kStreamWarps) * kStages * sizeof(uint64_t);
+  return static_cast<size_t>(kStreamWarps) * kStages *
+         (kChunkBytes + sizeof(uint64_t) + sizeof(ChunkRec));
 }
 // k_resid: 16 warps per SM, each with a ring of 3 stages of 2 KB per row (32
 // warps with 1 KB parts measured slower: the per-stage work halves, its

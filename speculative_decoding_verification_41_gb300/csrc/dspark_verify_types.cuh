@@ -25,9 +25,11 @@ struct ResampleDesc;  // the draw after a block (dspark_verify.cu)
 
 struct WsHeader {
   int32_t total_rows;
-  uint32_t ties_scratch;  // near-tie counter used when the caller passes none
-  int32_t pad[62];
+  uint32_t ties_scratch;         // near-tie counter used when the caller passes none
+  unsigned long long next_unit;  // claim counter of the streaming pass's last units
+  int32_t pad[60];
 };
+static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
 
 struct VerifyWs {
   WsHeader* hdr;
