@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verif
     *status = DSPARK_OK;
     *ties = 0;
     ws.hdr->next_unit = 0ull;
+    ws.hdr->next_item = 0ull;
     carry = 0;
   }
   __syncthreads();
@@ -910,13 +911,14 @@ __global__ void __launch_bounds__(kDecideWarps * 32) k_desc(
 // Persistent, W warps per CTA and one CTA per SM, like the streaming pass:
 // warp w takes items w, w + GW, ... (item = s * n_jobs + j for segment s of
 // job j: a warp's items fall in different segments, so that the segments rich
-// in heavy tokens do not all land on the same warps) through its own ring of
-// stages, each holding kRowPart bytes of the target row and kRowPart bytes of
-// the draft row (only the target row for a bonus draw), fed by bulk copies;
-// the ring runs on across items. The descriptors of a warp's next 32 items are
-// loaded together, one per lane, so that setting up an item costs shuffles,
-// not a dependent load. k_pick then draws each request's token from the
-// segment sums.
+// in heavy tokens do not all land on the same warps) for all but the last
+// 1/kDynamicDiv of them, which warps claim one at a time from a counter;
+// items go through the warp's own ring of stages, each holding kRowPart bytes
+// of the target row and kRowPart bytes of the draft row (only the target row
+// for a bonus draw), fed by bulk copies; the ring runs on across items. The
+// descriptors of a warp's next 32 fixed items are loaded together, one per
+// lane, so that setting up an item costs shuffles, not a dependent load.
+// k_pick then draws each request's token from the segment sums.
 struct __align__(16) StageInfo {  // what a ring stage holds; written by lane 0
   float nK, E_hi, E_lo, D_hi, D_lo;
   int32_t mode;    // kModeResidual, kModeTarget or kModeMin
@@ -939,7 +941,7 @@ template <typename Tin, int W, int STAGES, int kRowPart>
 __global__ void __launch_bounds__(W * 32, 1)
     k_resid(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int n_jobs, int V, int n_seg,
             ExpParams ep, const ResampleDesc* __restrict__ jobs, ff* __restrict__ sums,
-            int32_t* status) {
+            unsigned long long* claim, int32_t* status) {
   constexpr int RPL = kRowPart / 16 / 32;  // 16-byte vectors per lane and row part
   constexpr int kSegBytes = kSeg * static_cast<int>(sizeof(Tin));
   constexpr int kStage = 2 * kRowPart;  // target part, then draft part
@@ -965,32 +967,38 @@ __global__ void __launch_bounds__(W * 32, 1)
   const long long N = static_cast<long long>(n_jobs) * n_seg;
   const long long GW = static_cast<long long>(gridDim.x) * W;
   const long long g0 = static_cast<long long>(blockIdx.x) * W + warp;
-  const int n_items = g0 < N ? static_cast<int>((N - 1 - g0) / GW + 1) : 0;
+  // items in fixed rounds for all but about 1/kDynamicDiv of them (warp g0:
+  // items g0 + k GW, k < n_fixed), then claimed one at a time from *claim, so
+  // that warps of CTAs that start late or run slow take fewer of the last ones
+  const long long n_static = (N - N / kDynamicDiv) / GW;
+  const int n_fixed = static_cast<int>(n_static);
+  const long long dyn0 = n_static * GW;
 
+  auto describe = [&](long long i, ItemRegs& o) {  // the descriptor of item i
+    o.mode = kModeNone;
+    const int sg = static_cast<int>(i / n_jobs);
+    const int j = static_cast<int>(i - static_cast<long long>(sg) * n_jobs);
+    const ResampleDesc d = jobs[j];  // written by the previous kernel
+    if (d.mode == kModeResidual || d.mode == kModeTarget || d.mode == kModeMin) {
+      const long long off = static_cast<long long>(sg) * kSegBytes;
+      const long long left = row_bytes - off;
+      o.bytes = static_cast<int>(left < kSegBytes ? left : kSegBytes);
+      o.p_t = reinterpret_cast<const char*>(tl) + d.t_row * row_bytes + off;
+      o.p_d = reinterpret_cast<const char*>(dl) + d.d_row * row_bytes + off;
+      o.nK = -static_cast<float>(d.K_t);
+      o.E_hi = d.E_hi;
+      o.E_lo = d.E_lo;
+      o.D_hi = d.D_hi;
+      o.D_lo = d.D_lo;
+      o.out = j * n_seg + sg;
+      o.mode = d.mode;
+    }
+  };
   ItemRegs mine{};
-  auto load_batch = [&](int base) {  // lane l: the descriptor of item base + l
+  auto load_batch = [&](int base) {  // lane l: the descriptor of fixed item base + l
     mine.mode = kModeNone;
     const int k = base + lane;
-    if (k < n_items) {
-      const long long i = g0 + static_cast<long long>(k) * GW;
-      const int sg = static_cast<int>(i / n_jobs);
-      const int j = static_cast<int>(i - static_cast<long long>(sg) * n_jobs);
-      const ResampleDesc d = jobs[j];  // written by the previous kernel
-      if (d.mode == kModeResidual || d.mode == kModeTarget || d.mode == kModeMin) {
-        const long long off = static_cast<long long>(sg) * kSegBytes;
-        const long long left = row_bytes - off;
-        mine.bytes = static_cast<int>(left < kSegBytes ? left : kSegBytes);
-        mine.p_t = reinterpret_cast<const char*>(tl) + d.t_row * row_bytes + off;
-        mine.p_d = reinterpret_cast<const char*>(dl) + d.d_row * row_bytes + off;
-        mine.nK = -static_cast<float>(d.K_t);
-        mine.E_hi = d.E_hi;
-        mine.E_lo = d.E_lo;
-        mine.D_hi = d.D_hi;
-        mine.D_lo = d.D_lo;
-        mine.out = j * n_seg + sg;
-        mine.mode = d.mode;
-      }
-    }
+    if (k < n_fixed) describe(g0 + static_cast<long long>(k) * GW, mine);
   };
 
   // producer (warp-uniform state; lane 0 issues): item kp, its next stage pc
@@ -999,7 +1007,7 @@ __global__ void __launch_bounds__(W * 32, 1)
   bool have = false;
   auto next_item = [&]() {  // sets up the next item with something to sum, if any
     have = false;
-    for (; kp < n_items; ++kp) {
+    for (; kp < n_fixed; ++kp) {
       if ((kp >> 5) != batch) {
         batch = kp >> 5;
         load_batch(batch << 5);
@@ -1019,6 +1027,18 @@ __global__ void __launch_bounds__(W * 32, 1)
       cur.D_lo = __shfl_sync(kFull, mine.D_lo, l);
       cur.bytes = __shfl_sync(kFull, mine.bytes, l);
       cur.out = __shfl_sync(kFull, mine.out, l);
+      pc = 0;
+      have = true;
+      return;
+    }
+    for (;;) {  // the claimed items
+      unsigned long long c = 0;
+      if (lane == 0) c = atomicAdd(claim, 1ull);
+      c = __shfl_sync(kFull, c, 0);
+      const long long i = dyn0 + static_cast<long long>(c);
+      if (i >= N) return;
+      describe(i, cur);  // every lane the same item
+      if (cur.mode == kModeNone) continue;
       pc = 0;
       have = true;
       return;
@@ -1396,7 +1416,8 @@ int launch_verify(const Tin* tl, const Tin* dl, const int32_t* tokens, const int
     const int grid = static_cast<int>(want < sms ? want : sms);
     if (launch_pdl(k_resid<Tin, kResidWarps, kResidStages, kResidPart>, grid, kResidWarps * 32,
                    resid_smem_bytes(), stream, tl, dl, B, V, n_seg, ep,
-                   static_cast<const ResampleDesc*>(ws.desc), ws.seg_sum, status) != cudaSuccess)
+                   static_cast<const ResampleDesc*>(ws.desc), ws.seg_sum, &ws.hdr->next_item,
+                   status) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     if (launch_pdl(k_pick<Tin>, B, kDecideWarps * 32, 0, stream, tl, dl, gamma, V, n_seg, ep, ws,
                    emitted, tie_ctr, status) != cudaSuccess)
@@ -1595,7 +1616,7 @@ int launch_acceptance(const Tin* tl, const Tin* dl, const int32_t* vlen, float t
     e = launch_pdl(k_resid<Tin, kResidWarps, kResidStages, kResidPart>,
                    static_cast<int>(want < sms ? want : sms), kResidWarps * 32, resid_smem_bytes(),
                    stream, tl, dl, n_jobs, V, n_seg, ep, static_cast<const ResampleDesc*>(jobs),
-                   sums, status);
+                   sums, &ws.hdr->next_item, status);
   } else {
     const long long want = (items + 7) / 8;
     e = launch_pdl(k_rate_sum_plain<Tin>, static_cast<int>(want < 4LL * sms ? want : 4LL * sms),
