@@ -376,6 +376,22 @@ def native_arm(args):
         if i > 0:
             acc_ms.append(a0.elapsed_time(a1))
     del acc_ws
+    # the verification and the rates in one call (one statistics pass for both)
+    rbuf = binding.VerifyBuffers(vi.B, vi.gamma, vi.V, dev, with_rates=True)
+    vr_ms = []
+    for i in range(6):
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        binding.dspark_verify(vi.target_logits, vi.draft_logits, vi.draft_tokens,
+                              sbuf.verify_len, vi.uniforms, vi.temperature, buffers=rbuf,
+                              with_rates=True)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i > 0:
+            vr_ms.append(a0.elapsed_time(a1))
+    if not torch.equal(rbuf.rates, acc_rates):
+        raise SystemExit("dspark_verify_rates and dspark_acceptance disagree")
+    del rbuf
 
     drafter = None if args.no_drafter else drafter_measure(args, dev, stream, rank, ws)
 
@@ -485,7 +501,8 @@ def native_arm(args):
                       "schedule_median": statistics.median(sched_ms),
                       "serial_step_median": serial_step_ms,
                       "passes_median": pass_ms,
-                      "acceptance_median": statistics.median(acc_ms)},
+                      "acceptance_median": statistics.median(acc_ms),
+                      "verify_rates_median": statistics.median(vr_ms)},
         "gpu_launches": args.steps * 7,  # per step: k_sched_rank, k_sched_sweep, k_plan, k_rowstats_tma, k_desc, k_resid, k_pick
         "near_ties": int(vbuf.near_tie_count.item()),
         "clocks": clk,

@@ -289,13 +289,37 @@ int dspark_schedule_threshold(const float* confidences, float threshold, int32_t
  *                 256-byte aligned; no initial contents needed.
  * It reads every verified row pair twice (the statistics pass, then the
  * minima), so it costs about two streaming passes; dspark_verify does not
- * compute it.
+ * compute it, dspark_verify_rates computes both with one statistics pass.
  */
 int dspark_acceptance(const void* target_logits, const void* draft_logits,
                       const int32_t* verify_len, float temperature, int32_t dtype, int32_t B,
                       int32_t gamma, int32_t V, const int64_t* target_row_off,
                       const int64_t* draft_row_off, float* rates, int32_t* device_status,
                       void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * dspark_verify_rates -- dspark_verify and dspark_acceptance on the same
+ * inputs in one call: the verification (section 2.1) and then the acceptance
+ * probability of every verified position (equation 8) from the same row
+ * statistics, so the rows are streamed for statistics once, not twice (the
+ * label of section 3.2.1 for the verified positions of a serving step).
+ *
+ * Arguments are those of dspark_verify, plus
+ *   rates         out [B][gamma] float32, as in dspark_acceptance (required
+ *                 when B > 0, else DSPARK_ERR_INVALID_ARG).
+ *   workspace     at least DSPARK_ACCEPTANCE_WS_BYTES(B, gamma, V) bytes
+ *                 (else DSPARK_ERR_WORKSPACE), 256-byte aligned.
+ * The verification outputs equal dspark_verify's and the rates equal
+ * dspark_acceptance's, bit for bit. Errors as in dspark_verify.
+ */
+int dspark_verify_rates(const void* target_logits, const void* draft_logits,
+                        const int32_t* draft_tokens, const int32_t* verify_len,
+                        const float* uniforms, float temperature, int32_t dtype, int32_t B,
+                        int32_t gamma, int32_t V, const int64_t* target_row_off,
+                        const int64_t* draft_row_off, int32_t* accepted_len,
+                        int32_t* emitted_tokens, float* probs_out, uint32_t* near_tie_count,
+                        float* rates, int32_t* device_status, void* workspace,
+                        size_t workspace_bytes, struct CUstream_st* stream);
 
 /* Size of the library-owned scratch array behind dspark_verify_static. */
 #define DSPARK_STATIC_WS_BYTES ((size_t)16u << 20)

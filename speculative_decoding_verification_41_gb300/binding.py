@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_CUDA
 DSPARK_F32, DSPARK_BF16 = 0, 1
 EXPORTED = ("dspark_verify", "dspark_acceptance", "dspark_schedule", "dspark_schedule_capacity",
             "dspark_schedule_topk", "dspark_schedule_threshold", "dspark_verify_static",
-            "dspark_verify_timed", "dspark_draft_markov", "dspark_draft_markov_timed")
+            "dspark_verify_timed", "dspark_verify_rates", "dspark_draft_markov",
+            "dspark_draft_markov_timed")
 
 
 class DsparkError(RuntimeError):
@@ -110,6 +111,9 @@ def load(path: Optional[str] = None):
         lib.dspark_verify_timed.restype = ctypes.c_int
         lib.dspark_verify_timed.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp, vp,
                                             vp, vp, vp, vp, vp, sz, vp, vp]
+        lib.dspark_verify_rates.restype = ctypes.c_int
+        lib.dspark_verify_rates.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp,
+                                            vp, vp, vp, vp, vp, vp, vp, sz, vp]
         lib.dspark_verify_static.restype = ctypes.c_int
         lib.dspark_verify_static.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp,
                                              vp, vp, vp, vp, vp, vp]
@@ -155,9 +159,11 @@ def _require_cuda(name: str, t: torch.Tensor, dtype=None, device=None):
 
 class VerifyBuffers:
     """Outputs and workspace of dspark_verify for a fixed (B, gamma, V), so that
-    repeated calls (and CUDA-graph capture) allocate nothing."""
+    repeated calls (and CUDA-graph capture) allocate nothing. with_rates=True
+    adds the rates output and the larger workspace of dspark_verify_rates."""
 
-    def __init__(self, B: int, gamma: int, V: int, device, with_probs: bool = True):
+    def __init__(self, B: int, gamma: int, V: int, device, with_probs: bool = True,
+                 with_rates: bool = False):
         self.B, self.gamma, self.V = B, gamma, V
         dev = torch.device(device)
         self.accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
@@ -165,7 +171,9 @@ class VerifyBuffers:
         self.probs = torch.empty(B, gamma, 2, dtype=torch.float32, device=dev) if with_probs else None
         self.near_tie_count = torch.zeros(1, dtype=torch.int32, device=dev)
         self.device_status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.workspace = torch.empty(verify_workspace_bytes(B, gamma, V), dtype=torch.uint8, device=dev)
+        self.rates = torch.empty(B, gamma, dtype=torch.float32, device=dev) if with_rates else None
+        ws = acceptance_workspace_bytes(B, gamma, V) if with_rates else verify_workspace_bytes(B, gamma, V)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
         assert self.workspace.data_ptr() % 256 == 0
 
 
@@ -174,7 +182,7 @@ def dspark_verify(target_logits: torch.Tensor, draft_logits: torch.Tensor,
                   temperature: float, target_row_off: Optional[torch.Tensor] = None,
                   draft_row_off: Optional[torch.Tensor] = None, *, with_probs: bool = True,
                   buffers: Optional[VerifyBuffers] = None, stream=None, check: bool = False,
-                  events=None) -> dict:
+                  events=None, with_rates: bool = False) -> dict:
     """Batched speculative verification through libdspark (see include/dspark.h).
 
     Returns a dict of device tensors: accepted_len [B] int32, emitted_tokens
@@ -182,7 +190,10 @@ def dspark_verify(target_logits: torch.Tensor, draft_logits: torch.Tensor,
     [1], device_status [1]. With check=True the call synchronises and raises on
     a non-OK device status. With events (four torch.cuda.Event made with
     enable_timing=True) the call goes through dspark_verify_timed, which records
-    them around the planning, streaming and decision passes."""
+    them around the planning, streaming and decision passes. With
+    with_rates=True it goes through dspark_verify_rates and the dict also holds
+    rates [B, gamma] float32, the acceptance probability of every verified
+    position (-1 beyond l_r), from the same row statistics."""
     dev = target_logits.device
     if target_logits.dtype == torch.bfloat16:
         dtype = DSPARK_BF16
@@ -206,9 +217,13 @@ def dspark_verify(target_logits: torch.Tensor, draft_logits: torch.Tensor,
         raise ValueError("target and draft vocabularies differ")
     if uniforms.shape != (B, gamma + 1) or verify_len.shape != (B,):
         raise ValueError("uniforms must be [B, gamma+1] and verify_len [B]")
-    buf = buffers or VerifyBuffers(B, gamma, V, dev, with_probs)
+    if with_rates and events is not None:
+        raise ValueError("with_rates and events are separate entry points")
+    buf = buffers or VerifyBuffers(B, gamma, V, dev, with_probs, with_rates)
     if (buf.B, buf.gamma, buf.V) != (B, gamma, V):
         raise ValueError("buffers were made for another shape")
+    if with_rates and buf.rates is None:
+        raise ValueError("buffers were made without rates (VerifyBuffers(..., with_rates=True))")
     lib = load()
     args = (_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(verify_len),
             _ptr(uniforms), float(temperature), dtype, B, gamma, V, _ptr(target_row_off),
@@ -217,7 +232,10 @@ def dspark_verify(target_logits: torch.Tensor, draft_logits: torch.Tensor,
             _ptr(buf.device_status), _ptr(buf.workspace), buf.workspace.numel())
     with torch.cuda.device(dev):
         s = _stream_handle(stream)
-        if events is None:
+        if with_rates:
+            rargs = args[:16] + (_ptr(buf.rates),) + args[16:]
+            rc = lib.dspark_verify_rates(*rargs, s)
+        elif events is None:
             rc = lib.dspark_verify(*args, s)
         else:
             if len(events) != 4:
@@ -228,10 +246,14 @@ def dspark_verify(target_logits: torch.Tensor, draft_logits: torch.Tensor,
             handles = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
             rc = lib.dspark_verify_timed(*args, s, handles)
     if rc != 0:
-        raise DsparkError("dspark_verify_timed" if events is not None else "dspark_verify", rc)
+        name = ("dspark_verify_rates" if with_rates else
+                "dspark_verify_timed" if events is not None else "dspark_verify")
+        raise DsparkError(name, rc)
     out = {"accepted_len": buf.accepted_len, "emitted_tokens": buf.emitted_tokens,
            "probs": buf.probs if with_probs else None, "near_tie_count": buf.near_tie_count,
            "device_status": buf.device_status}
+    if with_rates:
+        out["rates"] = buf.rates
     if check:
         torch.cuda.synchronize(dev)
         st = int(buf.device_status.item())

@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verif
     *ties = 0;
     ws.hdr->next_unit = 0ull;
     ws.hdr->next_item = 0ull;
+    ws.hdr->next_rate = 0ull;
     carry = 0;
   }
   __syncthreads();
@@ -1571,10 +1572,14 @@ extern "C" int dspark_verify_static(const void* target_logits, const void* draft
 // ---------------------------------------------------------------------------
 namespace dspark {
 
+// The acceptance probabilities of every verified position from the row
+// statistics already in the workspace (k_plan and the streaming pass ran):
+// k_rate_desc, the minima's segment sums, k_rate_finish. The jobs and their
+// sums follow the verification workspace (DSPARK_ACCEPTANCE_WS_BYTES).
 template <typename Tin>
-int launch_acceptance(const Tin* tl, const Tin* dl, const int32_t* vlen, float temperature,
-                      int B, int gamma, int V, const int64_t* toff, const int64_t* doff,
-                      float* rates, int32_t* status, void* workspace, cudaStream_t stream) {
+int launch_rates(const Tin* tl, const Tin* dl, int B, int gamma, int V, float temperature,
+                 float* rates, int32_t* status, void* workspace, cudaStream_t stream,
+                 bool aligned) {
   int sms = 0, decide_per_sm = 1;
   if (int rc = device_setup(sms, decide_per_sm)) return rc;
   VerifyWs ws = carve_verify_ws(workspace, B, gamma, V);
@@ -1587,6 +1592,42 @@ int launch_acceptance(const Tin* tl, const Tin* dl, const int32_t* vlen, float t
   const int n_units = (V + unit_elems - 1) / unit_elems;
   const int n_seg = (V + kSeg - 1) / kSeg;
   const int n_jobs = B * gamma;
+  if (launch_pdl(k_rate_desc, B, kDecideWarps * 32, 0, stream, gamma, n_units, ws, jobs,
+                 status) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  const long long items = static_cast<long long>(n_jobs) * n_seg;
+  cudaError_t e;
+  if (aligned) {
+    const long long want = (items + kResidWarps - 1) / kResidWarps;
+    e = launch_pdl(k_resid<Tin, kResidWarps, kResidStages, kResidPart>,
+                   static_cast<int>(want < sms ? want : sms), kResidWarps * 32, resid_smem_bytes(),
+                   stream, tl, dl, n_jobs, V, n_seg, ep, static_cast<const ResampleDesc*>(jobs),
+                   sums, &ws.hdr->next_rate, status);
+  } else {
+    const long long want = (items + 7) / 8;
+    e = launch_pdl(k_rate_sum_plain<Tin>, static_cast<int>(want < 4LL * sms ? want : 4LL * sms),
+                   256, 0, stream, tl, dl, n_jobs, V, n_seg, ep,
+                   static_cast<const ResampleDesc*>(jobs), sums);
+  }
+  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (launch_pdl(k_rate_finish, (n_jobs + kFinishWarps - 1) / kFinishWarps, kFinishWarps * 32, 0,
+                 stream, n_jobs, n_seg, static_cast<const ResampleDesc*>(jobs),
+                 static_cast<const ff*>(sums), rates) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
+  return DSPARK_OK;
+}
+
+template <typename Tin>
+int launch_acceptance(const Tin* tl, const Tin* dl, const int32_t* vlen, float temperature,
+                      int B, int gamma, int V, const int64_t* toff, const int64_t* doff,
+                      float* rates, int32_t* status, void* workspace, cudaStream_t stream) {
+  int sms = 0, decide_per_sm = 1;
+  if (int rc = device_setup(sms, decide_per_sm)) return rc;
+  VerifyWs ws = carve_verify_ws(workspace, B, gamma, V);
+  const ExpParams ep = exp_params(temperature);
+  const int unit_elems = kUnitBytes / static_cast<int>(sizeof(Tin));
+  const int n_units = (V + unit_elems - 1) / unit_elems;
   if (launch_pdl(k_plan, 1, 1024, 0, stream, vlen, toff, doff, B, gamma, ws,
                  &ws.hdr->ties_scratch, status) != cudaSuccess)
     return DSPARK_ERR_CUDA;
@@ -1607,30 +1648,8 @@ int launch_acceptance(const Tin* tl, const Tin* dl, const int32_t* vlen, float t
                    256, 0, stream, tl, dl, V, n_units, ws, ep, status);
   }
   if (e != cudaSuccess) return DSPARK_ERR_CUDA;
-  if (launch_pdl(k_rate_desc, B, kDecideWarps * 32, 0, stream, gamma, n_units, ws, jobs,
-                 status) != cudaSuccess)
-    return DSPARK_ERR_CUDA;
-  const long long items = static_cast<long long>(n_jobs) * n_seg;
-  if (aligned) {
-    const long long want = (items + kResidWarps - 1) / kResidWarps;
-    e = launch_pdl(k_resid<Tin, kResidWarps, kResidStages, kResidPart>,
-                   static_cast<int>(want < sms ? want : sms), kResidWarps * 32, resid_smem_bytes(),
-                   stream, tl, dl, n_jobs, V, n_seg, ep, static_cast<const ResampleDesc*>(jobs),
-                   sums, &ws.hdr->next_item, status);
-  } else {
-    const long long want = (items + 7) / 8;
-    e = launch_pdl(k_rate_sum_plain<Tin>, static_cast<int>(want < 4LL * sms ? want : 4LL * sms),
-                   256, 0, stream, tl, dl, n_jobs, V, n_seg, ep,
-                   static_cast<const ResampleDesc*>(jobs), sums);
-  }
-  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
-  if (launch_pdl(k_rate_finish, (n_jobs + kFinishWarps - 1) / kFinishWarps, kFinishWarps * 32, 0,
-                 stream, n_jobs, n_seg,
-                 static_cast<const ResampleDesc*>(jobs), static_cast<const ff*>(sums),
-                 rates) != cudaSuccess)
-    return DSPARK_ERR_CUDA;
-  if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
-  return DSPARK_OK;
+  return launch_rates<Tin>(tl, dl, B, gamma, V, temperature, rates, status, workspace, stream,
+                           aligned);
 }
 
 }  // namespace dspark
@@ -1663,4 +1682,42 @@ extern "C" int dspark_acceptance(const void* target_logits, const void* draft_lo
                                   static_cast<const float*>(draft_logits), verify_len,
                                   temperature, B, gamma, V, target_row_off, draft_row_off, rates,
                                   device_status, workspace, s);
+}
+
+// ---------------------------------------------------------------------------
+// dspark_verify_rates: dspark_verify, then the acceptance probabilities of
+// every verified position from the same row statistics (one streaming pass
+// for both)
+// ---------------------------------------------------------------------------
+extern "C" int dspark_verify_rates(const void* target_logits, const void* draft_logits,
+                                   const int32_t* draft_tokens, const int32_t* verify_len,
+                                   const float* uniforms, float temperature, int32_t dtype,
+                                   int32_t B, int32_t gamma, int32_t V,
+                                   const int64_t* target_row_off, const int64_t* draft_row_off,
+                                   int32_t* accepted_len, int32_t* emitted_tokens,
+                                   float* probs_out, uint32_t* near_tie_count, float* rates,
+                                   int32_t* device_status, void* workspace,
+                                   size_t workspace_bytes, struct CUstream_st* stream) {
+  using namespace dspark;
+  if (B > 0 && !rates) return DSPARK_ERR_INVALID_ARG;
+  if (B >= 0 && B <= 65535 && gamma >= 1 && gamma <= DSPARK_MAX_GAMMA && V >= 1 &&
+      V <= (1 << 30) && workspace_bytes < DSPARK_ACCEPTANCE_WS_BYTES(B, gamma, V))
+    return DSPARK_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int rc = verify_entry(target_logits, draft_logits, draft_tokens, verify_len, uniforms,
+                              temperature, dtype, B, gamma, V, target_row_off, draft_row_off,
+                              accepted_len, emitted_tokens, probs_out, near_tie_count,
+                              device_status, workspace, workspace_bytes, s, nullptr);
+  if (rc != DSPARK_OK || B == 0) return rc;
+  const size_t esz = dtype == DSPARK_BF16 ? 2 : 4;
+  const bool aligned = (static_cast<size_t>(V) * esz) % 16 == 0 &&
+                       reinterpret_cast<uintptr_t>(target_logits) % 16 == 0 &&
+                       reinterpret_cast<uintptr_t>(draft_logits) % 16 == 0;
+  if (dtype == DSPARK_BF16)
+    return launch_rates<uint16_t>(static_cast<const uint16_t*>(target_logits),
+                                  static_cast<const uint16_t*>(draft_logits), B, gamma, V,
+                                  temperature, rates, device_status, workspace, s, aligned);
+  return launch_rates<float>(static_cast<const float*>(target_logits),
+                             static_cast<const float*>(draft_logits), B, gamma, V, temperature,
+                             rates, device_status, workspace, s, aligned);
 }

@@ -27,8 +27,9 @@ struct WsHeader {
   int32_t total_rows;
   uint32_t ties_scratch;         // near-tie counter used when the caller passes none
   unsigned long long next_unit;  // claim counter of the streaming pass's last units
-  unsigned long long next_item;  // claim counter of k_resid's last items
-  int32_t pad[58];
+  unsigned long long next_item;  // claim counter of k_resid's last items (the draws)
+  unsigned long long next_rate;  // claim counter of k_resid's last items (acceptance rates)
+  int32_t pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
 

@@ -166,6 +166,33 @@ def test_acceptance_rejects_bad_arguments_on_host(lib):
     assert call(wsb=100) == 3
 
 
+def test_verify_rates_rejects_bad_arguments_on_host(lib):
+    """dspark_verify_rates: dspark_verify's checks, a rates pointer, and the
+    larger workspace of dspark_acceptance (no device is needed)."""
+    p = ctypes.c_void_p
+    B, g, V = 4, 4, 32
+
+    def call(**kw):
+        a = dict(tl=256, dl=256, tok=256, vlen=256, uni=256, T=1.0, dtype=1, toff=None,
+                 doff=None, acc=256, em=256, pr=None, ties=None, rates=256, st=256, ws=256,
+                 wsb=1 << 30)
+        a.update(kw)
+        q = lambda x: None if x is None else p(x)
+        return lib.dspark_verify_rates(q(a["tl"]), q(a["dl"]), q(a["tok"]), q(a["vlen"]),
+                                       q(a["uni"]), a["T"], a["dtype"], B, g, V, q(a["toff"]),
+                                       q(a["doff"]), q(a["acc"]), q(a["em"]), q(a["pr"]),
+                                       q(a["ties"]), q(a["rates"]), q(a["st"]), q(a["ws"]),
+                                       a["wsb"], None)
+    assert call(rates=None) == 1
+    assert call(T=0.0) == 1
+    assert call(st=None) == 1
+    assert call(toff=64) == 1
+    assert call(ws=None) == 3
+    # enough for dspark_verify, not for the rates' jobs and sums
+    assert call(wsb=binding.verify_workspace_bytes(B, g, V)) == 3
+    assert binding.acceptance_workspace_bytes(B, g, V) > binding.verify_workspace_bytes(B, g, V)
+
+
 def _draft_call(lib, timed=False, events=None, **kw):
     a = dict(U=256, w1=256, w2t=256, x0=256, uni=256, T=1.0, B=4, g=4, V=1024, r=256, L=256,
              tok=256, st=256, ws=256, wsb=1 << 30)

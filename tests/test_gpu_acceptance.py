@@ -88,3 +88,39 @@ def test_named_workloads(dev, name, sample):
     vi = workloads.make_config(name, device=dev)
     idx = np.sort(np.random.default_rng(0).choice(vi.B, sample, replace=False))
     check(vi, idx)
+
+
+# ---------------------------------------------------------------------------
+# dspark_verify_rates: the verification and the rates from one statistics pass
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("B,g,V,dt,T,vl,ragged", SHAPES + [
+    (64, 16, 40000, torch.bfloat16, 0.7, "uniform", False),  # items claimed past the fixed rounds
+])
+def test_verify_rates_equal_the_separate_calls(dev, B, g, V, dt, T, vl, ragged):
+    """Outputs bit-identical to dspark_verify's, rates bit-identical to
+    dspark_acceptance's (the same kernels on the same statistics), and so
+    within the oracle's tolerance."""
+    vi = workloads.make_verify(B, g, V, dt, T, rho=(0.5, 0.95), verify_len=vl, ragged=ragged,
+                               seed=31 + B + g, device=dev)
+    args = (vi.target_logits, vi.draft_logits, vi.draft_tokens, vi.verify_len, vi.uniforms,
+            vi.temperature, vi.target_row_off, vi.draft_row_off)
+    plain = {k: v.clone() for k, v in binding.dspark_verify(*args, check=True).items()
+             if v is not None}
+    both = binding.dspark_verify(*args, check=True, with_rates=True)
+    for k in plain:
+        assert torch.equal(plain[k], both[k]), k
+    sep, _ = check(vi)  # dspark_acceptance against the oracle
+    assert np.array_equal(both["rates"].cpu().numpy(), np.asarray(sep))
+
+
+def test_verify_rates_repeated_with_buffers(dev):
+    """Reused buffers (and their counters) give the same rates call after call."""
+    vi = workloads.make_verify(24, 16, 30000, torch.bfloat16, 0.7, rho=(0.6, 0.95), seed=8,
+                               device=dev)
+    bufs = binding.VerifyBuffers(24, 16, 30000, dev, with_rates=True)
+    args = (vi.target_logits, vi.draft_logits, vi.draft_tokens, vi.verify_len, vi.uniforms,
+            vi.temperature)
+    a = binding.dspark_verify(*args, buffers=bufs, check=True, with_rates=True)["rates"].clone()
+    for _ in range(3):
+        b = binding.dspark_verify(*args, buffers=bufs, check=True, with_rates=True)["rates"]
+        assert torch.equal(a, b)

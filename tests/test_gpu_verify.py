@@ -164,6 +164,29 @@ def test_timed_entry_matches_plain_call(dev):
     assert all(t > 0 for t in passes), passes
 
 
+def test_busy_device_gives_the_same_outputs(dev):
+    """The streaming pass and the residual sums claim their last work units
+    from counters, so which CTA takes which unit depends on timing. With other
+    kernels holding SMs on a second stream (CTAs start late), the outputs stay
+    bit-identical to a call on an idle device."""
+    vi = workloads.make_verify(64, 16, 40000, torch.bfloat16, 0.7, rho=(0.6, 0.95), seed=6,
+                               device=dev)
+    bufs = binding.VerifyBuffers(64, 16, 40000, dev)
+    a = {k: v.clone() for k, v in run(vi, buffers=bufs).items() if v is not None}
+    side = torch.cuda.Stream(dev)
+    x = torch.randn(4096, 4096, device=dev, dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    for _ in range(4):
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                y = x @ x  # holds SMs while the verification starts
+        b = run(vi, buffers=bufs)
+        torch.cuda.synchronize()
+        for k in a:
+            assert torch.equal(a[k], b[k]), k
+    del y
+
+
 # ---------------------------------------------------------------------------
 # the named workloads at full size (bench launch configuration)
 # ---------------------------------------------------------------------------
