@@ -124,3 +124,19 @@ def test_verify_rates_repeated_with_buffers(dev):
     for _ in range(3):
         b = binding.dspark_verify(*args, buffers=bufs, check=True, with_rates=True)["rates"]
         assert torch.equal(a, b)
+
+
+def test_verify_rates_headline_size(dev):
+    """The headline workload (256 x 16 x 129,280 bf16) in the bench's launch
+    configuration: the combined call equals the two separate calls bit for bit."""
+    vi = workloads.make_config("b256_g16_v129280_bf16", device=dev)
+    args = (vi.target_logits, vi.draft_logits, vi.draft_tokens, vi.verify_len, vi.uniforms,
+            vi.temperature)
+    plain = {k: v.clone() for k, v in binding.dspark_verify(*args, check=True).items()
+             if v is not None}
+    rates = binding.dspark_acceptance(vi.target_logits, vi.draft_logits, vi.verify_len,
+                                      vi.temperature, vi.gamma, check=True)["rates"].clone()
+    both = binding.dspark_verify(*args, check=True, with_rates=True)
+    for k in plain:
+        assert torch.equal(plain[k], both[k]), k
+    assert torch.equal(rates, both["rates"])
