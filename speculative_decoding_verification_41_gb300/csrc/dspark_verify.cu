@@ -139,14 +139,15 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verif
     ws.hdr->total_rows = carry;
   }
   __syncthreads();
-  for (int r = tid; r < B; r += 1024) {
+  // the row list: one warp per request, lanes over its rows (coalesced stores)
+  for (int r = warp; r < B; r += 32) {
     const int start = ws.req_row_start[r], end = ws.req_row_start[r + 1];
     if (end == start) continue;  // invalid request: nothing to read
     const int ell = (end - start - 1) / 2;
     const long long tb = toff ? toff[r] : (long long)r * (gamma + 1);
     const long long db = doff ? doff[r] : (long long)r * gamma;
-    for (int i = 0; i <= ell; ++i) ws.row_list[start + i] = (tb + i) << 1;
-    for (int i = 0; i < ell; ++i) ws.row_list[start + ell + 1 + i] = ((db + i) << 1) | 1;
+    for (int i = lane; i < end - start; i += 32)
+      ws.row_list[start + i] = i <= ell ? (tb + i) << 1 : ((db + i - ell - 1) << 1) | 1;
   }
 }
 
