@@ -321,6 +321,25 @@ int dspark_verify_rates(const void* target_logits, const void* draft_logits,
                         float* rates, int32_t* device_status, void* workspace,
                         size_t workspace_bytes, struct CUstream_st* stream);
 
+/*
+ * dspark_wait_selftest -- a diagnostic of the bounded waits (no counterpart in
+ * the paper). Every wait in the library gives up after about a second of the
+ * device's global timer, writes DSPARK_ERR_TIMEOUT to the status word and lets
+ * its kernel return, so that a lost completion never hangs the GPU. This call
+ * runs one such wait on a condition that never comes true, in one CTA:
+ *   which 0  the ring waits of the pipelines: an mbarrier that no copy and no
+ *            thread completes;
+ *   which 1  the drafter's grid barrier: two CTAs expected in a grid of one;
+ *            sync_words = 8 bytes of caller device memory, zeroed before the
+ *            call (left holding one arrival).
+ * The kernel records DSPARK_ERR_TIMEOUT in *device_status (if it holds
+ * DSPARK_OK) after about a second and returns; later calls on the stream run
+ * normally. Host errors: which not 0 or 1, device_status NULL, or (which 1)
+ * sync_words NULL or not 8-byte aligned -> DSPARK_ERR_INVALID_ARG.
+ */
+int dspark_wait_selftest(int32_t which, void* sync_words, int32_t* device_status,
+                         struct CUstream_st* stream);
+
 /* Size of the library-owned scratch array behind dspark_verify_static. */
 #define DSPARK_STATIC_WS_BYTES ((size_t)16u << 20)
 

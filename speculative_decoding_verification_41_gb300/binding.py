@@ -24,11 +24,12 @@ LIB_PATH = os.path.join(PKG, "libdspark.so")
 STATUS_NAMES = {0: "DSPARK_OK", 1: "DSPARK_ERR_INVALID_ARG", 2: "DSPARK_ERR_CUDA",
                 3: "DSPARK_ERR_WORKSPACE", 4: "DSPARK_ERR_TIMEOUT", 5: "DSPARK_ERR_BAD_DATA",
                 6: "DSPARK_ERR_TOO_LARGE"}
+DSPARK_OK, DSPARK_ERR_TIMEOUT, DSPARK_ERR_BAD_DATA = 0, 4, 5
 DSPARK_F32, DSPARK_BF16 = 0, 1
 EXPORTED = ("dspark_verify", "dspark_acceptance", "dspark_schedule", "dspark_schedule_capacity",
             "dspark_schedule_topk", "dspark_schedule_threshold", "dspark_verify_static",
             "dspark_verify_timed", "dspark_verify_rates", "dspark_draft_markov",
-            "dspark_draft_markov_timed")
+            "dspark_draft_markov_timed", "dspark_wait_selftest")
 
 
 class DsparkError(RuntimeError):
@@ -114,6 +115,8 @@ def load(path: Optional[str] = None):
         lib.dspark_verify_rates.restype = ctypes.c_int
         lib.dspark_verify_rates.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp,
                                             vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.dspark_wait_selftest.restype = ctypes.c_int
+        lib.dspark_wait_selftest.argtypes = [i32, vp, vp, vp]
         lib.dspark_verify_static.restype = ctypes.c_int
         lib.dspark_verify_static.argtypes = [vp, vp, vp, vp, vp, f32, i32, i32, i32, i32, vp, vp,
                                              vp, vp, vp, vp, vp, vp]
@@ -488,3 +491,23 @@ def dspark_draft_markov(base_logits: torch.Tensor, w1: torch.Tensor, w2t: torch.
         if st != 0:
             raise DsparkError("dspark_draft_markov (device)", st)
     return {"draft_logits": out, "draft_tokens": tok, "device_status": status}
+
+
+def wait_selftest(which: int, device="cuda", stream=None) -> dict:
+    """Run dspark_wait_selftest (include/dspark.h): one bounded wait that never
+    completes. Returns the device status it left (DSPARK_ERR_TIMEOUT expected)
+    and the seconds the call took on the device."""
+    dev = torch.device(device)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sync = torch.zeros(2, dtype=torch.int32, device=dev)
+    lib = load()
+    with torch.cuda.device(dev):
+        st = stream if stream is not None else torch.cuda.current_stream(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        rc = lib.dspark_wait_selftest(int(which), _ptr(sync), _ptr(status), _stream_handle(st))
+        b.record(st)
+        if rc != 0:
+            raise DsparkError("dspark_wait_selftest", rc)
+        torch.cuda.synchronize(dev)
+    return {"status": int(status.item()), "seconds": a.elapsed_time(b) / 1e3}

@@ -14,10 +14,33 @@
 
 namespace dspark {
 
-// Spin limit of every bounded wait: far beyond any legitimate copy latency
-// (each try_wait may itself suspend for a while), small enough that a lost
-// completion ends the kernel instead of hanging the GPU.
-constexpr uint32_t kWaitLimit = 1u << 22;
+// Every bounded wait gives up after about a second of wall time (the
+// device's global timer): far beyond any legitimate copy or barrier latency,
+// short enough that a lost completion ends the kernel with DSPARK_ERR_TIMEOUT
+// instead of hanging the GPU. The clock is read once every 1,024 failed
+// tries, so a wait that succeeds soon never reads it.
+constexpr uint64_t kWaitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+struct WaitClock {
+  uint64_t t0 = 0;
+  uint32_t n = 0;
+  // call after each failed try; true once the wait has lasted kWaitNs
+  __device__ __forceinline__ bool expired() {
+    if ((++n & 1023u) != 0u) return false;
+    const uint64_t now = globaltimer_ns();
+    if (t0 == 0) {
+      t0 = now;
+      return false;
+    }
+    return now - t0 > kWaitNs;
+  }
+};
 
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, (int32_t)DSPARK_OK, code);
@@ -53,7 +76,8 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 // Bounded wait for the phase with the given parity to complete.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t addr = smem_addr(bar);
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+  WaitClock clock;
+  for (;;) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -63,8 +87,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
         : "r"(addr), "r"(parity)
         : "memory");
     if (done) return true;
+    if (clock.expired()) return false;
   }
-  return false;
 }
 
 // 1-D bulk copy global -> shared, completing `bytes` of transaction count on

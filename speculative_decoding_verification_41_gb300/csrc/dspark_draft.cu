@@ -551,7 +551,6 @@ __global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickA
 // buffers, so a CTA already writing position k+1's may not overwrite what a
 // slower one still reads). Launched cooperatively (every CTA resident, one per
 // SM), so no wait can be on a CTA that is not running; every spin is bounded.
-constexpr uint32_t kGridSpinLimit = 1u << 22;
 
 // One thread per CTA. sync[0] counts arrivals and is 0 between uses (zeroed
 // before the launch, reset by the last arrival); sync[1] is a generation that
@@ -564,15 +563,33 @@ __device__ bool grid_barrier(uint32_t* sync, uint32_t nctas, uint32_t& gen) {
     __threadfence();
     st_release_gpu(&sync[1], g + 1u);
   } else {
-    uint32_t i = 0;
+    WaitClock clock;
     while (ld_acquire_gpu(&sync[1]) == g) {
-      if (++i > kGridSpinLimit) return false;
+      if (clock.expired()) return false;
       __nanosleep(128);
     }
   }
   gen = g + 1u;
   __threadfence();
   return true;
+}
+
+// A diagnostic of the bounded waits: one thread runs a wait whose condition
+// never comes true -- which 0: wait_or_flag on an mbarrier that no copy or
+// thread completes (the waits of the pipelines' rings); which 1: grid_barrier
+// for two CTAs in a grid of one (the drafter's grid barrier) -- and the wait
+// gives up, writes DSPARK_ERR_TIMEOUT to *status and the kernel returns.
+__global__ void k_wait_selftest(int which, uint32_t* sync, int32_t* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  if (which == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    (void)wait_or_flag(&bar, 0, status);  // sets DSPARK_ERR_TIMEOUT when it gives up
+  } else {
+    uint32_t gen = ld_acquire_gpu(&sync[1]);
+    if (!grid_barrier(sync, 2u, gen)) set_status(status, DSPARK_ERR_TIMEOUT);
+  }
 }
 
 struct DraftBlockArgs {
@@ -771,10 +788,10 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
               x = 0;
             }
           } else {
-            uint32_t i = 0;
+            WaitClock clock;
             unsigned long long f;
             while (((f = ld_acquire_gpu64(&ba.ready[b])) >> 32) < static_cast<unsigned>(k)) {
-              if (++i > kGridSpinLimit) {
+              if (clock.expired()) {
                 r_ok = false;
                 break;
               }
@@ -1137,4 +1154,15 @@ extern "C" int dspark_draft_markov_timed(const void* base_logits, const void* w1
   return dspark::draft_entry(base_logits, w1, w2t, anchors, uniforms, temperature, B, gamma, V, r,
                              draft_logits, draft_tokens, device_status, workspace,
                              workspace_bytes, stream, events);
+}
+
+// A diagnostic (no counterpart in the paper): one bounded wait that runs out.
+extern "C" int dspark_wait_selftest(int32_t which, void* sync_words, int32_t* device_status,
+                                    struct CUstream_st* stream) {
+  if ((which != 0 && which != 1) || !device_status || (which == 1 && !sync_words) ||
+      (reinterpret_cast<uintptr_t>(sync_words) & 7u) != 0)
+    return DSPARK_ERR_INVALID_ARG;
+  dspark::k_wait_selftest<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      which, static_cast<uint32_t*>(sync_words), device_status);
+  return cudaGetLastError() == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
 }

@@ -193,6 +193,15 @@ def test_verify_rates_rejects_bad_arguments_on_host(lib):
     assert binding.acceptance_workspace_bytes(B, g, V) > binding.verify_workspace_bytes(B, g, V)
 
 
+def test_wait_selftest_rejects_bad_arguments_on_host(lib):
+    p = ctypes.c_void_p
+    assert lib.dspark_wait_selftest(2, p(256), p(256), None) == 1
+    assert lib.dspark_wait_selftest(-1, p(256), p(256), None) == 1
+    assert lib.dspark_wait_selftest(0, p(256), None, None) == 1
+    assert lib.dspark_wait_selftest(1, None, p(256), None) == 1
+    assert lib.dspark_wait_selftest(1, p(260), p(256), None) == 1  # sync words not 8-byte aligned
+
+
 def _draft_call(lib, timed=False, events=None, **kw):
     a = dict(U=256, w1=256, w2t=256, x0=256, uni=256, T=1.0, B=4, g=4, V=1024, r=256, L=256,
              tok=256, st=256, ws=256, wsb=1 << 30)
