@@ -402,42 +402,66 @@ def native_arm(args):
                 ("target_logits", "draft_logits", "draft_tokens", "uniforms")}
         host_conf = sched.confidences.cpu().pin_memory()
         host_prof = sched.step_time_ms.cpu().pin_memory()
-        dbuf = {k: torch.empty_like(getattr(vi, k)) for k in host}
-        dconf = torch.empty_like(sched.confidences)
-        dprof = torch.empty_like(sched.step_time_ms)
+        # two sets of device inputs: step i+1's inputs cross the host link on a
+        # copy stream while step i is verified (every step still copies its
+        # own inputs in and its results out inside the timed region)
+        dbufs = [{k: torch.empty_like(getattr(vi, k)) for k in host} for _ in range(2)]
+        dconfs = [torch.empty_like(sched.confidences) for _ in range(2)]
+        dprofs = [torch.empty_like(sched.step_time_ms) for _ in range(2)]
         out_acc = torch.empty(vi.B, dtype=torch.int32).pin_memory()
         out_em = torch.empty(vi.B, vi.gamma + 1, dtype=torch.int32).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
             host_conf.numel() * 4 + host_prof.numel() * 8
         d2h = out_acc.numel() * 4 + out_em.numel() * 4
+        copy_stream = torch.cuda.Stream(dev)
+        n_e2e = args.e2e_steps + 1  # one untimed step first
+        copied = [torch.cuda.Event() for _ in range(n_e2e)]
+        used = [torch.cuda.Event() for _ in range(n_e2e)]
 
-        def e2e_step():
-            for k, t in host.items():
-                dbuf[k].copy_(t, non_blocking=True)
-            dconf.copy_(host_conf, non_blocking=True)
-            dprof.copy_(host_prof, non_blocking=True)
-            s = binding.dspark_schedule(dconf, dprof, buffers=sbuf)
-            o = binding.dspark_verify(dbuf["target_logits"], dbuf["draft_logits"],
-                                      dbuf["draft_tokens"], s["verify_len"], dbuf["uniforms"],
-                                      vi.temperature, buffers=vbuf)
+        def copy_in(i):
+            j = i % 2
+            with torch.cuda.stream(copy_stream):
+                if i >= 2:
+                    copy_stream.wait_event(used[i - 2])  # step i-2 is done with this set
+                for k, t in host.items():
+                    dbufs[j][k].copy_(t, non_blocking=True)
+                dconfs[j].copy_(host_conf, non_blocking=True)
+                dprofs[j].copy_(host_prof, non_blocking=True)
+                copied[i].record(copy_stream)
+
+        def compute(i):
+            j = i % 2
+            stream.wait_event(copied[i])
+            s = binding.dspark_schedule(dconfs[j], dprofs[j], buffers=sbuf)
+            d = dbufs[j]
+            o = binding.dspark_verify(d["target_logits"], d["draft_logits"], d["draft_tokens"],
+                                      s["verify_len"], d["uniforms"], vi.temperature,
+                                      buffers=vbuf)
+            used[i].record(stream)
             out_acc.copy_(o["accepted_len"], non_blocking=True)
             out_em.copy_(o["emitted_tokens"], non_blocking=True)
 
-        e2e_step()
+        copy_in(0)
+        compute(0)
         torch.cuda.synchronize(dev)
         barrier(dist, dev)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
+        copy_stream.wait_event(a)
+        copy_in(1)
+        for i in range(1, n_e2e):
+            if i + 1 < n_e2e:
+                copy_in(i + 1)
+            compute(i)
         b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(dist, a.elapsed_time(b), dev)
         e2e = {"value": positions * ws * args.e2e_steps / (e2e_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e2e_ms / args.e2e_steps}
-        del host, dbuf
+               "ms_per_step": e2e_ms / args.e2e_steps,
+               "copies": "step i+1's inputs copied on a second stream while step i is verified"}
+        del host, dbufs
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
