@@ -34,6 +34,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "dspark_sync.cuh"
 #include "dspark_tc.cuh"
 #include "dspark_verify_types.cuh"
 
@@ -250,31 +251,6 @@ struct DraftPickArgs {
   int32_t* status;
   unsigned long long* ready;  // k_draft_block: [B], (k + 1) << 32 | x_k once drawn
 };
-
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned long long ld_acquire_gpu64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_gpu64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
-               : "=r"(old)
-               : "l"(p), "r"(v)
-               : "memory");
-  return old;
-}
 
 constexpr int kPickWarps = 4;   // one request per warp
 constexpr int kPickBatch = 32;  // statistics loaded per round trip by a lane
@@ -551,28 +527,6 @@ __global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickA
 // buffers, so a CTA already writing position k+1's may not overwrite what a
 // slower one still reads). Launched cooperatively (every CTA resident, one per
 // SM), so no wait can be on a CTA that is not running; every spin is bounded.
-
-// One thread per CTA. sync[0] counts arrivals and is 0 between uses (zeroed
-// before the launch, reset by the last arrival); sync[1] is a generation that
-// every CTA reads before its first arrival. Returns false if the wait gave up.
-__device__ bool grid_barrier(uint32_t* sync, uint32_t nctas, uint32_t& gen) {
-  const uint32_t g = gen;
-  __threadfence();
-  if (atom_add_acq_rel_gpu(&sync[0], 1u) == nctas - 1) {
-    atomicExch(&sync[0], 0u);
-    __threadfence();
-    st_release_gpu(&sync[1], g + 1u);
-  } else {
-    WaitClock clock;
-    while (ld_acquire_gpu(&sync[1]) == g) {
-      if (clock.expired()) return false;
-      __nanosleep(128);
-    }
-  }
-  gen = g + 1u;
-  __threadfence();
-  return true;
-}
 
 // A diagnostic of the bounded waits: one thread runs a wait whose condition
 // never comes true -- which 0: wait_or_flag on an mbarrier that no copy or

@@ -939,31 +939,36 @@ struct ItemRegs {
   int32_t out;      // index of the segment's sum
 };
 
+// Shared memory of the residual streamer: per warp STAGES stages of
+// 2 * kRowPart bytes, then per warp STAGES barriers, then per warp STAGES
+// stage records.
+template <int W, int STAGES, int kRowPart>
+__device__ __forceinline__ uint64_t* resid_bars(unsigned char* smem, int warp) {
+  return reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(W) * STAGES * 2 * kRowPart) +
+         warp * STAGES;
+}
+
+// The residual-sum streaming of one warp over its items (the body of k_resid):
+// its ring barriers are initialised and the jobs visible. Returns early (with
+// DSPARK_ERR_TIMEOUT recorded) if a copy never lands.
 template <typename Tin, int W, int STAGES, int kRowPart>
-__global__ void __launch_bounds__(W * 32, 1)
-    k_resid(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int n_jobs, int V, int n_seg,
-            ExpParams ep, const ResampleDesc* __restrict__ jobs, ff* __restrict__ sums,
-            unsigned long long* claim, int32_t* status) {
+__device__ __forceinline__ void resid_stream(const Tin* __restrict__ tl,
+                                             const Tin* __restrict__ dl, int n_jobs, int V,
+                                             int n_seg, const ExpParams& ep,
+                                             const ResampleDesc* __restrict__ jobs,
+                                             ff* __restrict__ sums, unsigned long long* claim,
+                                             int32_t* status, unsigned char* smem) {
   constexpr int RPL = kRowPart / 16 / 32;  // 16-byte vectors per lane and row part
   constexpr int kSegBytes = kSeg * static_cast<int>(sizeof(Tin));
   constexpr int kStage = 2 * kRowPart;  // target part, then draft part
   constexpr unsigned kFull = 0xFFFFFFFFu;
-  extern __shared__ __align__(1024) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* buf = smem + static_cast<size_t>(warp) * STAGES * kStage;
-  uint64_t* bars =
-      reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(W) * STAGES * kStage) +
-      warp * STAGES;
+  uint64_t* bars = resid_bars<W, STAGES, kRowPart>(smem, warp);
   StageInfo* info =
       reinterpret_cast<StageInfo*>(smem + static_cast<size_t>(W) * STAGES * (kStage + 8)) +
       warp * STAGES;
-  if (lane == 0) {
-    for (int st = 0; st < STAGES; ++st) mbar_init(&bars[st], 1);
-    fence_barrier_init();
-  }
-  __syncwarp();
-  pdl_wait();  // predecessor grid complete, its writes visible
-  pdl_trigger();
+  if (lane == 0) fence_proxy_async();  // the stages may have been written by generic stores
 
   const long long row_bytes = static_cast<long long>(V) * sizeof(Tin);
   const long long N = static_cast<long long>(n_jobs) * n_seg;
@@ -1145,6 +1150,25 @@ __global__ void __launch_bounds__(W * 32, 1)
       if (lane == 0) sums[in.out] = ff_norm(hi, lo);
     }
   }
+}
+
+template <typename Tin, int W, int STAGES, int kRowPart>
+__global__ void __launch_bounds__(W * 32, 1)
+    k_resid(const Tin* __restrict__ tl, const Tin* __restrict__ dl, int n_jobs, int V, int n_seg,
+            ExpParams ep, const ResampleDesc* __restrict__ jobs, ff* __restrict__ sums,
+            unsigned long long* claim, int32_t* status) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    uint64_t* bars = resid_bars<W, STAGES, kRowPart>(smem, warp);
+    for (int st = 0; st < STAGES; ++st) mbar_init(&bars[st], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  resid_stream<Tin, W, STAGES, kRowPart>(tl, dl, n_jobs, V, n_seg, ep, jobs, sums, claim, status,
+                                          smem);
 }
 
 // k_pick: one CTA per request draws the token after the block from the
@@ -1330,6 +1354,7 @@ int device_setup(int& sms, int& decide_per_sm) {
   decide_per_sm = s.decide_ctas_per_sm;
   return DSPARK_OK;
 }
+
 
 ExpParams exp_params(float temperature) {
   ExpParams ep;
