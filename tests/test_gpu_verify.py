@@ -164,6 +164,23 @@ def test_timed_entry_matches_plain_call(dev):
     assert all(t > 0 for t in passes), passes
 
 
+@pytest.mark.parametrize("V", [64, 63])  # bulk-copy path, plain-load path
+def test_largest_batch(dev, V):
+    """B = 65,535, the largest batch the calls take (one CTA per request in the
+    decision kernels), short rows: every request against the oracle."""
+    vi = workloads.make_verify(65535, 2, V, torch.bfloat16, 1.0, rho=(0.5, 0.95),
+                               verify_len="uniform", seed=13, device=dev)
+    check_all(vi, nthreads=None)
+
+
+def test_very_long_rows(dev):
+    """V = 1,000,000 (123 work units and 489 resample segments per row): more
+    segment sums than the draw keeps in registers."""
+    vi = workloads.make_verify(3, 2, 1000000, torch.bfloat16, 0.8, rho=(0.5, 0.95), seed=14,
+                               device=dev)
+    check_all(vi)
+
+
 def test_busy_device_gives_the_same_outputs(dev):
     """The streaming pass and the residual sums claim their last work units
     from counters, so which CTA takes which unit depends on timing. With other
