@@ -63,6 +63,8 @@ SHAPES = [
     (12, 16, 5000, torch.float32, 1.3, "uniform", True),    # fp32, ragged rows
     (6, 4, 4099, torch.float32, 0.7, "full", False),        # fp32 odd V: plain path
     (5, 32, 9000, torch.bfloat16, 1.0, "full", False),      # gamma = 32
+    (8, 16, 10000, torch.bfloat16, 0.05, "full", False),    # cold: nearly one-hot rows
+    (8, 16, 10000, torch.bfloat16, 20.0, "uniform", False), # hot: nearly flat rows
 ]
 
 

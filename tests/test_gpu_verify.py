@@ -55,6 +55,9 @@ SMALL = [
     (6, 4, 4099, torch.float32, 0.7, "full", False),         # fp32 odd V: plain path
     (5, 32, 9000, torch.bfloat16, 1.0, "full", False),       # gamma = 32
     (40, 1, 16384, torch.bfloat16, 0.9, "full", True),       # gamma = 1, exact tile multiple
+    (8, 16, 10000, torch.bfloat16, 0.05, "full", False),     # cold: nearly one-hot rows
+    (8, 16, 10000, torch.bfloat16, 20.0, "uniform", False),  # hot: nearly flat rows
+    (6, 8, 7000, torch.float32, 0.05, "uniform", True),      # cold fp32, ragged
 ]
 
 
