@@ -310,6 +310,7 @@ def native_arm(args):
     torch.cuda.synchronize(dev)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed steps")  # for a profiler's timeline
     t_start.record(stream)
     side.wait_event(t_start)
     schedule_on_side(0)
@@ -322,6 +323,7 @@ def native_arm(args):
                               stream=stream)
         done[i].record(stream)
     t_end.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     barrier(dist, dev)
     clk = clocks.stop()
