@@ -123,9 +123,9 @@ __device__ __forceinline__ void unit_finish(const LaneAcc& a, TileStat* out, int
 // must be 16-byte aligned. Shared memory: W warps x STAGES x (4 KB + barrier +
 // 16-byte chunk record).
 //
-// Work assignment: warp gw takes units gw, gw + GW, ... for the first n_static
-// rounds (all but about 1/kDynamicDiv of the units), then claims the remaining
-// units one at a time from a counter (reset by k_plan). A CTA that starts late
+// Work assignment: warp gw takes units gw, gw + GW, ... among the first
+// U - U/kDynamicDiv units, then claims the remaining ones (about
+// 1/kDynamicDiv) one at a time from a counter (reset by k_plan). A CTA that starts late
 // -- its SM still held by another kernel, e.g. a scheduler running on another
 // stream -- then takes fewer of the last units instead of finishing late. The
 // producer (lane 0) records which unit and bytes each stage holds, so the
@@ -165,8 +165,11 @@ __global__ void __launch_bounds__(W * 32, 1)
   const long long gw = static_cast<long long>(blockIdx.x) * W + warp;
   const long long GW = static_cast<long long>(gridDim.x) * W;
   const long long row_bytes = static_cast<long long>(V) * sizeof(Tin);
-  const long long n_static = (U - U / kDynamicDiv) / GW;  // rounds taken statically
-  const long long dyn0 = n_static * GW;                    // first unit of the claims
+  // the first S units in fixed rounds (warp gw: gw, gw + GW, ... below S),
+  // the last U - S (about 1/kDynamicDiv) claimed
+  const long long S = U - U / kDynamicDiv;
+  const long long n_static = gw < S ? (S - 1 - gw) / GW + 1 : 0;
+  const long long dyn0 = S;  // first unit of the claims
 
   // producer cursor (lane 0): the unit being copied and its next chunk
   long long k_st = 0;

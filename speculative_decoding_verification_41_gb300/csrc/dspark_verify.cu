@@ -977,9 +977,9 @@ __device__ __forceinline__ void resid_stream(const Tin* __restrict__ tl,
   // items in fixed rounds for all but about 1/kDynamicDiv of them (warp g0:
   // items g0 + k GW, k < n_fixed), then claimed one at a time from *claim, so
   // that warps of CTAs that start late or run slow take fewer of the last ones
-  const long long n_static = (N - N / kDynamicDiv) / GW;
-  const int n_fixed = static_cast<int>(n_static);
-  const long long dyn0 = n_static * GW;
+  const long long S = N - N / kDynamicDiv;  // items in fixed rounds
+  const int n_fixed = g0 < S ? static_cast<int>((S - 1 - g0) / GW + 1) : 0;
+  const long long dyn0 = S;
 
   auto describe = [&](long long i, ItemRegs& o) {  // the descriptor of item i
     o.mode = kModeNone;
