@@ -495,6 +495,12 @@ __device__ __forceinline__ void draw_request(const DraftPickArgs& a, int b, int 
   if (gw != 0) return;
   if (lane == 0) a.tokens[static_cast<size_t>(b) * a.gamma + a.k] = y;
   if (a.ready) {  // publish the token: the next position's CTAs read W1[x_k] themselves
+    // (first pulled into L2 here, so that those reads hit it)
+    if (a.k + 1 < a.gamma && lane * 128 < a.r * 2) {
+      const char* line = reinterpret_cast<const char*>(a.W1 + static_cast<size_t>(y) * a.r) +
+                         lane * 128;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
+    }
     if (lane == 0 && a.k + 1 < a.gamma)
       st_release_gpu64(&a.ready[b], (static_cast<unsigned long long>(a.k + 1) << 32) |
                                         static_cast<uint32_t>(y));
