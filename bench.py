@@ -540,6 +540,7 @@ def native_arm(args):
         drafter["roofline"]["peak"] = peak
         drafter["roofline"]["frac"] = drafter["roofline"]["achieved"] / peak
         drafter["roofline"]["peak_source"] = peak_src
+        drafter["block"]["frac"] = drafter["block"]["achieved"] / peak
     print(json.dumps(line), flush=True)
 
 
@@ -631,6 +632,11 @@ def drafter_measure(args, dev, stream, rank, ws):
                      "kernel": "k_draft_step (median CUDA-event interval around each of the 16 "
                                "launches, dspark_draft_markov_timed)",
                      "tensor_tflops": flops / (t_step * 1e-3) / 1e12},
+        # the product path, the whole block as one launch: the same bytes per
+        # position (W2 counted once) over the call time, serial chain included
+        "block": {"kernel": "k_draft_block", "algorithmic_bytes": alg * g,
+                  "achieved": alg * g / (t_call * 1e-3) / 1e9, "unit": "GB/s",
+                  "tensor_tflops": flops * g / (t_call * 1e-3) / 1e12},
         "gpu_launches_per_call": 1,  # k_draft_block (cooperative), after one 2 KB memset
         "gpu_launches_per_call_timed_path": 1 + 2 * g,
         "cpu_baseline": None,
