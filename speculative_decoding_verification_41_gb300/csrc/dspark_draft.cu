@@ -303,6 +303,90 @@ struct DrawShared {
   int32_t pad;
 };
 
+// The token inside crossing tile g of request b: the tile's 128 terms
+// recomputed exactly as the tile kernel did (each 32-column chunk (8 lanes)
+// with its own reference, scaled to the request's Rmax), scanned on from
+// s_before to the first running sum above target. All lanes of one warp.
+template <bool kCoherent>
+__device__ __forceinline__ int draw_in_tile(const DraftPickArgs& a, int b, int g, ff s_before,
+                                            ff target, int32_t Rmax, int lane) {
+  // the crossing tile: recompute its 128 terms exactly as the step kernel
+  // did, each 32-column chunk (8 lanes) with its own reference
+  const int v = g * kDN + 4 * lane;
+  float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  if (v < a.V) {  // V is a multiple of 8: v + 3 < V too
+    const uint2 raw =
+        ld_u2<kCoherent>(a.L + (static_cast<size_t>(b) * a.gamma + a.k) * a.V + v);
+    z[0] = bf16_lo(raw.x);
+    z[1] = bf16_hi(raw.x);
+    z[2] = bf16_lo(raw.y);
+    z[3] = bf16_hi(raw.y);
+  }
+  float cm = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, o));
+  const int32_t Rc = chunk_reference(cm, a.ep.c_hi);
+  float w[4] = {0.f, 0.f, 0.f, 0.f};
+  if (Rc != INT_MIN && v < a.V) {
+    const float nK = -static_cast<float>(Rc);
+    const float scale = pow2_nonpos(Rc - Rmax);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) w[e] = exp_term(z[e], nK, a.ep) * scale;
+  }
+  ff lsum{0.f, 0.f};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) lsum = ff_add(lsum, ff{w[e], 0.f});
+  const ff inc_l = warp_incl_scan_ff(lsum, lane);
+  const ff pre = shfl_up_ff(inc_l, 1);
+  const ff base = ff_add(s_before, lane > 0 ? pre : ff{0.f, 0.f});
+  const uint32_t cross = __ballot_sync(0xFFFFFFFFu, ff_cmp(ff_add(s_before, inc_l), target) > 0);
+  int pick = -1;
+  if (cross) {
+    const int L0 = __ffs(cross) - 1;
+    if (lane == L0) {
+      ff c = base;
+      int last = -1;
+      for (int e = 0; e < 4; ++e) {
+        if (w[e] > 0.f) last = e;
+        const ff nc = ff_add(c, ff{w[e], 0.f});
+        if (w[e] > 0.f && ff_cmp(nc, target) > 0) {
+          pick = v + e;
+          break;
+        }
+        c = nc;
+      }
+      if (pick < 0) pick = v + (last >= 0 ? last : 0);
+    }
+    pick = __shfl_sync(0xFFFFFFFFu, pick, L0);
+  } else {  // rounding: the last token of the tile with positive weight
+    const int lpos = (w[3] > 0.f) ? 3 : (w[2] > 0.f) ? 2 : (w[1] > 0.f) ? 1 : (w[0] > 0.f) ? 0 : -1;
+    const uint32_t any = __ballot_sync(0xFFFFFFFFu, lpos >= 0);
+    const int Lh = any ? 31 - __clz(any) : 0;
+    const int e = __shfl_sync(0xFFFFFFFFu, lpos, Lh);
+    pick = g * kDN + 4 * Lh + (e >= 0 ? e : 0);
+  }
+  return pick;
+}
+
+// The drawn token out: the tokens array, then either the ready flag the single
+// launch's next position waits on (with W1[x_k] pulled into L2 first, so that
+// the CTAs loading it hit L2) or the row G[b] = W1[x_k] the next launch reads.
+__device__ __forceinline__ void publish_token(const DraftPickArgs& a, int b, int y, int lane) {
+  if (lane == 0) a.tokens[static_cast<size_t>(b) * a.gamma + a.k] = y;
+  if (a.ready) {
+    if (a.k + 1 < a.gamma && lane * 128 < a.r * 2) {
+      const char* line = reinterpret_cast<const char*>(a.W1 + static_cast<size_t>(y) * a.r) +
+                         lane * 128;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
+    }
+    if (lane == 0 && a.k + 1 < a.gamma)
+      st_release_gpu64(&a.ready[b], (static_cast<unsigned long long>(a.k + 1) << 32) |
+                                        static_cast<uint32_t>(y));
+  } else if (a.k + 1 < a.gamma) {
+    copy_row(a.W1, a.G, y, b, a.r, lane);
+  }
+}
+
 // NW warps draw position k of request b together (gw = this warp's index in
 // the group; NW > 1 synchronises the group on named barrier bar_id through
 // *sh), in float-float arithmetic (about 48 significant bits; this GPU's FP64
@@ -433,80 +517,163 @@ __device__ __forceinline__ void draw_request(const DraftPickArgs& a, int b, int 
       g = own ? __shfl_sync(0xFFFFFFFFu, gs, ol) : -1;
       s_before = shfl_ff(before, ol);
     }
-    if (g >= 0 && gw == 0) {
-      // the crossing tile: recompute its 128 terms exactly as the step kernel
-      // did, each 32-column chunk (8 lanes) with its own reference
-      const int v = g * kDN + 4 * lane;
-      float z[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (v < a.V) {  // V is a multiple of 8: v + 3 < V too
-        const uint2 raw =
-            ld_u2<kCoherent>(a.L + (static_cast<size_t>(b) * a.gamma + a.k) * a.V + v);
-        z[0] = bf16_lo(raw.x);
-        z[1] = bf16_hi(raw.x);
-        z[2] = bf16_lo(raw.y);
-        z[3] = bf16_hi(raw.y);
-      }
-      float cm = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, o));
-      const int32_t Rc = chunk_reference(cm, a.ep.c_hi);
-      float w[4] = {0.f, 0.f, 0.f, 0.f};
-      if (Rc != INT_MIN && v < a.V) {
-        const float nK = -static_cast<float>(Rc);
-        const float scale = pow2_nonpos(Rc - Rmax);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) w[e] = exp_term(z[e], nK, a.ep) * scale;
-      }
-      ff lsum{0.f, 0.f};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) lsum = ff_add(lsum, ff{w[e], 0.f});
-      const ff inc_l = warp_incl_scan_ff(lsum, lane);
-      const ff pre = shfl_up_ff(inc_l, 1);
-      const ff base = ff_add(s_before, lane > 0 ? pre : ff{0.f, 0.f});
-      const uint32_t cross = __ballot_sync(0xFFFFFFFFu, ff_cmp(ff_add(s_before, inc_l), target) > 0);
-      int pick = -1;
-      if (cross) {
-        const int L0 = __ffs(cross) - 1;
-        if (lane == L0) {
-          ff c = base;
-          int last = -1;
-          for (int e = 0; e < 4; ++e) {
-            if (w[e] > 0.f) last = e;
-            const ff nc = ff_add(c, ff{w[e], 0.f});
-            if (w[e] > 0.f && ff_cmp(nc, target) > 0) {
-              pick = v + e;
-              break;
-            }
-            c = nc;
-          }
-          if (pick < 0) pick = v + (last >= 0 ? last : 0);
-        }
-        pick = __shfl_sync(0xFFFFFFFFu, pick, L0);
-      } else {  // rounding: the last token of the tile with positive weight
-        const int lpos = (w[3] > 0.f) ? 3 : (w[2] > 0.f) ? 2 : (w[1] > 0.f) ? 1 : (w[0] > 0.f) ? 0 : -1;
-        const uint32_t any = __ballot_sync(0xFFFFFFFFu, lpos >= 0);
-        const int Lh = any ? 31 - __clz(any) : 0;
-        const int e = __shfl_sync(0xFFFFFFFFu, lpos, Lh);
-        pick = g * kDN + 4 * Lh + (e >= 0 ? e : 0);
-      }
-      y = pick;
-    }
+    if (g >= 0 && gw == 0) y = draw_in_tile<kCoherent>(a, b, g, s_before, target, Rmax, lane);
   }
   if (gw != 0) return;
-  if (lane == 0) a.tokens[static_cast<size_t>(b) * a.gamma + a.k] = y;
-  if (a.ready) {  // publish the token: the next position's CTAs read W1[x_k] themselves
-    // (first pulled into L2 here, so that those reads hit it)
-    if (a.k + 1 < a.gamma && lane * 128 < a.r * 2) {
-      const char* line = reinterpret_cast<const char*>(a.W1 + static_cast<size_t>(y) * a.r) +
-                         lane * 128;
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
-    }
-    if (lane == 0 && a.k + 1 < a.gamma)
-      st_release_gpu64(&a.ready[b], (static_cast<unsigned long long>(a.k + 1) << 32) |
-                                        static_cast<uint32_t>(y));
-  } else if (a.k + 1 < a.gamma) {
-    copy_row(a.W1, a.G, y, b, a.r, lane);
+  publish_token(a, b, y, lane);
+}
+
+// The vocabulary tiles of a request tile are split into per_m contiguous
+// ranges, one per CTA: range p is [range_begin(p), range_begin(p + 1)).
+__device__ __forceinline__ int range_begin(int p, int n_tiles, int per_m) {
+  return static_cast<int>(static_cast<long long>(p) * n_tiles / per_m);
+}
+
+// One request's softmax mass over one CTA's range of tiles at one position:
+// sum 2^(L_v * c - R) = hi + lo (a float pair), R the largest tile reference
+// of the range (INT_MIN if every term is 0). The single launch's draws scan
+// these first, then the tiles of the one range holding the cut.
+struct __align__(16) DraftPartial {
+  float hi, lo;
+  int32_t R;
+  int32_t pad;
+};
+// Partial records the workspace holds per position parity: per_m ranges of
+// 128 requests for each of at most this many CTAs of a single-launch grid.
+constexpr int kMaxBlockCtas = 256;
+
+// A per-range record of the running single launch (through L2 only).
+__device__ __forceinline__ DraftPartial ld_part(const DraftPartial* p) {
+  int4 v;
+  asm volatile("ld.global.cg.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return DraftPartial{__int_as_float(v.x), __int_as_float(v.y), v.z, v.w};
+}
+
+// (R, S) += (R2, S2) for masses referenced to 2^R: aligned by an exact power
+// of two (R = INT_MIN: nothing yet).
+__device__ __forceinline__ void mass_add(int32_t& R, ff& S, int32_t R2, ff S2) {
+  if (R2 == INT_MIN || !(S2.hi > 0.f)) return;
+  if (R2 > R) {
+    S = R == INT_MIN ? ff{0.f, 0.f} : ff_scale(S, pow2_nonpos(R - R2));
+    R = R2;
   }
+  S = ff_add(S, ff_scale(S2, pow2_nonpos(R2 - R)));
+}
+
+// One warp draws position k of request b in the single launch, from the
+// masses of the CTAs' contiguous vocabulary ranges (parts: this request's
+// per_m ranges, two group records each): the lanes own contiguous runs of
+// ranges and scan them to the range holding u*Z (the lanes partition [0, Z)
+// as in draw_request), that range's tiles are scanned to the crossing tile,
+// and draw_in_tile finishes. Float pairs and exact powers of two throughout,
+// as in draw_request; only the grouping of the sums differs.
+constexpr int kRangesHeld = kMaxBlockCtas / 32;  // ranges per lane at most
+__device__ __forceinline__ void draw_ranges(const DraftPickArgs& a, int b, int lane,
+                                            const DraftPartial* parts, int per_m) {
+  const int per = (per_m + 31) / 32;
+  const int p0 = min(lane * per, per_m), p1 = min(p0 + per, per_m);
+  int32_t rR[kRangesHeld];
+  ff rS[kRangesHeld];
+  int32_t Rl = INT_MIN;
+  ff Sl{0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < kRangesHeld; ++i) {
+    rR[i] = INT_MIN;
+    rS[i] = ff{0.f, 0.f};
+    if (p0 + i < p1) {
+      const DraftPartial q0 = ld_part(parts + 2 * (p0 + i)), q1 = ld_part(parts + 2 * (p0 + i) + 1);
+      mass_add(rR[i], rS[i], q0.R, ff{q0.hi, q0.lo});
+      mass_add(rR[i], rS[i], q1.R, ff{q1.hi, q1.lo});
+      mass_add(Rl, Sl, rR[i], rS[i]);
+    }
+  }
+  int32_t Rmax = Rl;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Rmax = max(Rmax, __shfl_xor_sync(0xFFFFFFFFu, Rmax, o));
+  const float u = a.uniforms[static_cast<size_t>(b) * a.gamma + a.k];
+  int y = 0;
+  if (Rmax == INT_MIN || !(u >= 0.f && u < 1.f)) {
+    if (lane == 0) set_status(a.status, DSPARK_ERR_BAD_DATA);
+    publish_token(a, b, y, lane);
+    return;
+  }
+  // level 1: the ranges
+  const ff S = Rl == INT_MIN ? ff{0.f, 0.f} : ff_scale(Sl, pow2_nonpos(Rl - Rmax));
+  const ff incl = warp_incl_scan_ff(S, lane);
+  const ff Z = shfl_ff(incl, 31);
+  const ff prev = shfl_up_ff(incl, 1);
+  const ff excl = lane > 0 ? prev : ff{0.f, 0.f};
+  const ff target = ff_mul(ff{u, 0.f}, Z);
+  const uint32_t own = __ballot_sync(0xFFFFFFFFu, S.hi > 0.f && ff_cmp(excl, target) <= 0 &&
+                                                        ff_cmp(target, incl) < 0);
+  int ps = -1;
+  ff before{0.f, 0.f};
+  if (own && lane == __ffs(own) - 1) {  // walk this lane's ranges
+    ff C = excl, Clast = excl;
+    int plast = -1;
+#pragma unroll
+    for (int i = 0; i < kRangesHeld; ++i) {
+      if (ps >= 0 || p0 + i >= p1 || rR[i] == INT_MIN || !(rS[i].hi > 0.f)) continue;
+      const ff next = ff_add(C, ff_scale(rS[i], pow2_nonpos(rR[i] - Rmax)));
+      if (ff_cmp(next, target) > 0) {
+        ps = p0 + i;
+        before = C;
+      } else {
+        plast = p0 + i;
+        Clast = C;
+        C = next;
+      }
+    }
+    if (ps < 0) {  // rounding left the target past this lane's last range: take it
+      ps = plast;
+      before = Clast;
+    }
+  }
+  const int ol = own ? __ffs(own) - 1 : 0;
+  ps = own ? __shfl_sync(0xFFFFFFFFu, ps, ol) : -1;
+  before = shfl_ff(before, ol);
+  if (ps < 0) {  // no mass where the scan put the cut: the masses and the scan disagree
+    if (lane == 0) set_status(a.status, DSPARK_ERR_BAD_DATA);
+    publish_token(a, b, y, lane);
+    return;
+  }
+  // level 2: the tiles of range ps, in order
+  const DraftStat* st = a.stats + static_cast<size_t>(b) * a.n_tiles;
+  const int t0 = range_begin(ps, a.n_tiles, per_m), t1 = range_begin(ps + 1, a.n_tiles, per_m);
+  int g = -1, glast = -1;
+  ff s_before{0.f, 0.f}, s_last{0.f, 0.f}, base = before;
+  for (int c0 = t0; c0 < t1 && g < 0; c0 += 32) {
+    const int t = c0 + lane;
+    ff w{0.f, 0.f};
+    if (t < t1) {
+      const DraftStat d = ld_stat<true>(st + t);
+      if (d.s > 0.f && d.R != INT_MIN) w = ff{d.s * pow2_nonpos(d.R - Rmax), 0.f};
+    }
+    const ff inc_t = ff_add(base, warp_incl_scan_ff(w, lane));
+    const ff pre = shfl_up_ff(inc_t, 1);
+    const ff exc_t = lane > 0 ? pre : base;
+    const uint32_t cross = __ballot_sync(0xFFFFFFFFu, w.hi > 0.f && ff_cmp(inc_t, target) > 0);
+    const uint32_t pos = __ballot_sync(0xFFFFFFFFu, w.hi > 0.f);
+    if (cross) {
+      const int l = __ffs(cross) - 1;
+      g = c0 + l;
+      s_before = shfl_ff(exc_t, l);
+    } else if (pos) {
+      const int l = 31 - __clz(pos);
+      glast = c0 + l;
+      s_last = shfl_ff(exc_t, l);
+    }
+    base = shfl_ff(inc_t, 31);
+  }
+  if (g < 0) {  // rounding: the range's last tile with mass
+    g = glast;
+    s_before = s_last;
+  }
+  if (g >= 0) y = draw_in_tile<true>(a, b, g, s_before, target, Rmax, lane);
+  publish_token(a, b, y, lane);
 }
 
 __global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickArgs a) {
@@ -552,6 +719,7 @@ __global__ void k_wait_selftest(int which, uint32_t* sync, int32_t* status) {
   }
 }
 
+
 struct DraftBlockArgs {
   DraftStepArgs s;     // s.k unused; s.stats: the statistics (of even positions)
   DraftPickArgs p;     // p.k and p.stats set per position
@@ -561,6 +729,7 @@ struct DraftBlockArgs {
   const int32_t* anchors;       // x_0
   uint32_t* sync;               // [2]
   unsigned long long* ready;    // [B]
+  DraftPartial* parts;          // [2][n_m * 128][per_m]: per-range masses by position parity
 };
 
 template <bool kBlock>
@@ -574,16 +743,16 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tile = blockIdx.x % a.n_m;
-  const int p = blockIdx.x / a.n_m;
-  const int n_local = p < a.n_tiles ? (a.n_tiles - p + a.per_m - 1) / a.per_m : 0;
+  const int p = blockIdx.x / a.n_m;  // this CTA's vocabulary range in its request tile
+  const int lo = range_begin(p, a.n_tiles, a.per_m), hi = range_begin(p + 1, a.n_tiles, a.per_m);
+  const int n_local = hi - lo;
   const int KC = a.r / kDK;
   const int k0 = ba.k_begin;
   const int npos = ba.k_end - ba.k_begin;  // positions of this launch
-  // position k's t-th vocabulary tile of this CTA (odd positions walk backwards)
-  auto tile_of = [&](int k, int t) {
-    const int n = p + t * a.per_m;
-    return (k & 1) ? a.n_tiles - 1 - n : n;
-  };
+  // position k's t-th vocabulary tile of this CTA: its contiguous range, odd
+  // positions backwards (a position starts on the W2 tiles the previous one
+  // read last; the CTAs of the other request tiles walk the same ranges)
+  auto tile_of = [&](int k, int t) { return (k & 1) ? hi - 1 - t : lo + t; };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->a_full, kDEpiWarps);
@@ -711,7 +880,6 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
     const bool leader = (warp == 2 + 4 * grp) && lane == 0;
     const bool syncer = warp == 2 && lane == 0;  // takes part in the grid barriers
     const uint64_t pol_out = policy_evict_first();
-    __shared__ DrawShared sh_draw[2];
     uint32_t gen = 0;
     if (syncer) gen = ld_acquire_gpu(&ba.sync[1]);
     int jg = 0;        // tiles this group has finished (all positions)
@@ -794,7 +962,10 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->a_full);
       }
-      // this position's tiles: tile tg of the block goes to group tg & 1
+      // this position's tiles: tile tg of the block goes to group tg & 1; the
+      // single launch also sums each request's mass over the group's tiles
+      int32_t Rp = INT_MIN;
+      ff Sp{0.f, 0.f};
       for (int t = 0; t < n_local; ++t) {
         const int tg = j * n_local + t;
         if ((tg & 1) != grp) continue;
@@ -825,6 +996,8 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
           ((kBlock && (k & 1)) ? ba.stats1 : a.stats)[static_cast<size_t>(b) * a.n_tiles + n] =
               DraftStat{bad ? 0.f : total, bad ? INT_MIN : R};
         }
+        if constexpr (kBlock)
+          if (!bad && total > 0.f) mass_add(Rp, Sp, R, ff{total, 0.f});
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->st_ready[grp]);
@@ -842,6 +1015,9 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
       }
       if (!ok) break;
       if constexpr (!kBlock) break;  // one position; the draw is the next kernel
+      if (row_ok)  // this group's share of the request's mass over the CTA's range
+        ba.parts[((static_cast<size_t>(k & 1) * a.n_m * kDM + b) * a.per_m + p) * 2 + grp] =
+            DraftPartial{Sp.hi, Sp.lo, Rp, 0};
       // the rows of this position are in memory (stores complete, visible to
       // the generic proxy of every CTA) and so are the statistics
       if (leader) {
@@ -858,9 +1034,11 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
       pa.k = k;
       pa.stats = (k & 1) ? ba.stats1 : a.stats;
       pa.ready = ba.ready;
-      // one request per group of four epilogue warps
-      for (int rq = (ew >> 2) * gridDim.x + blockIdx.x; rq < a.B; rq += 2 * gridDim.x)
-        draw_request<true, 4>(pa, rq, ew & 3, lane, &sh_draw[ew >> 2], 1 + (ew >> 2));
+      // one request per epilogue warp, from the ranges' masses
+      const DraftPartial* parts_k =
+          ba.parts + static_cast<size_t>(k & 1) * a.n_m * kDM * a.per_m * 2;
+      for (int rq = ew * gridDim.x + blockIdx.x; rq < a.B; rq += kDEpiWarps * gridDim.x)
+        draw_ranges(pa, rq, lane, parts_k + static_cast<size_t>(rq) * a.per_m * 2, a.per_m);
     }
     if (leader) bulk_wait<0>();
   }
@@ -1008,6 +1186,8 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
       2 * DSPARK_ALIGN256(static_cast<size_t>(B) * n_tiles * 8));
   unsigned long long* ready =
       reinterpret_cast<unsigned long long*>(sync + 64);  // 256 bytes after the barrier words
+  DraftPartial* parts = reinterpret_cast<DraftPartial*>(
+      reinterpret_cast<char*>(ready) + DSPARK_ALIGN256(static_cast<size_t>(B) * 8));
 
   CUtensorMap mapW, mapU, mapL;
   {
@@ -1029,7 +1209,7 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
   const uint16_t* W1 = static_cast<const uint16_t*>(w1);
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   const int grid = n_m * per_m;
-  if (!ev && coop && grid <= sms) {
+  if (!ev && coop && grid <= sms && grid <= kMaxBlockCtas) {
     // the whole block in one cooperative launch (every CTA resident, one per SM)
     if (cudaMemsetAsync(sync, 0, 256 + static_cast<size_t>(B) * 8, stream) != cudaSuccess)
       return DSPARK_ERR_CUDA;
@@ -1045,6 +1225,7 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
     ba.anchors = anchors;
     ba.sync = sync;
     ba.ready = ready;
+    ba.parts = parts;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = kDThreads;
