@@ -541,6 +541,9 @@ struct __align__(16) DraftPartial {
 // Partial records the workspace holds per position parity: per_m ranges of
 // 128 requests for each of at most this many CTAs of a single-launch grid.
 constexpr int kMaxBlockCtas = 256;
+// Barrier words of the single launch's request tiles (at most kMaxBlockCtas
+// tiles, 16 bytes each).
+constexpr size_t kTileSyncBytes = 16 * kMaxBlockCtas;
 
 // A per-range record of the running single launch (through L2 only).
 __device__ __forceinline__ DraftPartial ld_part(const DraftPartial* p) {
@@ -729,6 +732,7 @@ struct DraftBlockArgs {
   const int32_t* anchors;       // x_0
   uint32_t* sync;               // [2]
   unsigned long long* ready;    // [B]
+  uint32_t* tile_sync;          // [n_m][4]: a barrier (count, generation) per request tile
   DraftPartial* parts;          // [2][n_m * 128][per_m]: per-range masses by position parity
 };
 
@@ -881,7 +885,13 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
     const bool syncer = warp == 2 && lane == 0;  // takes part in the grid barriers
     const uint64_t pol_out = policy_evict_first();
     uint32_t gen = 0;
-    if (syncer) gen = ld_acquire_gpu(&ba.sync[1]);
+    // the CTAs of one request tile synchronise among themselves: a position's
+    // draws read only that tile's statistics and range masses, and its next
+    // position waits only on that tile's tokens
+    // (the per-launch kernel has no barrier words and never touches them)
+    uint32_t* const tbar = kBlock ? ba.tile_sync + 4 * m_tile : nullptr;
+    if constexpr (kBlock)
+      if (syncer) gen = ld_acquire_gpu(&tbar[1]);
     int jg = 0;        // tiles this group has finished (all positions)
     int uses = 0;      // epi_done / step_go phases used so far
     bool ok = true;
@@ -891,7 +901,7 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
       bool good = true;
       if (syncer) {
         good = wait_or_flag(&bars->epi_done, uses & 1, a.status) &&
-               grid_barrier(ba.sync, gridDim.x, gen);
+               grid_barrier(tbar, static_cast<uint32_t>(a.per_m), gen);
         if (!good) set_status(a.status, DSPARK_ERR_TIMEOUT);
         mbar_arrive(&bars->step_go);
       }
@@ -1029,7 +1039,7 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
         ok = false;
         break;
       }
-      // the draws: one warp per request, spread over every CTA
+      // the draws: one warp per request, spread over the request tile's CTAs
       DraftPickArgs pa = ba.p;
       pa.k = k;
       pa.stats = (k & 1) ? ba.stats1 : a.stats;
@@ -1037,8 +1047,11 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
       // one request per epilogue warp, from the ranges' masses
       const DraftPartial* parts_k =
           ba.parts + static_cast<size_t>(k & 1) * a.n_m * kDM * a.per_m * 2;
-      for (int rq = ew * gridDim.x + blockIdx.x; rq < a.B; rq += kDEpiWarps * gridDim.x)
+      for (int i = ew * a.per_m + p; i < kDM; i += kDEpiWarps * a.per_m) {
+        const int rq = m_tile * kDM + i;
+        if (rq >= a.B) break;
         draw_ranges(pa, rq, lane, parts_k + static_cast<size_t>(rq) * a.per_m * 2, a.per_m);
+      }
     }
     if (leader) bulk_wait<0>();
   }
@@ -1186,8 +1199,10 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
       2 * DSPARK_ALIGN256(static_cast<size_t>(B) * n_tiles * 8));
   unsigned long long* ready =
       reinterpret_cast<unsigned long long*>(sync + 64);  // 256 bytes after the barrier words
-  DraftPartial* parts = reinterpret_cast<DraftPartial*>(
-      reinterpret_cast<char*>(ready) + DSPARK_ALIGN256(static_cast<size_t>(B) * 8));
+  uint32_t* tile_sync = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(ready) +
+                                                     DSPARK_ALIGN256(static_cast<size_t>(B) * 8));
+  DraftPartial* parts =
+      reinterpret_cast<DraftPartial*>(reinterpret_cast<char*>(tile_sync) + kTileSyncBytes);
 
   CUtensorMap mapW, mapU, mapL;
   {
@@ -1211,7 +1226,9 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
   const int grid = n_m * per_m;
   if (!ev && coop && grid <= sms && grid <= kMaxBlockCtas) {
     // the whole block in one cooperative launch (every CTA resident, one per SM)
-    if (cudaMemsetAsync(sync, 0, 256 + static_cast<size_t>(B) * 8, stream) != cudaSuccess)
+    if (cudaMemsetAsync(sync, 0,
+                        256 + DSPARK_ALIGN256(static_cast<size_t>(B) * 8) + kTileSyncBytes,
+                        stream) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     DraftBlockArgs ba{};
     ba.s = DraftStepArgs{B, Vi, r, gamma, 0, n_tiles, n_m, per_m, ep, stats, device_status};
@@ -1226,6 +1243,7 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
     ba.sync = sync;
     ba.ready = ready;
     ba.parts = parts;
+    ba.tile_sync = tile_sync;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = kDThreads;
