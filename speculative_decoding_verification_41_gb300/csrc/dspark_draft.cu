@@ -294,15 +294,6 @@ __device__ __forceinline__ ff warp_incl_scan_ff(ff v, int lane) {
   return v;
 }
 
-// Scratch of a group of warps drawing one request together.
-struct DrawShared {
-  int32_t rmax[4];
-  ff tot[4];
-  ff before;
-  int32_t g;
-  int32_t pad;
-};
-
 // The token inside crossing tile g of request b: the tile's 128 terms
 // recomputed exactly as the tile kernel did (each 32-column chunk (8 lanes)
 // with its own reference, scaled to the request's Rmax), scanned on from
@@ -387,25 +378,20 @@ __device__ __forceinline__ void publish_token(const DraftPickArgs& a, int b, int
   }
 }
 
-// NW warps draw position k of request b together (gw = this warp's index in
-// the group; NW > 1 synchronises the group on named barrier bar_id through
-// *sh), in float-float arithmetic (about 48 significant bits; this GPU's FP64
-// rate is far too low for it): the group's lanes own contiguous runs of the
-// request's tile statistics, a scan gives every lane its exclusive prefix (the
-// next lane's exclusive prefix is bitwise this lane's inclusive one, across
-// warps too, so the lanes partition [0, Z)), the owning lane walks its run to
-// the crossing tile, and the group's first warp recomputes that tile's 128
-// terms exactly as the step kernel did and draws.
-template <bool kCoherent, int NW>
-__device__ __forceinline__ void draw_request(const DraftPickArgs& a, int b, int gw, int lane,
-                                             DrawShared* sh, int bar_id) {
+// One warp draws position k of request b from the tile statistics of an
+// earlier kernel, in float-float arithmetic (about 48 significant bits; this
+// GPU's FP64 rate is far too low for it): the lanes own contiguous runs of
+// the request's tile statistics, a scan gives every lane its exclusive prefix
+// (the next lane's exclusive prefix is bitwise this lane's inclusive one, so
+// the lanes partition [0, Z)), the owning lane walks its run to the crossing
+// tile, and draw_in_tile recomputes that tile's 128 terms exactly as the step
+// kernel did and draws.
+template <bool kCoherent>
+__device__ __forceinline__ void draw_request(const DraftPickArgs& a, int b, int lane) {
   const DraftStat* st = a.stats + static_cast<size_t>(b) * a.n_tiles;
-  const int per = (a.n_tiles + 32 * NW - 1) / (32 * NW);
-  const int g0 = (gw * 32 + lane) * per < a.n_tiles ? (gw * 32 + lane) * per : a.n_tiles;
+  const int per = (a.n_tiles + 31) / 32;
+  const int g0 = lane * per < a.n_tiles ? lane * per : a.n_tiles;
   const int g1 = g0 + per < a.n_tiles ? g0 + per : a.n_tiles;
-  auto gsync = [&]() {
-    if constexpr (NW > 1) named_bar_sync(bar_id, NW * 32);
-  };
 
   // one pass over the lane's tiles, loads issued kPickBatch at a time (all at
   // once, and kept for the walk below, when they fit): the lane's largest
@@ -432,43 +418,17 @@ __device__ __forceinline__ void draw_request(const DraftPickArgs& a, int b, int 
   int32_t Rmax = Rl;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) Rmax = max(Rmax, __shfl_xor_sync(0xFFFFFFFFu, Rmax, o));
-  if constexpr (NW > 1) {
-    if (lane == 0) {
-      sh->rmax[gw] = Rmax;
-      if (gw == 0) sh->g = -1;
-    }
-    gsync();
-#pragma unroll
-    for (int w = 0; w < NW; ++w) Rmax = max(Rmax, sh->rmax[w]);
-  }
   const float u = a.uniforms[static_cast<size_t>(b) * a.gamma + a.k];
   int y = 0;
-  if (Rmax == INT_MIN || !(u >= 0.f && u < 1.f)) {  // the same verdict in every warp of the group
-    if (lane == 0 && gw == 0) set_status(a.status, DSPARK_ERR_BAD_DATA);
+  if (Rmax == INT_MIN || !(u >= 0.f && u < 1.f)) {
+    if (lane == 0) set_status(a.status, DSPARK_ERR_BAD_DATA);
   } else {
     const ff S = Rl == INT_MIN ? ff{0.f, 0.f} : ff_scale(Sl, pow2_nonpos(Rl - Rmax));
     const bool has = S.hi > 0.f;
-    const ff loc = warp_incl_scan_ff(S, lane);
-    ff off{0.f, 0.f}, Z;
-    if constexpr (NW > 1) {
-      if (lane == 31) sh->tot[gw] = loc;
-      gsync();
-      // warp w starts at off_w = (...(tot_0 + tot_1) + ...) + tot_{w-1}
-      ff run{0.f, 0.f};
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        if (w == gw) off = run;
-        run = ff_add(run, sh->tot[w]);
-      }
-      Z = ff{0.f, 0.f};
-#pragma unroll
-      for (int w = 0; w < NW; ++w) Z = ff_add(Z, sh->tot[w]);
-    } else {
-      Z = shfl_ff(loc, 31);
-    }
-    const ff incl = ff_add(off, loc);
+    const ff incl = warp_incl_scan_ff(S, lane);
+    const ff Z = shfl_ff(incl, 31);
     const ff prev = shfl_up_ff(incl, 1);
-    const ff excl = lane > 0 ? prev : off;
+    const ff excl = lane > 0 ? prev : ff{0.f, 0.f};
     const ff target = ff_mul(ff{u, 0.f}, Z);
     const uint32_t own =
         __ballot_sync(0xFFFFFFFFu, has && ff_cmp(excl, target) <= 0 && ff_cmp(target, incl) < 0);
@@ -501,25 +461,12 @@ __device__ __forceinline__ void draw_request(const DraftPickArgs& a, int b, int 
         C = Clast;
       }
       before = C;
-      if constexpr (NW > 1) {
-        sh->g = gs;
-        sh->before = before;
-      }
     }
-    int g;
-    ff s_before;
-    if constexpr (NW > 1) {
-      gsync();
-      g = sh->g;
-      s_before = sh->before;
-    } else {
-      const int ol = own ? __ffs(own) - 1 : 0;
-      g = own ? __shfl_sync(0xFFFFFFFFu, gs, ol) : -1;
-      s_before = shfl_ff(before, ol);
-    }
-    if (g >= 0 && gw == 0) y = draw_in_tile<kCoherent>(a, b, g, s_before, target, Rmax, lane);
+    const int ol = own ? __ffs(own) - 1 : 0;
+    const int g = own ? __shfl_sync(0xFFFFFFFFu, gs, ol) : -1;
+    const ff s_before = shfl_ff(before, ol);
+    if (g >= 0) y = draw_in_tile<kCoherent>(a, b, g, s_before, target, Rmax, lane);
   }
-  if (gw != 0) return;
   publish_token(a, b, y, lane);
 }
 
@@ -682,7 +629,7 @@ __device__ __forceinline__ void draw_ranges(const DraftPickArgs& a, int b, int l
 __global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickArgs a) {
   const int b = blockIdx.x * kPickWarps + (threadIdx.x >> 5);
   if (b >= a.B) return;  // whole warps only
-  draw_request<false, 1>(a, b, 0, threadIdx.x & 31, nullptr, 0);
+  draw_request<false>(a, b, threadIdx.x & 31);
 }
 
 
