@@ -331,7 +331,8 @@ int dspark_verify_rates(const void* target_logits, const void* draft_logits,
  * runs one such wait on a condition that never comes true, in one CTA:
  *   which 0  the ring waits of the pipelines: an mbarrier that no copy and no
  *            thread completes;
- *   which 1  the drafter's grid barrier: two CTAs expected in a grid of one;
+ *   which 1  the drafter's barrier among the CTAs of a request tile: two CTAs
+ *            expected in a grid of one;
  *            sync_words = 8 bytes of caller device memory, zeroed before the
  *            call (left holding one arrival).
  * The kernel records DSPARK_ERR_TIMEOUT in *device_status (if it holds

@@ -76,8 +76,8 @@ struct DraftBars {
   uint64_t acc_full[2], acc_empty[2];
   uint64_t st_ready[2];  // a group's rows are in shared memory, ready to store
   uint64_t mma_done;
-  uint64_t epi_done;     // k_draft_block: the CTA's epilogue warps reached a grid barrier
-  uint64_t step_go;      // k_draft_block: the grid barrier was crossed
+  uint64_t epi_done;     // k_draft_block: the CTA's epilogue warps reached the tile barrier
+  uint64_t step_go;      // k_draft_block: the tile barrier was crossed
   uint32_t tmem_base;
 };
 static_assert(sizeof(DraftBars) <= 512, "barrier block");
@@ -642,19 +642,21 @@ __global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickA
 // kernel: the roles stay alive across the positions, so
 // the producers stream W2 and U for position after position (the next
 // position's tiles load while the current one draws), the tensor memory and
-// the barriers stay set up, and the draws run inside the kernel between two
-// grid barriers (every CTA's statistics and rows of position k are written
-// before any warp draws; every G row of position k+1 is written before any CTA
-// loads it: each drawing warp publishes its request's row with a flag, and a
-// CTA waits only for its own rows; the statistics alternate between two
-// buffers, so a CTA already writing position k+1's may not overwrite what a
-// slower one still reads). Launched cooperatively (every CTA resident, one per
+// the barriers stay set up, and the draws run inside the kernel after a
+// barrier among the CTAs of each request tile (every statistic, range mass and
+// row of the tile's requests at position k is written before any warp draws
+// one of them; every G row of position k+1 is written before any CTA loads it:
+// each drawing warp publishes its request's token with a flag, and a CTA waits
+// only for its own rows; statistics and masses alternate between two buffers,
+// so a CTA already writing position k+1's may not overwrite what a slower one
+// still reads). Launched cooperatively (every CTA resident, one per
 // SM), so no wait can be on a CTA that is not running; every spin is bounded.
 
 // A diagnostic of the bounded waits: one thread runs a wait whose condition
 // never comes true -- which 0: wait_or_flag on an mbarrier that no copy or
 // thread completes (the waits of the pipelines' rings); which 1: grid_barrier
-// for two CTAs in a grid of one (the drafter's grid barrier) -- and the wait
+// for two CTAs in a grid of one (the drafter's barrier among the CTAs of a
+// request tile) -- and the wait
 // gives up, writes DSPARK_ERR_TIMEOUT to *status and the kernel returns.
 __global__ void k_wait_selftest(int which, uint32_t* sync, int32_t* status) {
   __shared__ uint64_t bar;
@@ -829,7 +831,7 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
     const int b = m_tile * kDM + m;
     const bool row_ok = b < a.B;
     const bool leader = (warp == 2 + 4 * grp) && lane == 0;
-    const bool syncer = warp == 2 && lane == 0;  // takes part in the grid barriers
+    const bool syncer = warp == 2 && lane == 0;  // takes part in the tile barriers
     const uint64_t pol_out = policy_evict_first();
     uint32_t gen = 0;
     // the CTAs of one request tile synchronise among themselves: a position's
@@ -842,8 +844,9 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
     int jg = 0;        // tiles this group has finished (all positions)
     int uses = 0;      // epi_done / step_go phases used so far
     bool ok = true;
-    // a grid barrier: the CTA's eight warps report, one thread crosses, all go on
-    auto cta_grid_sync = [&]() {
+    // the request tile's barrier: the CTA's eight warps report, one thread
+    // crosses with the tile's other CTAs, all go on
+    auto tile_barrier = [&]() {
       if (lane == 0) mbar_arrive(&bars->epi_done);
       bool good = true;
       if (syncer) {
@@ -982,7 +985,7 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
         asm volatile("fence.proxy.async.global;" ::: "memory");
       }
       __threadfence();
-      if (!cta_grid_sync()) {
+      if (!tile_barrier()) {
         ok = false;
         break;
       }
