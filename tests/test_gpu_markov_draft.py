@@ -68,6 +68,7 @@ def compare_chains(L_gpu, x_gpu, ref, requests):
     (3, 2, 1032, 64, 1.0),       # the last tile holds 8 tokens
     (257, 2, 2048, 192, 2.0),    # three request tiles, rank 192
     (40, 16, 20000, 256, 0.7),   # the full block length
+    (150, 4, 30000, 128, 0.9),   # two request tiles, 3 or 4 vocabulary tiles per CTA's range
     (24, 8, 6000, 128, 0.05),    # cold: the draws nearly argmax
     (24, 8, 6000, 128, 25.0),    # hot: the draws nearly uniform over the tiles
 ])
