@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verif
   pdl_trigger();
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t carry;
+  __shared__ int32_t sh_start[1025];  // this chunk's row starts (and the chunk's end)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     *status = DSPARK_OK;
@@ -128,26 +129,34 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verif
       warp_tot[lane] = w;  // inclusive over warps
     }
     __syncthreads();
+    // (past the batch cnt = 0, so a thread's start is the chunk's end)
     const int before = carry + (warp ? warp_tot[warp - 1] : 0) + incl - cnt;
     if (r < B) ws.req_row_start[r] = before;
+    sh_start[tid] = before;
     __syncthreads();
-    if (tid == 0) carry += warp_tot[31];
+    if (tid == 0) {
+      carry += warp_tot[31];
+      sh_start[1024] = carry;
+    }
     __syncthreads();
+    // the chunk's row list: one warp per request, lanes over its rows
+    // (coalesced stores), the starts from shared memory
+    const int nb = B - base < 1024 ? B - base : 1024;
+    for (int q = warp; q < nb; q += 32) {
+      const int rq = base + q;
+      const int start = sh_start[q], end = sh_start[q + 1];
+      if (end == start) continue;  // invalid request: nothing to read
+      const int ell = (end - start - 1) / 2;
+      const long long tb = toff ? toff[rq] : (long long)rq * (gamma + 1);
+      const long long db = doff ? doff[rq] : (long long)rq * gamma;
+      for (int i = lane; i < end - start; i += 32)
+        ws.row_list[start + i] = i <= ell ? (tb + i) << 1 : ((db + i - ell - 1) << 1) | 1;
+    }
+    __syncthreads();  // sh_start is rewritten by the next chunk
   }
   if (tid == 0) {
     ws.req_row_start[B] = carry;
     ws.hdr->total_rows = carry;
-  }
-  __syncthreads();
-  // the row list: one warp per request, lanes over its rows (coalesced stores)
-  for (int r = warp; r < B; r += 32) {
-    const int start = ws.req_row_start[r], end = ws.req_row_start[r + 1];
-    if (end == start) continue;  // invalid request: nothing to read
-    const int ell = (end - start - 1) / 2;
-    const long long tb = toff ? toff[r] : (long long)r * (gamma + 1);
-    const long long db = doff ? doff[r] : (long long)r * gamma;
-    for (int i = lane; i < end - start; i += 32)
-      ws.row_list[start + i] = i <= ell ? (tb + i) << 1 : ((db + i - ell - 1) << 1) | 1;
   }
 }
 
