@@ -524,19 +524,35 @@ __device__ __forceinline__ bool vec_weight_sum(const uint4& qt, const uint4& qd,
   float zt[E], zd[E];
   unpack_vec<Tin>(qt, zt);
   if constexpr (MODE != kModeTarget) unpack_vec<Tin>(qd, zd);
+  // The exponents of a token's target and draft terms (or of two target
+  // terms) go through one two-lane FMA chain: each lane rounds exactly as
+  // fmaf does, so the terms are bitwise those of the scalar form
+  // (exp_term: fma(z, c_lo, fma(z, c_hi, nK)); the draft side then adds E_lo).
+  const float2 chi = make_float2(ep.c_hi, ep.c_hi), clo = make_float2(ep.c_lo, ep.c_lo);
   float s = 0.f, emax = 0.f;
+  if constexpr (MODE == kModeTarget) {
+    const float2 k2 = make_float2(w.nK, w.nK);
 #pragma unroll
-  for (int i = 0; i < E; ++i) {
-    const float e = exp_term(zt[i], w.nK, ep);
-    if constexpr (MODE == kModeResidual) {
-      const float edv = ex2_approx(fmaf(zd[i], ep.c_lo, fmaf(zd[i], ep.c_hi, w.E_hi)) + w.E_lo);
-      emax = fmaxf(emax, e);
-      s += fmaxf(e - edv, 0.f);
-    } else if constexpr (MODE == kModeMin) {
-      const float edv = ex2_approx(fmaf(zd[i], ep.c_lo, fmaf(zd[i], ep.c_hi, w.E_hi)) + w.E_lo);
-      s += fminf(e, edv);
-    } else {
-      s += e;
+    for (int i = 0; i < E; i += 2) {
+      const float2 z2 = make_float2(zt[i], zt[i + 1]);
+      const float2 a = __ffma2_rn(z2, clo, __ffma2_rn(z2, chi, k2));
+      s += ex2_approx(a.x);
+      s += ex2_approx(a.y);
+    }
+  } else {
+    const float2 k2 = make_float2(w.nK, w.E_hi);
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const float2 z2 = make_float2(zt[i], zd[i]);
+      const float2 a = __ffma2_rn(z2, clo, __ffma2_rn(z2, chi, k2));
+      const float e = ex2_approx(a.x);
+      const float edv = ex2_approx(a.y + w.E_lo);
+      if constexpr (MODE == kModeResidual) {
+        emax = fmaxf(emax, e);
+        s += fmaxf(e - edv, 0.f);
+      } else {
+        s += fminf(e, edv);
+      }
     }
   }
   sum = s;
