@@ -67,6 +67,10 @@ def _setup(lib):
     lib.oracle_schedule.argtypes = [
         ctypes.POINTER(ctypes.c_float), c_f64p, ctypes.c_int64, ctypes.c_int32,
         ctypes.c_int32, ctypes.c_int32, c_i32p, c_f64p, c_i64p, c_i32p]
+    lib.oracle_schedule_path.restype = ctypes.c_int
+    lib.oracle_schedule_path.argtypes = [
+        ctypes.POINTER(ctypes.c_float), c_f64p, ctypes.c_int64, ctypes.c_int32,
+        ctypes.c_int32, c_i64p, c_f64p, c_i64p]
     lib.oracle_acceptance.restype = ctypes.c_int
     lib.oracle_acceptance.argtypes = [
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, c_i32p, ctypes.c_double, ctypes.c_int32,
@@ -193,6 +197,25 @@ def schedule(confidences, step_time, early_stop=True, lib=None):
         raise OracleError(f"oracle_schedule returned {rc}")
     return {"verify_len": ell, "theta_best": theta.value, "n_admitted": n_adm.value,
             "near_ties": ties.value}
+
+
+def schedule_path(confidences, step_time, lib=None):
+    """Algorithm 1's greedy admission path without the break. Returns dict:
+    order [|E|] (flattened index r*gamma + j - 1 of each candidate in admission
+    order) and theta [|E| + 1] (Theta after the first n admissions)."""
+    lib = lib or load()
+    c = np.ascontiguousarray(confidences, dtype=np.float32)
+    R, gamma = c.shape
+    T = np.ascontiguousarray(step_time, dtype=np.float64)
+    order = np.zeros(R * gamma, np.int64)
+    theta = np.zeros(R * gamma + 1, np.float64)
+    nE = ctypes.c_int64(0)
+    rc = lib.oracle_schedule_path(_ptr(c, ctypes.c_float), _ptr(T, ctypes.c_double), T.shape[0],
+                                  R, gamma, _ptr(order, ctypes.c_int64),
+                                  _ptr(theta, ctypes.c_double), ctypes.byref(nE))
+    if rc != 0:
+        raise OracleError(f"oracle_schedule_path returned {rc}")
+    return {"order": order[:nE.value], "theta": theta[:nE.value + 1]}
 
 
 def acceptance(target_logits, draft_logits, verify_len, temperature, gamma,

@@ -470,6 +470,61 @@ int oracle_schedule(const float* confidences, const double* step_time,
 }
 
 /*
+ * The greedy admission path of Algorithm 1 [P-3.2.2, P2-Alg1], written out in
+ * full for a comparison that has to judge another implementation's stopping
+ * point: the candidates of E in the loop's order and Theta after each
+ * admission, with no break.
+ *   order[i]  : flattened index r*gamma + (j-1) of the (i+1)-th candidate
+ *   theta[n]  : Theta after admitting the first n candidates, n = 0..|E|
+ *               (theta[0] = R / T(R), the loop's initial Theta_best)
+ * Both arrays need room for R*gamma (+1) entries; *n_candidates = |E|. The
+ * arithmetic is oracle_schedule's, step for step, so theta[n] equals the Theta
+ * that loop compares at its n-th admission bit for bit.
+ */
+int oracle_schedule_path(const float* confidences, const double* step_time,
+                         int64_t n_profile, int32_t R, int32_t gamma,
+                         int64_t* order, double* theta, int64_t* n_candidates) {
+  if (!confidences || !step_time || !order || !theta || !n_candidates || R < 1 || gamma < 1)
+    return ORACLE_ERR_ARG;
+  if (n_profile < (int64_t)R * (gamma + 1) + 1) return ORACLE_ERR_ARG;
+  for (int64_t i = 0; i < (int64_t)R * gamma; ++i) {
+    const float c = confidences[i];
+    if (!(c >= 0.0f && c <= 1.0f)) return ORACLE_ERR_DATA;
+  }
+  const int64_t n = (int64_t)R * gamma;
+  double* a = (double*)malloc(sizeof(double) * (size_t)n);
+  candidate* E = (candidate*)malloc(sizeof(candidate) * (size_t)n);
+  if (!a || !E) {
+    free(a);
+    free(E);
+    return ORACLE_ERR_NOMEM;
+  }
+  survival_products(confidences, R, gamma, a);
+  int64_t nE = 0;
+  for (int64_t i = 0; i < n; ++i)
+    if (a[i] > 0.0) {
+      E[nE].a = a[i];
+      E[nE].flat = i;
+      ++nE;
+    }
+  qsort(E, (size_t)nE, sizeof(candidate), candidate_cmp);
+
+  int64_t Bsz = R;
+  double tau = (double)R;
+  theta[0] = tau / step_time[Bsz];
+  for (int64_t i = 0; i < nE; ++i) {
+    order[i] = E[i].flat;
+    Bsz += 1;
+    tau += E[i].a;
+    theta[i + 1] = tau / step_time[Bsz];
+  }
+  *n_candidates = nE;
+  free(a);
+  free(E);
+  return ORACLE_OK;
+}
+
+/*
  * Dynamic top-K admission of the production scheduler ("DSpark: Confidence-
  * Scheduled Speculative Decoding with Semi-Autoregressive Generation", section
  * 5.2, "Hardware-Aware Prefix Scheduler in Practice"). The candidates are

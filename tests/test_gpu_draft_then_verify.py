@@ -53,12 +53,13 @@ def test_draft_then_verify(dev, B, gamma, V, r, T):
     gx = dr["draft_tokens"].cpu().numpy()
     acc = out["accepted_len"].cpu().numpy()
     em = out["emitted_tokens"].cpu().numpy()
-    compared = 0
+    # every request compared; a difference only where the oracle flags a near
+    # tie in that request's draft or verification, and at most one such request
+    differ = 0
     for b in range(B):
-        if draft_tie[b] or verify_tie[b]:
-            continue
-        compared += 1
-        np.testing.assert_array_equal(gx[b], od["tokens"][b])
-        assert acc[b] == ov["accepted_len"][b], b
-        np.testing.assert_array_equal(em[b], ov["emitted"][b])
-    assert compared >= B - 2
+        same = (np.array_equal(gx[b], od["tokens"][b]) and acc[b] == ov["accepted_len"][b]
+                and np.array_equal(em[b], ov["emitted"][b]))
+        if not same:
+            assert draft_tie[b] or verify_tie[b], (b, gx[b], od["tokens"][b], acc[b], em[b])
+            differ += 1
+    assert differ <= 1, differ

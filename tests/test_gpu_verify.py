@@ -1,8 +1,9 @@
 """GPU parity of dspark_verify against the CPU oracle.
 
 Bar: accepted lengths and emitted tokens bit-exact, except requests where the
-oracle flags a near tie (a uniform within 1e-6 of its threshold); probabilities
-within 1e-5 absolute. Sizes span several 8 KB tiles with ragged tails, both
+oracle flags a near tie (a uniform within 1e-6 of its threshold), and those
+actual disagreements no more than 1e-4 of the ratio tests plus draws;
+probabilities within 1e-5 absolute. Sizes span several 8 KB tiles with ragged tails, both
 load paths (bulk-copy for 16-byte-aligned rows, plain loads otherwise), both
 dtypes, dense and ragged layouts, and the five named workloads at full size.
 """
@@ -210,22 +211,26 @@ def test_busy_device_gives_the_same_outputs(dev):
 # ---------------------------------------------------------------------------
 # the named workloads at full size (bench launch configuration)
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("name,sample", [
-    ("b64_g16_v151936_bf16", None),
-    ("b256_g16_v129280_bf16", None),
-    ("ragged_b1024_g16_v151936_f32", 96),
+@pytest.mark.parametrize("name", [
+    "b64_g16_v151936_bf16",
+    "b256_g16_v129280_bf16",
+    "ragged_b1024_g16_v151936_f32",
 ])
-def test_full_size_workloads(dev, name, sample):
+def test_full_size_workloads(dev, name):
+    """Every request of the named workload against the oracle. Besides the
+    element-wise bar, the requests whose outputs actually differ at a flagged
+    near tie stay within 1e-4 of the ratio tests plus draws (compare())."""
     vi = workloads.make_config(name, device=dev)
     out = run(vi)
-    rng = np.random.default_rng(0)
-    idx = np.arange(vi.B) if sample is None else np.sort(rng.choice(vi.B, sample, replace=False))
+    idx = np.arange(vi.B)
     ref = oracle_on_requests(vi, idx)
     st = compare(out, ref, vi, idx)
     assert st["prob_max_rel_err"] <= PROB_RTOL_QUALITY, st
-    # near ties stay at or below 1e-4 of the decisions; a decision is one ratio
-    # test taken or one comparison of the inverse-CDF scan (y + 1 per draw)
+    assert st["excused"] <= st["mismatch_budget"], st
+    # the GPU's own near-tie count, per decision counted both ways: per ratio
+    # test + draw, and per comparison taken (each inverse-CDF scan counts y + 1)
     ties = int(out["near_tie_count"].item())
     n = near_tie_budget(out, vi)
     assert ties <= max(1, 1e-4 * n["decisions"]), (ties, n)
-    print(name, st, "gpu near ties", ties, n)
+    print(name, st, "gpu near ties", ties, "per (ratio test + draw)",
+          ties / (n["ratio_tests"] + n["draws"]), "per comparison", ties / n["decisions"])

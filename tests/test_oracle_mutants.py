@@ -12,7 +12,7 @@ import scipy.special
 
 import oracle
 from tests._law import emitted_law, first_token_law, softmax
-from tests._sched import exhaustive_best
+from tests._sched import exhaustive_best, greedy_order, lengths_of_prefix, theta_of
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "dspark_oracle.c")
 
@@ -35,8 +35,13 @@ MUTANTS = {
                        "if (x->a > y->a) return 1;\n  if (x->a < y->a) return -1;"),
     "survival_not_cumulative": ("prod *= (double)confidences[(int64_t)r * gamma + j];",
                                 "prod = (double)confidences[(int64_t)r * gamma + j];"),
-    "batch_not_counted": ("    Bsz += 1;\n", "\n"),
-    "anchor_token_dropped": ("double tau = (double)R;", "double tau = 0.0;"),
+    # the scheduler and its written-out admission path take the same steps, so
+    # these two mistakes are planted in both (two occurrences each)
+    "batch_not_counted": ("    Bsz += 1;\n", "\n", 2),
+    "anchor_token_dropped": ("double tau = (double)R;", "double tau = 0.0;", 2),
+    "path_theta_not_cumulative": ("theta[i + 1] = tau / step_time[Bsz];",
+                                  "theta[i + 1] = (R + E[i].a) / step_time[Bsz];"),
+    "path_order_off_by_one": ("order[i] = E[i].flat;", "order[i] = E[i].flat + 1;"),
     "draft_embedding_from_w2": ("a[j] = bf16_to_double(W1[(int64_t)prev * r + j]);",
                                 "a[j] = bf16_to_double(W2t[(int64_t)prev * r + j]);"),
     "draft_projection_from_w1": ("const uint16_t* col = W2t + v * r;",
@@ -99,6 +104,14 @@ def check_schedule(lib):
         s = oracle.schedule(conf, T, early_stop=True, lib=lib)
         best, _ = exhaustive_best(conf, T)
         assert abs(s["theta_best"] - best) <= 1e-12 * best
+        # the written-out admission path: the independent order, and Theta of
+        # every prefix from the objective's definition
+        p = oracle.schedule_path(conf, T, lib=lib)
+        order = greedy_order(conf)
+        assert [(int(f // g), int(f % g) + 1) for f in p["order"]] == [(r, j) for r, j, _ in order]
+        for k in range(len(order) + 1):
+            ell = lengths_of_prefix(p["order"], k, R, g)
+            assert abs(p["theta"][k] - theta_of(ell, conf, T)) <= 1e-12 * p["theta"][k]
 
 
 def _bits(vals):
@@ -173,9 +186,10 @@ def test_unmodified_oracle_passes_all_checks():
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_mutant_is_caught(name, tmp_path):
-    old, new = MUTANTS[name]
+    old, new, *count = MUTANTS[name]
+    count = count[0] if count else 1
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    assert src.count(old) == count, f"mutation anchor for {name} not found {count} time(s)"
     path = tmp_path / "mutant.c"
     path.write_text(src.replace(old, new))
     lib = oracle.load(oracle.build(str(path), str(tmp_path / "libmutant.so")))

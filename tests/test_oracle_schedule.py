@@ -94,3 +94,54 @@ def test_scheduled_workload_is_sane():
     # flat profile: every candidate is admitted
     s2 = oracle.schedule(conf, np.full(R * (g + 1) + 1, 4.0), early_stop=True)
     assert np.all(s2["verify_len"] == g)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_admission_path_matches_independent_statement(seed):
+    """The oracle's admission path equals the sorted order stated independently
+    (numpy stable sort of the survival products) and Theta recomputed from the
+    objective's definition at every prefix; the early-stop and global-search
+    results sit on that path where their rules put them."""
+    from tests._sched import judge_schedule, lengths_of_prefix
+    rng = np.random.default_rng(300 + seed)
+    R, g = int(rng.integers(1, 7)), int(rng.integers(1, 6))
+    conf = _confidences(rng, R, g)
+    T = (rng.uniform(1.0, 3.0, R * (g + 1) + 1) if seed % 2 else
+         _convex_profile(rng, R * (g + 1) + 1))
+    p = oracle.schedule_path(conf, T)
+    order = greedy_order(conf)
+    assert [(int(f // g), int(f % g) + 1) for f in p["order"]] == [(r, j) for r, j, _ in order]
+    for n in range(len(order) + 1):
+        ell = lengths_of_prefix(p["order"], n, R, g)
+        assert int(ell.sum()) == n
+        assert abs(p["theta"][n] - theta_of(ell, conf, T)) <= 1e-12 * p["theta"][n]
+    for es in (True, False):
+        s = oracle.schedule(conf, T, early_stop=es)
+        assert judge_schedule(s["verify_len"], s["theta_best"], p, R, g, early_stop=es) == 0
+        assert p["theta"][s["n_admitted"]] == s["theta_best"]
+
+
+def test_judge_rejects_a_wrong_stopping_point():
+    """The comparison the GPU tests use refuses a length vector one admission
+    short of or past the oracle's, and one that is not a prefix of its order."""
+    from tests._sched import judge_schedule, lengths_of_prefix
+    rng = np.random.default_rng(5)
+    R, g = 6, 4
+    conf = _confidences(rng, R, g)
+    N = np.arange(R * (g + 1) + 1, dtype=np.float64)
+    T = 2.0 + 0.05 * N + 0.004 * N * N   # stops at 5 of 20 candidates
+    p = oracle.schedule_path(conf, T)
+    s = oracle.schedule(conf, T, early_stop=True)
+    n = s["n_admitted"]
+    assert 0 < n < len(p["order"])
+    for m in (n - 1, n + 1):
+        with pytest.raises(AssertionError):
+            judge_schedule(lengths_of_prefix(p["order"], m, R, g), None, p, R, g)
+    bad = s["verify_len"].copy()
+    r = int(np.argmax(bad))
+    bad[r] -= 1
+    other = int(np.argmin(bad + (np.arange(R) == r) * 99))
+    bad[other] += 1
+    if not np.array_equal(bad, s["verify_len"]):
+        with pytest.raises(AssertionError):
+            judge_schedule(bad, None, p, R, g)
