@@ -46,7 +46,6 @@ extern "C" {
 #endif
 
 struct CUstream_st; /* cudaStream_t / CUstream */
-struct CUevent_st;  /* cudaEvent_t / CUevent */
 
 typedef enum {
   DSPARK_OK = 0,
@@ -323,26 +322,6 @@ int dspark_verify_rates(const void* target_logits, const void* draft_logits,
                         float* rates, int32_t* device_status, void* workspace,
                         size_t workspace_bytes, struct CUstream_st* stream);
 
-/*
- * dspark_wait_selftest -- a diagnostic of the bounded waits (no counterpart in
- * the paper). Every wait in the library gives up after about a second of the
- * device's global timer, writes DSPARK_ERR_TIMEOUT to the status word and lets
- * its kernel return, so that a lost completion never hangs the GPU. This call
- * runs one such wait on a condition that never comes true, in one CTA:
- *   which 0  the ring waits of the pipelines: an mbarrier that no copy and no
- *            thread completes;
- *   which 1  the drafter's barrier among the CTAs of a request tile: two CTAs
- *            expected in a grid of one;
- *            sync_words = 8 bytes of caller device memory, zeroed before the
- *            call (left holding one arrival).
- * The kernel records DSPARK_ERR_TIMEOUT in *device_status (if it holds
- * DSPARK_OK) after about a second and returns; later calls on the stream run
- * normally. Host errors: which not 0 or 1, device_status NULL, or (which 1)
- * sync_words NULL or not 8-byte aligned -> DSPARK_ERR_INVALID_ARG.
- */
-int dspark_wait_selftest(int32_t which, void* sync_words, int32_t* device_status,
-                         struct CUstream_st* stream);
-
 /* Size of the library-owned scratch array behind dspark_verify_static. */
 #define DSPARK_STATIC_WS_BYTES ((size_t)16u << 20)
 
@@ -362,7 +341,11 @@ int dspark_wait_selftest(int32_t which, void* sync_words, int32_t* device_status
  * libdspark. Every GPU that loads the library holds it until the process exits.
  * The first call on each device, with that device current, looks up the
  * array's device address (cudaGetSymbolAddress); make that first call before
- * any stream capture. No call allocates or frees memory.
+ * any stream capture. The address is kept per device and per context: after a
+ * device reset (cudaDeviceReset, or another library resetting the primary
+ * context) the next call finds a new context and looks the address up again,
+ * so make one call outside stream capture after a reset too. No call
+ * allocates or frees memory.
  *
  * Limits and sharing: a batch whose DSPARK_VERIFY_WS_BYTES(B, gamma, V)
  * exceeds DSPARK_STATIC_WS_BYTES is rejected with DSPARK_ERR_TOO_LARGE before
@@ -382,37 +365,6 @@ int dspark_verify_static(const void* target_logits, const void* draft_logits,
                          int32_t* accepted_len, int32_t* emitted_tokens,
                          float* probs_out, uint32_t* near_tie_count,
                          int32_t* device_status, struct CUstream_st* stream);
-
-/*
- * dspark_verify_timed -- dspark_verify with per-pass timing events (a
- * measurement aid; no counterpart in the paper).
- *
- * Does exactly the work of dspark_verify and also records, on `stream`:
- *   events[0] before the planning pass (k_plan),
- *   events[1] before the streaming pass (k_rowstats),
- *   events[2] before the decision pass (k_decide: ratio tests, residual sums
- *             and the draw),
- *   events[3] after it.
- * cudaEventElapsedTime(events[i], events[i+1]), after the caller's own
- * synchronisation, gives the duration of pass i. events points to 4 events
- * the caller created with timing enabled (cudaEventCreate) and still owns.
- * Recording between the passes stops a pass's launch from overlapping the end
- * of the previous one, so the three intervals add up to slightly more than a
- * dspark_verify call takes.
- *
- * Arguments, outputs and error behaviour are those of dspark_verify; a NULL
- * events pointer or event is DSPARK_ERR_INVALID_ARG.
- */
-int dspark_verify_timed(const void* target_logits, const void* draft_logits,
-                        const int32_t* draft_tokens, const int32_t* verify_len,
-                        const float* uniforms, float temperature, int32_t dtype,
-                        int32_t B, int32_t gamma, int32_t V,
-                        const int64_t* target_row_off, const int64_t* draft_row_off,
-                        int32_t* accepted_len, int32_t* emitted_tokens,
-                        float* probs_out, uint32_t* near_tie_count,
-                        int32_t* device_status, void* workspace,
-                        size_t workspace_bytes, struct CUstream_st* stream,
-                        struct CUevent_st** events);
 
 /*
  * dspark_draft_markov -- the sequential stage of the DSpark drafter with the
@@ -460,24 +412,6 @@ int dspark_draft_markov(const void* base_logits, const void* w1, const void* w2t
                         int32_t r, void* draft_logits, int32_t* draft_tokens,
                         int32_t* device_status, void* workspace,
                         size_t workspace_bytes, struct CUstream_st* stream);
-
-/*
- * dspark_draft_markov_timed -- dspark_draft_markov with timing events (a
- * measurement aid; no counterpart in the paper). Records events[0] before the
- * first gather, events[1] after it, and for k = 0..gamma-1 events[2+2k] after
- * position k's tensor-core kernel (k_draft_step) and events[3+2k] after its
- * draw (k_draft_pick): 2*gamma + 2 events created by the caller with timing
- * enabled. The recordings keep consecutive kernels from overlapping, so the
- * intervals add up to a little more than an untimed call. A NULL events
- * pointer or event is DSPARK_ERR_INVALID_ARG.
- */
-int dspark_draft_markov_timed(const void* base_logits, const void* w1, const void* w2t,
-                              const int32_t* anchors, const float* uniforms,
-                              float temperature, int32_t B, int32_t gamma, int64_t V,
-                              int32_t r, void* draft_logits, int32_t* draft_tokens,
-                              int32_t* device_status, void* workspace,
-                              size_t workspace_bytes, struct CUstream_st* stream,
-                              struct CUevent_st** events);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,7 @@ def _stale() -> bool:
         return True
     t = os.path.getmtime(LIB_PATH)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    deps.append(os.path.join(ROOT, "include", "dspark.h"))
+    deps += [os.path.join(ROOT, "include", h) for h in ("dspark.h", "dspark_testing.h")]
     deps.append(os.path.abspath(__file__))
     return any(os.path.getmtime(d) > t for d in deps)
 

@@ -10,7 +10,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/dspark.h"
+#include "../../include/dspark_testing.h"
 
 namespace dspark {
 

@@ -38,6 +38,8 @@
 //               segment holding the cut and picks the token.
 // Rows that are not 16-byte aligned take k_rowstats_plain (plain loads) and
 // k_decide (several CTAs per request: ratio tests, segment sums, the draw).
+#include <cuda.h>
+
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -1578,21 +1580,61 @@ namespace dspark {
 static __device__ __align__(256) unsigned char g_static_ws[DSPARK_STATIC_WS_BYTES];
 
 std::mutex g_static_mutex;
-void* g_static_ws_ptr[128];  // device address of g_static_ws, per device
+struct StaticWsAddress {
+  unsigned long long ctx_id;  // context the address belongs to (0: unknown)
+  void* ptr;
+};
+StaticWsAddress g_static_ws_ptr[128];  // device address of g_static_ws, per device
 
-// In host code g_static_ws names a host-side stand-in, not device memory: the
-// device address is looked up once per device, with that device current.
+// The unique ID of the calling thread's current context, or 0 when there is
+// none or the driver cannot say. IDs are never reused within a process, so a
+// context created after a device reset gets a new one even if it lands at the
+// same address.
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(fn);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// In host code g_static_ws names a host-side stand-in, not device memory. Its
+// device address is looked up with the device current, once per device and
+// context: a device reset (cudaDeviceReset, or another library resetting the
+// primary context) reloads the module at a new address, and the context ID
+// changes with it, so the lookup is repeated then. Without a context ID from
+// the driver every call looks the address up.
 int static_ws_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return DSPARK_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_static_mutex);
-  if (g_static_ws_ptr[dev] == nullptr) {
+  StaticWsAddress& c = g_static_ws_ptr[dev];
+  const unsigned long long id = current_context_id();
+  if (id == 0 || c.ctx_id != id || c.ptr == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || p == nullptr)
       return DSPARK_ERR_CUDA;
-    g_static_ws_ptr[dev] = p;
+    // the lookup makes the primary context current if none was
+    c.ctx_id = id ? id : current_context_id();
+    c.ptr = p;
   }
-  *out = g_static_ws_ptr[dev];
+  *out = c.ptr;
   return DSPARK_OK;
 }
 

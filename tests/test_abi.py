@@ -1,5 +1,5 @@
 """The C-ABI boundary, checked on the CPU: the library loads and exports every
-entry point include/dspark.h declares, the workspace macros agree with the
+entry point include/dspark.h and include/dspark_testing.h declare, the workspace macros agree with the
 Python binding's statement of them, and host-side argument checks reject bad
 calls before anything is launched."""
 import ctypes
@@ -14,6 +14,13 @@ from speculative_decoding_verification_41_gb300 import build as cuda_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "dspark.h")
+TESTING_HEADER = os.path.join(ROOT, "include", "dspark_testing.h")
+# the method's calls (the two of the verification path and the rows after
+# them) and the no-allocation variant; the testing header holds the rest
+METHOD_CALLS = {"dspark_verify", "dspark_schedule", "dspark_acceptance", "dspark_verify_rates",
+                "dspark_schedule_capacity", "dspark_schedule_topk", "dspark_schedule_threshold",
+                "dspark_draft_markov", "dspark_verify_static"}
+TESTING_CALLS = {"dspark_wait_selftest", "dspark_verify_timed", "dspark_draft_markov_timed"}
 
 
 @pytest.fixture(scope="module")
@@ -22,13 +29,18 @@ def lib():
     return binding.load()
 
 
-def declared_functions():
-    txt = open(HEADER).read()
+def declared_functions(headers=(HEADER, TESTING_HEADER)):
+    txt = "".join(open(h).read() for h in headers)
     return sorted(set(re.findall(r"^int\s+(dspark_\w+)\s*\(", txt, flags=re.M)))
 
 
 def test_header_declares_the_exported_calls():
     assert declared_functions() == sorted(binding.EXPORTED)
+
+
+def test_method_header_holds_only_the_methods_calls():
+    assert set(declared_functions((HEADER,))) == METHOD_CALLS
+    assert set(declared_functions((TESTING_HEADER,))) == TESTING_CALLS
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -43,7 +55,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_header_compiles_as_c_and_macros_match_binding(tmp_path):
     shapes = [(1, 1, 1), (4, 4, 32), (64, 16, 151936), (256, 16, 129280), (1024, 16, 151936),
               (7, 32, 1001), (0, 3, 5)]
-    src = ['#include <stdio.h>', '#include "dspark.h"', "int main(void) {"]
+    src = ['#include <stdio.h>', '#include "dspark.h"', '#include "dspark_testing.h"',
+           "int main(void) {"]
     for B, g, V in shapes:
         src.append(f'  printf("%zu %zu %zu\\n", DSPARK_VERIFY_WS_BYTES({B}, {g}, {V}), '
                    f'DSPARK_SCHEDULE_WS_BYTES({max(B, 1)}, {g}), '
