@@ -70,6 +70,9 @@ def parse():
     p.add_argument("--configs", default=",".join(OTHER_CONFIGS),
                    help="comma-separated other workloads measured beside the headline "
                         "(empty: none)")
+    p.add_argument("--only", default=None, choices=OTHER_CONFIGS,
+                   help="measure this one named workload alone and print its line (the "
+                        "headline is not run)")
     return p.parse_args()
 
 
@@ -466,6 +469,13 @@ def native_arm(args):
         if rank == 0:
             print(json.dumps(res), flush=True)
         return
+    if args.only:
+        peak, peak_src = measured_hbm_peak()
+        res = measure_config(args.only, args, dev, torch.cuda.current_stream(dev), peak, peak_src,
+                             want_cpu=rank == 0 and not args.no_cpu_baseline)
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
 
     if args.batch is None and rank == 0:
         vi = workloads.make_config(WORKLOAD, device=dev)
@@ -720,14 +730,7 @@ def native_arm(args):
     if names:
         del vi
         torch.cuda.empty_cache()
-    peaks = {}
-    try:
-        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-    except (OSError, ValueError):
-        pass
-    peak = peaks.get("hbm_gbs")
-    peak_src = "measured" if peak else "fallback"
-    peak = peak or 6800.0
+    peak, peak_src = measured_hbm_peak()
     for nm in names:
         configs[nm] = measure_config(nm, args, dev, stream, peak, peak_src,
                                      want_cpu=rank == 0 and not args.no_cpu_baseline)
@@ -908,8 +911,8 @@ def drafter_measure(args, dev, stream, rank, ws):
 # logit byte; valid only for the sources the kernel is built from (the headers
 # hashed below), as they were at the capture.
 TRAFFIC_CAPTURE = {
-    "sources_sha256": "dd984eed553e9d940bcb7688ba5843493337be2afc1004a3db7f96c362564593",
-    "dram_bytes": 273094912 + 3209728,  # read + write, one launch at B = 32
+    "sources_sha256": "118816c64befe0531575031839ed371c052b6efabab2261d94be4f2980d328a1",
+    "dram_bytes": 273095936 + 3616768,  # read + write, one launch at B = 32
     "logit_bytes": 273039360,
 }
 
@@ -928,6 +931,16 @@ def measured_traffic(logit_bytes: int):
     if not cap["sources_sha256"] or cap["sources_sha256"] != kernel_sources_sha256():
         return None
     return cap["dram_bytes"] / cap["logit_bytes"] * logit_bytes
+
+
+def measured_hbm_peak():
+    """The HBM peak of the GB300s (a measured copy, burst), else the
+    fallback figure; returns (GB/s, "measured" | "fallback")."""
+    try:
+        peak = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("hbm_gbs")
+    except (OSError, ValueError):
+        peak = None
+    return (peak, "measured") if peak else (6800.0, "fallback")
 
 
 def _nvtx(op: str, name: str = "") -> None:

@@ -97,6 +97,27 @@ def test_shapes_and_ties(dev, R, g):
         check(conf, T, dev)
 
 
+@pytest.mark.parametrize("kind", ["all_ones", "quantized", "one_outlier"])
+def test_many_equal_survival_values(dev, kind):
+    """512 x 16 with massive ties in the sort: every confidence 1 (all
+    survival values equal); confidences from four levels (thousands of
+    exactly equal products across requests); and a dense cluster of distinct
+    values near 1 beside one far outlier."""
+    R, g = 512, 16
+    rng = np.random.default_rng(99)
+    if kind == "all_ones":
+        conf = np.ones((R, g), np.float32)
+    elif kind == "quantized":
+        conf = rng.choice(np.array([0.5, 0.75, 0.9, 1.0], np.float32), size=(R, g))
+    else:
+        conf = (1.0 - rng.uniform(0, 1e-6, (R, g))).astype(np.float32)
+        conf[7, 0] = 1e-30
+    N = np.arange(R * (g + 1) + 1, dtype=np.float64)
+    for T in (workloads.step_time_profile(R * (g + 1) + 1), 2.0 + 0.001 * N,
+              np.full(R * (g + 1) + 1, 4.0)):
+        check(conf, T, dev)
+
+
 def test_flat_profile_admits_everything(dev):
     conf = workloads.make_confidences(256, 16, seed=1)
     ell, _ = check(conf, np.full(256 * 17 + 1, 4.0), dev)
