@@ -134,3 +134,52 @@ def first_token_law(law, V):
     for seq, w in law.items():
         p[seq[0]] += w
     return p
+
+
+def chisq_pvalue(samples, p, minimum=5.0):
+    """Chi-square p-value of integer samples against the law p (cells whose
+    expected count is below `minimum` pooled into one)."""
+    from scipy import stats
+    n = len(samples)
+    counts = np.bincount(np.asarray(samples, np.int64), minlength=len(p))
+    keep = np.asarray(p) * n >= minimum
+    obs = np.append(counts[keep], counts[~keep].sum())
+    exp = np.append(np.asarray(p)[keep] * n, np.asarray(p)[~keep].sum() * n)
+    if exp[-1] == 0:
+        obs, exp = obs[:-1], exp[:-1]
+    return float(stats.chisquare(obs, exp).pvalue)
+
+
+def one_position_trials(V, T, seed, n):
+    """Trials of one request with a block of one position: bf16 target rows 1
+    and 2, draft row 1, n draft tokens drawn from p_d by inverse CDF and n
+    uniform pairs, all seeded. Returns (zt [2, V] and zd [V] as bf16 bit
+    patterns, x [n], uniforms [n, 2], pt1, pt2, pd1 in float64)."""
+    import torch
+    from scipy import special
+    from speculative_decoding_verification_41_gb300 import workloads
+    rng = np.random.default_rng(seed)
+    zt = torch.tensor(2.0 * rng.standard_normal((2, V)), dtype=torch.float32).to(torch.bfloat16)
+    zd = torch.tensor(0.6 * zt[0].float().numpy() + rng.standard_normal(V),
+                      dtype=torch.float32).to(torch.bfloat16)
+    pt1 = special.softmax(zt[0].double().numpy() / T)
+    pt2 = special.softmax(zt[1].double().numpy() / T)
+    pd1 = special.softmax(zd.double().numpy() / T)
+    u_draft = workloads.philox_uniforms(seed, workloads.PURPOSE_DRAFT_SAMPLING, n).astype(np.float64)
+    x = np.minimum(np.searchsorted(np.cumsum(pd1), u_draft, side="right"), V - 1).astype(np.int32)
+    uni = workloads.philox_uniforms(seed, workloads.PURPOSE_VERIFY_UNIFORMS, 2 * n).reshape(n, 2)
+    bits = lambda t: t.view(torch.int16).numpy().view(np.uint16)
+    return bits(zt), bits(zd), x, uni, pt1, pt2, pd1
+
+
+def law_pvalues(acc, em, x, pt1, pt2, pd1):
+    """The three checks of a block of one position: the acceptance rate's
+    distance from sum min(p_t, p_d) in standard deviations, and the chi-square
+    p-values of the first emitted token against p_t of row 1 and of the bonus
+    (after an accepted token) against p_t of row 2."""
+    acc = np.asarray(acc)
+    em = np.asarray(em)
+    n = len(acc)
+    alpha = np.minimum(pt1, pd1).sum()
+    z = abs(acc.mean() - alpha) / np.sqrt(alpha * (1 - alpha) / n)
+    return z, chisq_pvalue(em[:, 0], pt1), chisq_pvalue(em[acc == 1, 1], pt2)

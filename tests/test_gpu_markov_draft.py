@@ -191,3 +191,22 @@ def test_bad_data_sets_status(dev, what):
     assert int(out["device_status"].item()) == 5
     tok = out["draft_tokens"].cpu().numpy()
     assert (tok >= 0).all() and (tok < 1024).all()
+
+
+def test_draw_law_is_the_emitted_rows_softmax(dev):
+    """The law of the device's draw itself: 16,384 requests with the same base
+    rows and anchor but their own uniforms draw x_1 from softmax(L_1 / T) of
+    the (shared) emitted row; chi-square against that law in float64."""
+    from scipy import special
+    from tests._law import chisq_pvalue
+    B, gamma, V, r, T = 16384, 1, 64, 64, 0.8
+    one = workloads.make_markov_draft(1, gamma, V, r, temperature=T, seed=31, device="cpu")
+    u = torch.from_numpy(workloads.philox_uniforms(31, workloads.PURPOSE_DRAFT_SAMPLING, B)
+                         .reshape(B, gamma))
+    d = workloads.MarkovDraftInputs(one.base_logits.repeat(B, 1, 1), one.w1, one.w2t,
+                                    one.anchors.repeat(B), u, T)
+    L, x = run_gpu(d, dev)
+    assert (L == L[0]).all()  # every request emits the same row
+    z = (L[0, 0].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    pv = chisq_pvalue(x[:, 0], special.softmax(z / T))
+    assert pv > 1e-4, pv

@@ -194,3 +194,27 @@ def test_mutant_is_caught(name, tmp_path):
     path.write_text(src.replace(old, new))
     lib = oracle.load(oracle.build(str(path), str(tmp_path / "libmutant.so")))
     assert _all_checks(lib), f"planted mistake '{name}' passed every pin"
+
+
+def test_law_check_has_power():
+    """The statistical check the GPU losslessness test applies passes on the
+    oracle and rejects a planted wrong residual (p_t in place of the normalised
+    max(0, p_t - p_d)) at the same trial count."""
+    from tests._law import law_pvalues, one_position_trials
+    V, T, n = 8, 1.0, 65535
+    zt, zd, x, uni, pt1, pt2, pd1 = one_position_trials(V, T, 1, n)
+    tl = np.tile(zt, (n, 1))
+    dl = np.tile(zd.reshape(1, V), (n, 1))
+    ell = np.ones(n, np.int32)
+    good = oracle.verify(tl, dl, x.reshape(n, 1), ell, uni, T, nthreads=4)
+    z, p1, p2 = law_pvalues(good["accepted_len"], good["emitted"], x, pt1, pt2, pd1)
+    assert z <= 5.0 and p1 > 1e-4 and p2 > 1e-4, (z, p1, p2)
+    old, new = MUTANTS["residual_uses_target_only"][:2]
+    import tempfile
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, "mutant.c")
+        open(path, "w").write(open(SRC).read().replace(old, new))
+        lib = oracle.load(oracle.build(path, os.path.join(tmp, "libmutant.so")))
+        bad = oracle.verify(tl, dl, x.reshape(n, 1), ell, uni, T, nthreads=4, lib=lib)
+    z, p1, p2 = law_pvalues(bad["accepted_len"], bad["emitted"], x, pt1, pt2, pd1)
+    assert p1 < 1e-4, p1
