@@ -63,6 +63,8 @@ constexpr uint32_t kIdesc = idesc_bf16_f32(kDM, kDN);
 static_assert(kDN == 128 && kDK == 64, "epilogue and statistics assume 128-token tiles");
 static_assert(kColG + DSPARK_DRAFT_MAX_RANK / 2 <= kTmemCols, "tensor memory columns");
 static_assert(kDraftSmem <= 232448, "shared memory of k_draft_step");
+// more than half of an SM's 228 KB: one CTA per SM (the single launch maps CTAs by SM id)
+static_assert(kDraftSmem > 233472 / 2, "one drafter CTA per SM");
 
 struct DraftStat {  // one (request, tile): sum over the tile of 2^(L_v * c - R)
   float s;
@@ -695,8 +697,22 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
   const DraftStepArgs& a = ba.s;
   const uint32_t sbase = smem_addr(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tile = blockIdx.x % a.n_m;
-  const int p = blockIdx.x / a.n_m;  // this CTA's vocabulary range in its request tile
+  // The CTAs that share a vocabulary range (one per request tile) read the
+  // same W2 tiles. In the single launch every CTA holds an SM of its own
+  // (one fits per SM), so when the grid covers every SM id the SM id itself
+  // is a permutation of the CTA indices: neighbouring ids (the two SMs of a
+  // TPC) then take the same range. Block indices are dealt across the GPU, so
+  // without this the pair of a range sits on two distant SMs (measured about
+  // 1% slower per block).
+  uint32_t cta = blockIdx.x;
+  if (kBlock) {
+    uint32_t smid, nsmid;
+    asm("mov.u32 %0, %%smid;" : "=r"(smid));
+    asm("mov.u32 %0, %%nsmid;" : "=r"(nsmid));
+    if (nsmid == gridDim.x && smid < nsmid) cta = smid;
+  }
+  const int m_tile = static_cast<int>(cta) % a.n_m;
+  const int p = static_cast<int>(cta) / a.n_m;  // this CTA's vocabulary range in its request tile
   const int lo = range_begin(p, a.n_tiles, a.per_m), hi = range_begin(p + 1, a.n_tiles, a.per_m);
   const int n_local = hi - lo;
   const int KC = a.r / kDK;
