@@ -429,7 +429,9 @@ def measure_config(name: str, args, dev, stream, peak: float, peak_src: str, wan
             "n_admitted": positions, "theta_best": float(sbuf.theta_best.item()),
             "equals_oracle": bool(np.array_equal(ell, ref_s["verify_len"])
                                   and ref_s["near_ties"] == 0),
-            "gpu_launches_per_step": 2}
+            # the scheduler's rank path (two launches) takes up to 6,144
+            # candidates, its block path (four) larger batches
+            "gpu_launches_per_step": 2 if sched.R * sched.gamma <= 6144 else 4}
     if want_cpu:
         cores = oracle.max_threads()
         h = vi.to("cpu")

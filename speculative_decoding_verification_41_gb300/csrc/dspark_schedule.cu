@@ -7,7 +7,7 @@
 // that order with Theta = tau * SPS(B) (SPS = 1/T), stop at the first
 // Theta <= Theta_best.
 //
-// Up to 16,384 candidates (two launches):
+// Up to 6,144 candidates (two launches, the rank path):
 //   k_sched_rank   every CTA forms all survival products a_{r,j} in shared
 //                  memory (multiplied left to right in double: bit-identical to
 //                  a sequential evaluation) and computes the global rank of a
@@ -26,9 +26,12 @@
 //                  among the first n* candidates of request r. The decisions
 //                  equal the quotient comparisons of the definition outside
 //                  the 1e-9 near-tie window, which is counted.
-// Beyond that, k_schedule does everything in one CTA: the same products, a
-// merge sort of the runs (pairwise merges by rank), a double block scan and a
-// double sweep.
+// Beyond that (four launches, the block path): the products and a sort of
+// each block of 1,024 candidates, every candidate ranked against the other
+// sorted blocks, the same sweep over tiles of 4,096 positions, and the
+// lengths from the ranks (k_sched_blocks, k_sched_merge, k_sched_sweep_tiled,
+// k_sched_lengths). The rank path's work grows with candidates x requests,
+// the block path's with candidates x blocks.
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -37,13 +40,13 @@
 
 namespace dspark {
 
-constexpr int kSchedThreads = 1024;
-constexpr int kSchedSmemMaxN = 8192;  // candidates kept in shared memory (24 B each)
 
 typedef unsigned long long u64;
 
 struct SchedWs {
   uint32_t* ties_scratch;
+  uint32_t* n_cand;  // block path: the number of candidates (a > 0)
+  int32_t* n_star;   // block path: the admitted count
   u64* keysA;  // bit patterns of non-negative doubles
   u64* keysB;
   int32_t* idxA;
@@ -51,34 +54,7 @@ struct SchedWs {
   int32_t* ell;
 };
 
-__device__ __forceinline__ double block_sum_excl(double v, double* sh, double& total) {
-  // exclusive prefix of v over the block (1024 threads), and the block total
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  double incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const double t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) sh[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    double w = sh[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const double t = __shfl_up_sync(0xFFFFFFFFu, w, o);
-      if (lane >= o) w += t;
-    }
-    sh[lane] = w;
-  }
-  __syncthreads();
-  const double before = (warp ? sh[warp - 1] : 0.0) + (incl - v);
-  total = sh[31];
-  __syncthreads();
-  return before;
-}
-
-// Scheduling modes shared by the sweep and the one-CTA path:
+// Scheduling modes shared by both sweeps:
 //   kModeStop     Algorithm 1: stop at the first Theta(n) <= Theta(n-1)
 //   kModeGlobal   section 5.2: no break; n* = the first maximum of Theta(n)
 //                 over n = 0..|E| (the capacity K of the next steps)
@@ -135,199 +111,6 @@ __device__ Cand block_excl_pick(const Cand& v, Cand* sh) {
   const Cand r = cand_pick(before, ex);
   __syncthreads();  // sh is free again
   return r;
-}
-
-__global__ void __launch_bounds__(kSchedThreads, 1)
-    k_schedule(const float* __restrict__ conf, const double* __restrict__ T, int R, int gamma,
-               int32_t* __restrict__ verify_len, double* theta_out, uint32_t* ties,
-               int32_t* status, SchedWs gws, int use_smem, int mode, const int32_t* K_in,
-               int32_t* K_out) {
-  pdl_wait();  // predecessor grid complete, its writes visible
-  pdl_trigger();
-  extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ double red[32];
-  __shared__ int red_i[32];
-  __shared__ int sh_n_break, sh_nE;
-  __shared__ unsigned sh_ties;
-  __shared__ Cand sh_cand[32];
-  __shared__ int sh_nstar;
-  const int n = R * gamma;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  u64* kA = gws.keysA;
-  u64* kB = gws.keysB;
-  int32_t* iA = gws.idxA;
-  int32_t* iB = gws.idxB;
-  if (use_smem) {
-    kA = reinterpret_cast<u64*>(smem);
-    kB = kA + n;
-    iA = reinterpret_cast<int32_t*>(kB + n);
-    iB = iA + n;
-  }
-  if (tid == 0) {
-    *status = DSPARK_OK;
-    if (ties) *ties = 0;
-    sh_n_break = INT_MAX;
-    sh_nE = 0;
-    sh_ties = 0;
-  }
-  __syncthreads();
-
-  // 1. prefix survival probabilities
-  for (int r = tid; r < R; r += kSchedThreads) {
-    // all of the request's loads are issued before the multiply chain
-    float cv[DSPARK_MAX_GAMMA];
-#pragma unroll
-    for (int j = 0; j < DSPARK_MAX_GAMMA; ++j)
-      cv[j] = j < gamma ? conf[static_cast<long long>(r) * gamma + j] : 0.f;
-    double prod = 1.0;
-#pragma unroll
-    for (int j = 0; j < DSPARK_MAX_GAMMA; ++j) {
-      if (j >= gamma) break;
-      float c = cv[j];
-      if (!(c >= 0.f && c <= 1.f)) {
-        set_status(status, DSPARK_ERR_BAD_DATA);
-        c = 0.f;
-      }
-      prod *= static_cast<double>(c);
-      kA[r * gamma + j] = static_cast<u64>(__double_as_longlong(prod));
-      iA[r * gamma + j] = r * gamma + j;
-    }
-    gws.ell[r] = 0;
-  }
-  // profile entries that can be looked up must be positive and finite
-  if (T)
-    for (int b = R + tid; b <= R * (gamma + 1); b += kSchedThreads)
-      if (!(T[b] > 0.0) || !isfinite(T[b])) set_status(status, DSPARK_ERR_BAD_DATA);
-  __syncthreads();
-
-  // 2. stable descending merge of the per-request runs
-  for (int L = gamma; L < n; L *= 2) {
-    for (int i = tid; i < n; i += kSchedThreads) {
-      const int a0 = (i / (2 * L)) * (2 * L);
-      const int b0 = min(a0 + L, n), b1 = min(a0 + 2 * L, n);
-      const u64 key = kA[i];
-      int dst;
-      if (i < b0) {  // left run: right-run elements strictly greater come first
-        int lo = b0, hi = b1;
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (kA[mid] > key) lo = mid + 1; else hi = mid;
-        }
-        dst = i + (lo - b0);
-      } else {       // right run: left-run elements greater or equal come first
-        int lo = a0, hi = b0;
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (kA[mid] >= key) lo = mid + 1; else hi = mid;
-        }
-        dst = a0 + (i - b0) + (lo - a0);
-      }
-      kB[dst] = key;
-      iB[dst] = iA[i];
-    }
-    __syncthreads();
-    u64* tk = kA; kA = kB; kB = tk;
-    int32_t* ti = iA; iA = iB; iB = ti;
-  }
-
-  // 3. number of candidates (a > 0 sort first) and tau(n) into kB
-  {
-    int cnt = 0;
-    for (int i = tid; i < n; i += kSchedThreads) cnt += kA[i] != 0ull;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
-    if (lane == 0) atomicAdd(&sh_nE, cnt);
-  }
-  __syncthreads();
-  const int nE = sh_nE;
-  const int chunk = (nE + kSchedThreads - 1) / kSchedThreads;
-  const int c0 = min(tid * chunk, nE), c1 = min(c0 + chunk, nE);
-  double local = 0.0;
-  for (int i = c0; i < c1; ++i) local += __longlong_as_double(static_cast<long long>(kA[i]));
-  double total;
-  const double before = block_sum_excl(local, red, total);
-  double run = static_cast<double>(R) + before;
-  double* tau = reinterpret_cast<double*>(kB);  // tau(i + 1) in the free buffer
-  for (int i = c0; i < c1; ++i) {
-    run += __longlong_as_double(static_cast<long long>(kA[i]));
-    tau[i] = run;
-  }
-  __syncthreads();
-
-  int n_star;
-  if (mode == kModeStop) {
-    // 4. first non-improving admission
-    int first = INT_MAX;
-    for (int m = 1 + tid; m <= nE; m += kSchedThreads) {
-      const double tau_m = tau[m - 1];
-      const double tau_p = m == 1 ? static_cast<double>(R) : tau[m - 2];
-      if (!(tau_m * T[R + m - 1] > tau_p * T[R + m])) first = min(first, m);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xFFFFFFFFu, first, o));
-    if (lane == 0) red_i[warp] = first;
-    __syncthreads();
-    if (warp == 0) {
-      int f = red_i[lane];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) f = min(f, __shfl_xor_sync(0xFFFFFFFFu, f, o));
-      if (lane == 0) sh_n_break = f;
-    }
-    __syncthreads();
-    const int n_break = sh_n_break;  // INT_MAX: every admission improved
-    n_star = n_break <= nE ? n_break - 1 : nE;
-    // near ties among the comparisons actually evaluated (steps 1..min(n_break, nE))
-    const int last = min(n_break, nE);
-    unsigned t = 0;
-    for (int m = 1 + tid; m <= last; m += kSchedThreads) {
-      const double tau_m = tau[m - 1];
-      const double tau_p = m == 1 ? static_cast<double>(R) : tau[m - 2];
-      const double tm = T[R + m], tp = T[R + m - 1];
-      // |Theta(m) - Theta(m-1)| <= eps Theta(m-1), multiplied through by T(R+m) T(R+m-1)
-      if (fabs(tau_m * tp - tau_p * tm) <= DSPARK_SCHED_TIE_REL * tau_p * tm) ++t;
-    }
-    t = warp_sum_u32(t);
-    if (lane == 0 && t) atomicAdd(&sh_ties, t);
-  } else if (mode == kModeGlobal) {
-    // 4'. first maximum of Theta over n = 0..|E|: chunk bests, their exclusive
-    // scan, then every admission against the best before it
-    const int gc = (nE + kSchedThreads - 1) / kSchedThreads;
-    const int g0 = min(tid * gc, nE), g1 = min(g0 + gc, nE);
-    Cand loc{0.0, 1.0, -1};
-    for (int m = g0 + 1; m <= g1; ++m) loc = cand_pick(loc, Cand{tau[m - 1], T[R + m], m});
-    Cand run = cand_pick(Cand{static_cast<double>(R), T[R], 0}, block_excl_pick(loc, sh_cand));
-    unsigned t = 0;
-    for (int m = g0 + 1; m <= g1; ++m) {
-      const Cand c{tau[m - 1], T[R + m], m};
-      if (fabs(c.tau * run.t - run.tau * c.t) <= DSPARK_SCHED_TIE_REL * run.tau * c.t) ++t;
-      run = cand_pick(run, c);
-    }
-    t = warp_sum_u32(t);
-    if (lane == 0 && t) atomicAdd(&sh_ties, t);
-    if (tid == kSchedThreads - 1) sh_nstar = run.m;  // the last chunk's run covers every position
-    __syncthreads();
-    n_star = sh_nstar;
-  } else {
-    int K = *K_in;
-    if (K < 0) {
-      if (tid == 0) set_status(status, DSPARK_ERR_BAD_DATA);
-      K = 0;
-    }
-    n_star = K < nE ? K : nE;
-  }
-  // 5. verify lengths: the admitted prefix of each request
-  for (int i = tid; i < n_star; i += kSchedThreads) {
-    const int id = iA[i];
-    atomicMax(&gws.ell[id / gamma], id % gamma + 1);
-  }
-  __syncthreads();
-  for (int r = tid; r < R; r += kSchedThreads) verify_len[r] = gws.ell[r];
-  if (tid == 0) {
-    if (ties && sh_ties) atomicAdd(ties, sh_ties);
-    if (theta_out && T)
-      *theta_out = n_star > 0 ? tau[n_star - 1] / T[R + n_star] : static_cast<double>(R) / T[R];
-    if (K_out) *K_out = n_star;
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -664,6 +447,474 @@ __global__ void __launch_bounds__(kRankThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Block path (any number of candidates; taken above 6,144 candidates, where
+// searching every request's run costs more than these four launches, and
+// wherever the rank path's shared memory does not hold every key):
+//   k_sched_blocks       one CTA per 1,024 candidates in flattened order: the
+//                        survival products of the requests overlapping them,
+//                        then a stable descending merge sort of the block.
+//   k_sched_merge        one CTA per block: a candidate's rank is its place in
+//                        its own block plus, for every other block, the number
+//                        of that block's candidates before it (binary search;
+//                        the other blocks pass through a ring of shared-memory
+//                        stages filled by asynchronous copies, four blocks per
+//                        step). The keys land at their ranks, and the rank of
+//                        every flattened index is kept for the lengths.
+//   k_sched_sweep_tiled  one CTA: the sweep of k_sched_sweep over tiles of
+//                        4,096 positions (the next tile copied in while the
+//                        current one is walked), stopping at the tile that
+//                        holds the first non-improving admission.
+//   k_sched_lengths      l_r = the number of request r's candidates whose
+//                        rank is below n*.
+// ---------------------------------------------------------------------------
+constexpr int kBlockKeys = 1024;
+constexpr int kMergeGroup = 4;                           // blocks searched per step
+constexpr int kMergeGroups = 3;                          // steps in flight
+constexpr int kMergeSmem = kMergeGroup * kMergeGroups * kBlockKeys * 8;  // 96 KB
+constexpr int kTilePer = 4;                              // positions per thread per tile
+constexpr int kSweepTile = kTilePer * kRankThreads;      // 4,096
+// two tiles of sorted values and of the profile slice
+constexpr int kTiledSmem = 2 * kSweepTile * 8 + 2 * (kSweepTile + 1) * 8;
+constexpr int kLengthThreads = 256;
+// candidates from which the block path replaces the rank path
+constexpr int kBlockPathMinN = 6145;
+
+__device__ __forceinline__ void cp_async8(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+
+// Blocks of kBlockKeys candidates (flattened index e = r*gamma + j): CTA b
+// forms a_{r,j} for the requests overlapping [b*1024, b*1024 + 1024), left to
+// right in double as everywhere, and sorts the block descending, equal values
+// in flattened order (a bottom-up merge: an element of a left run goes after
+// the right run's strictly larger values, one of a right run after the left
+// run's larger or equal ones). A request's own values never increase, so
+// with gamma a power of two the merge starts from the requests' runs. Writes
+// the sorted block (keys and flattened indices), a flag per request for a
+// confidence outside [0, 1] (from the block holding the request's first
+// candidate), and -- CTA 0 -- the status and the candidate counter.
+__global__ void __launch_bounds__(kBlockKeys, 1)
+    k_sched_blocks(const float* __restrict__ conf, int R, int gamma, SchedWs gws,
+                   int32_t* status) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  __shared__ u64 sh_k[2][kBlockKeys];
+  __shared__ int32_t sh_i[2][kBlockKeys];
+  const int n = R * gamma;
+  const int tid = threadIdx.x;
+  const int e0 = blockIdx.x * kBlockKeys;
+  const int m = min(kBlockKeys, n - e0);
+  if (blockIdx.x == 0 && tid == 0) {
+    *status = DSPARK_OK;
+    *gws.n_cand = 0u;
+  }
+  const int r_first = e0 / gamma, r_last = (e0 + m - 1) / gamma;
+  for (int r = r_first + tid; r <= r_last; r += kBlockKeys) {
+    float cv[DSPARK_MAX_GAMMA];
+#pragma unroll
+    for (int j = 0; j < DSPARK_MAX_GAMMA; ++j)
+      cv[j] = j < gamma ? conf[static_cast<long long>(r) * gamma + j] : 0.f;
+    bool bad = false;
+    double prod = 1.0;
+#pragma unroll
+    for (int j = 0; j < DSPARK_MAX_GAMMA; ++j) {
+      if (j >= gamma) break;
+      float c = cv[j];
+      if (!(c >= 0.f && c <= 1.f)) {
+        bad = true;
+        c = 0.f;
+      }
+      prod *= f2d_exact(c);
+      const int e = r * gamma + j;
+      if (e >= e0 && e < e0 + m) {
+        sh_k[0][e - e0] = static_cast<u64>(__double_as_longlong(prod));
+        sh_i[0][e - e0] = e;
+      }
+    }
+    if (r * gamma >= e0) gws.ell[r] = bad ? 1 : 0;
+  }
+  __syncthreads();
+  int src = 0;
+  // runs of gamma sit at multiples of gamma (1024 is a multiple of gamma)
+  const int L0 = (gamma & (gamma - 1)) == 0 ? gamma : 1;
+  for (int L = L0; L < m; L <<= 1) {
+    if (tid < m) {
+      const u64 x = sh_k[src][tid];
+      const int a0 = (tid / (2 * L)) * (2 * L);
+      const int b0 = min(a0 + L, m), b1 = min(a0 + 2 * L, m);
+      const u64* A = sh_k[src];
+      int dst;
+      if (tid < b0) {
+        int lo = b0, hi = b1;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (A[mid] > x) lo = mid + 1; else hi = mid;
+        }
+        dst = tid + (lo - b0);
+      } else {
+        int lo = a0, hi = b0;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (A[mid] >= x) lo = mid + 1; else hi = mid;
+        }
+        dst = a0 + (tid - b0) + (lo - a0);
+      }
+      sh_k[src ^ 1][dst] = x;
+      sh_i[src ^ 1][dst] = sh_i[src][tid];
+    }
+    __syncthreads();
+    src ^= 1;
+  }
+  if (tid < m) {
+    gws.keysA[e0 + tid] = sh_k[src][tid];
+    gws.idxA[e0 + tid] = sh_i[src][tid];
+  }
+}
+
+// Global ranks from the sorted blocks: block o < b holds smaller flattened
+// indices, so its values equal to x come first; block o > b contributes only
+// its larger values. Each CTA also checks a share of the requests' flags and
+// of the profile slice T(R..R(gamma+1)) (positive, finite), and adds its
+// block's candidates (a > 0) to the counter.
+__global__ void __launch_bounds__(kBlockKeys, 1)
+    k_sched_merge(const double* __restrict__ T, int R, int gamma, SchedWs gws,
+                  int32_t* status) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  extern __shared__ __align__(16) unsigned char smem[];
+  u64* ring = reinterpret_cast<u64*>(smem);  // [kMergeGroups * kMergeGroup][kBlockKeys]
+  const int n = R * gamma;
+  const int nb = (n + kBlockKeys - 1) / kBlockKeys;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  bool bad = false;
+  for (long long r = static_cast<long long>(b) * kBlockKeys + tid; r < R;
+       r += static_cast<long long>(nb) * kBlockKeys)
+    if (__ldcg(gws.ell + r)) bad = true;
+  if (T)
+    for (long long m = static_cast<long long>(b) * kBlockKeys + tid; m <= n;
+         m += static_cast<long long>(nb) * kBlockKeys) {
+      const u64 t = static_cast<u64>(__double_as_longlong(T[R + m]));
+      if ((t >> 63) || ((t >> 52) & 0x7FFull) == 0x7FFull || t == 0ull) bad = true;
+    }
+  if (bad) set_status(status, DSPARK_ERR_BAD_DATA);
+
+  const int e0 = b * kBlockKeys;
+  const int mine = min(kBlockKeys, n - e0);
+  const bool live = tid < mine;
+  const u64 x = live ? __ldcg(gws.keysA + e0 + tid) : 0ull;
+  const int id = live ? __ldcg(gws.idxA + e0 + tid) : 0;
+  const int cand = __syncthreads_count(live && x != 0ull);
+  if (tid == 0 && cand) atomicAdd(gws.n_cand, static_cast<uint32_t>(cand));
+
+  // the other blocks in visiting order: visit q is block q, or q + 1 from this
+  // block on; step s searches visits [s*G, s*G + G)
+  const int others = nb - 1;
+  const int steps = (others + kMergeGroup - 1) / kMergeGroup;
+  auto issue = [&](int s) {
+    if (s < steps) {
+      for (int g = 0; g < kMergeGroup; ++g) {
+        const int q = s * kMergeGroup + g;
+        if (q >= others) break;
+        const int o = q + (q >= b);
+        const int len = min(kBlockKeys, n - o * kBlockKeys);
+        const u64* srcp = gws.keysA + static_cast<size_t>(o) * kBlockKeys;
+        u64* dst = ring + static_cast<size_t>((s % kMergeGroups) * kMergeGroup + g) * kBlockKeys;
+        for (int v = tid; v < len / 2; v += kBlockKeys) cp_async16(dst + 2 * v, srcp + 2 * v);
+        if ((len & 1) && tid == 0) cp_async8(dst + len - 1, srcp + len - 1);
+        // a short (last) block is padded with zeros, which no candidate counts
+        for (int v = len + tid; v < kBlockKeys; v += kBlockKeys) dst[v] = 0ull;
+      }
+    }
+    cp_async_commit();  // empty groups complete at once
+  };
+#pragma unroll
+  for (int s = 0; s < kMergeGroups - 1; ++s) issue(s);
+  int rank = tid;
+  for (int s = 0; s < steps; ++s) {
+    issue(s + kMergeGroups - 1);  // the stages read at s - 1, released by its barrier
+    cp_async_wait<kMergeGroups - 1>();
+    __syncthreads();  // every thread's copies of step s have landed
+    if (live && x != 0ull) {
+      // per block, the number of its values >= x (earlier blocks: equal
+      // values come first) or >= x + 1 (later blocks); the keys are integers,
+      // the blocks descending and zero-padded to 1024, so a 10-step lift
+      // finds each count; the group's lifts run side by side
+      int pos[kMergeGroup];
+      u64 xq[kMergeGroup];
+      const u64* run[kMergeGroup];
+#pragma unroll
+      for (int g = 0; g < kMergeGroup; ++g) {
+        const int q = s * kMergeGroup + g;
+        pos[g] = 0;
+        xq[g] = q >= others ? ~0ull : (q < b ? x : x + 1ull);  // past the end: counts nothing
+        run[g] = ring + static_cast<size_t>((s % kMergeGroups) * kMergeGroup + g) * kBlockKeys;
+      }
+#pragma unroll
+      for (int step = kBlockKeys / 2; step >= 1; step >>= 1)
+#pragma unroll
+        for (int g = 0; g < kMergeGroup; ++g)
+          pos[g] += run[g][pos[g] + step - 1] >= xq[g] ? step : 0;
+#pragma unroll
+      for (int g = 0; g < kMergeGroup; ++g)
+        rank += pos[g] + (pos[g] == kBlockKeys - 1 && run[g][kBlockKeys - 1] >= xq[g]);
+    }
+    __syncthreads();  // step s's stages may be refilled
+  }
+  cp_async_wait<0>();
+  if (live) {
+    // the candidates (a > 0) take ranks 0..|E|-1 and their values land there;
+    // a zero value is no candidate: its rank only has to exceed any n*
+    if (x != 0ull) gws.keysB[rank] = x;
+    gws.idxB[id] = x != 0ull ? rank : INT_MAX;  // the rank of flattened index id
+  }
+}
+
+// The sweep of k_sched_sweep (same float-float arithmetic, comparisons and
+// near-tie counts) over tiles of kSweepTile positions, with tau and, for the
+// global search, the best admission so far carried from tile to tile; each
+// tile's sorted values and profile slice are copied into shared memory while
+// the one before is walked. The profile slice was checked by k_sched_merge.
+// Writes n* to the workspace header for k_sched_lengths.
+template <int MODE>
+__global__ void __launch_bounds__(kRankThreads, 1)
+    k_sched_sweep_tiled(const double* __restrict__ T, int R, int gamma, SchedWs gws,
+                        double* theta_out, uint32_t* ties, int32_t* status,
+                        const int32_t* K_in, int32_t* K_out) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  extern __shared__ __align__(16) unsigned char smem[];
+  u64* sh_key = reinterpret_cast<u64*>(smem);                                  // [2][kSweepTile]
+  double* sh_Tb = reinterpret_cast<double*>(smem + 2 * kSweepTile * 8);        // [2][kSweepTile + 1]
+  __shared__ ff sh_w[32];
+  __shared__ int sh_break;
+  __shared__ unsigned sh_ties;
+  __shared__ ff sh_carry, sh_tau_star;
+  __shared__ Cand sh_cand[32];
+  __shared__ Cand sh_best;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nE = static_cast<int>(__ldcg(gws.n_cand));
+  if (tid == 0) {
+    sh_break = INT_MAX;
+    sh_ties = 0;
+    sh_carry = ff{static_cast<float>(R), 0.f};
+    sh_tau_star = ff{static_cast<float>(R), 0.f};
+    if (MODE == kModeGlobal) sh_best = Cand{static_cast<double>(R), T[R], 0};
+  }
+  // tile t0's values and profile slice T(R + t0 + i), i = 0..len, into buffer p
+  auto fetch = [&](int t0, int p) {
+    const int len = min(kSweepTile, nE - t0);
+    u64* kd = sh_key + p * kSweepTile;
+    double* td = sh_Tb + p * (kSweepTile + 1);
+    const u64* ks = gws.keysB + t0;  // t0 is a multiple of kSweepTile: 16-byte aligned
+    for (int v = tid; v < len / 2; v += blockDim.x) cp_async16(kd + 2 * v, ks + 2 * v);
+    if ((len & 1) && tid == 0) cp_async8(kd + len - 1, ks + len - 1);
+    for (int i = tid; i <= len; i += blockDim.x) cp_async8(td + i, T + R + t0 + i);
+    cp_async_commit();
+  };
+  int n_star = 0;
+  if constexpr (MODE == kModeTopK) {
+    __syncthreads();
+    int K = *K_in;
+    if (K < 0) {
+      if (tid == 0) set_status(status, DSPARK_ERR_BAD_DATA);
+      K = 0;
+    }
+    n_star = K < nE ? K : nE;
+    if (theta_out && T) {  // tau(n*) over the first n* sorted values
+      ff s{0.f, 0.f};
+      bool okv = true;
+      for (int i = tid; i < n_star; i += blockDim.x)
+        s = ff_add(s, ff_from_bits(__ldcg(gws.keysB + i), okv));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+        s = ff_add(s, ff{__shfl_xor_sync(0xFFFFFFFFu, s.hi, o),
+                         __shfl_xor_sync(0xFFFFFFFFu, s.lo, o)});
+      if (lane == 0) sh_w[warp] = s;
+      __syncthreads();
+      if (tid == 0) {
+        ff t{static_cast<float>(R), 0.f};
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t = ff_add(t, sh_w[w]);
+        sh_tau_star = t;
+      }
+    }
+  } else {
+    if (nE > 0) fetch(0, 0);
+    bool stopped = false;
+    int p = 0;
+    for (int t0 = 0; t0 < nE && !stopped; t0 += kSweepTile, p ^= 1) {
+      cp_async_wait<0>();
+      __syncthreads();  // tile t0 in buffer p; buffer p ^ 1 free (its tile was walked)
+      if (t0 + kSweepTile < nE) fetch(t0 + kSweepTile, p ^ 1);
+      const u64* kt = sh_key + p * kSweepTile;
+      const double* sh_T = sh_Tb + p * (kSweepTile + 1);
+      const int lenT = min(kSweepTile, nE - t0);  // positions t0 + 1 .. t0 + lenT
+      const int c0 = min(tid * kTilePer, lenT), c1 = min(c0 + kTilePer, lenT);
+      const int len = c1 - c0;
+      u64 kv[kTilePer];
+#pragma unroll
+      for (int q = 0; q < kTilePer; ++q) kv[q] = q < len ? kt[c0 + q] : 0ull;
+      bool ok = true;
+      ff local{0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < kTilePer; ++q) local = ff_add(local, ff_from_bits(kv[q], ok));
+      ff v = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const ff t = shfl_up_ff(v, o);
+        if (lane >= o) v = ff_add(t, v);
+      }
+      ff ex = shfl_up_ff(v, 1);
+      if (lane == 0) ex = ff{0.f, 0.f};
+      if (lane == 31) sh_w[warp] = v;
+      __syncthreads();
+      if (warp == 0) {
+        ff w = lane < static_cast<int>(blockDim.x >> 5) ? sh_w[lane] : ff{0.f, 0.f};
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const ff t = shfl_up_ff(w, o);
+          if (lane >= o) w = ff_add(t, w);
+        }
+        sh_w[lane] = w;  // inclusive over warps
+      }
+      __syncthreads();
+      const ff carry = sh_carry;
+      ff tau_start = ff_add(carry, ex);
+      if (warp > 0) tau_start = ff_add(tau_start, sh_w[warp - 1]);
+
+      if constexpr (MODE == kModeStop) {
+        int first = INT_MAX;
+        unsigned n_ties = 0;
+        ff tau_prev = tau_start;
+        bool okt = true;
+        ff tp = ff_from_double(sh_T[c0], okt);
+#pragma unroll
+        for (int q = 0; q < kTilePer; ++q) {
+          const int m = t0 + c0 + q + 1;
+          if (q < len && first == INT_MAX) {
+            bool okv = ok && okt;
+            const ff tau_m = ff_add(tau_prev, ff_from_bits(kv[q], okv));
+            const double Tp = sh_T[c0 + q], Tm = sh_T[c0 + q + 1];
+            const ff tm = ff_from_double(Tm, okv);
+            bool improve, tie;
+            if (okv) {
+              const ff lhs = ff_mul(tau_m, tp), rhs = ff_mul(tau_prev, tm);
+              improve = ff_cmp(lhs, rhs) > 0;
+              const ff d = ff_sub(lhs, rhs);
+              tie = fabsf(d.hi) <= static_cast<float>(DSPARK_SCHED_TIE_REL) * rhs.hi;
+            } else {  // values outside the float range: double precision
+              const double A = static_cast<double>(tau_m.hi) + tau_m.lo;
+              const double Bv = static_cast<double>(tau_prev.hi) + tau_prev.lo;
+              improve = A * Tp > Bv * Tm;
+              tie = fabs(A * Tp - Bv * Tm) <= DSPARK_SCHED_TIE_REL * Bv * Tm;
+            }
+            if (tie) ++n_ties;
+            if (!improve) first = m;
+            tau_prev = tau_m;
+            tp = tm;
+          }
+        }
+        const int fw = __reduce_min_sync(0xFFFFFFFFu, first);
+        if (lane == 0 && fw != INT_MAX) atomicMin(&sh_break, fw);
+        __syncthreads();
+        const int n_break = sh_break;
+        if (t0 + c0 + 1 <= n_break && n_ties) atomicAdd(&sh_ties, n_ties);
+        if (n_break != INT_MAX) {
+          stopped = true;
+          n_star = n_break - 1;
+          // tau(n*): the tile's start when n* = t0, else from the chunk holding it
+          if (n_star > t0 && t0 + c0 < n_star && n_star <= t0 + c1) {
+            ff t = tau_start;
+            bool okv = true;
+#pragma unroll
+            for (int q = 0; q < kTilePer; ++q)
+              if (t0 + c0 + q < n_star) t = ff_add(t, ff_from_bits(kv[q], okv));
+            sh_tau_star = t;
+          } else if (n_star == t0 && tid == 0) {
+            sh_tau_star = carry;
+          }
+        }
+      } else {  // kModeGlobal
+        Cand loc{0.0, 1.0, -1};
+        ff tau_m = tau_start;
+#pragma unroll
+        for (int q = 0; q < kTilePer; ++q) {
+          if (q < len) {
+            bool okv = true;
+            tau_m = ff_add(tau_m, ff_from_bits(kv[q], okv));
+            loc = cand_pick(loc, Cand{static_cast<double>(tau_m.hi) + tau_m.lo, sh_T[c0 + q + 1],
+                                      t0 + c0 + q + 1});
+          }
+        }
+        Cand run = cand_pick(sh_best, block_excl_pick(loc, sh_cand));
+        unsigned n_ties = 0;
+        tau_m = tau_start;
+#pragma unroll
+        for (int q = 0; q < kTilePer; ++q) {
+          if (q < len) {
+            bool okv = true;
+            tau_m = ff_add(tau_m, ff_from_bits(kv[q], okv));
+            const Cand c{static_cast<double>(tau_m.hi) + tau_m.lo, sh_T[c0 + q + 1],
+                         t0 + c0 + q + 1};
+            if (fabs(c.tau * run.t - run.tau * c.t) <= DSPARK_SCHED_TIE_REL * run.tau * c.t)
+              ++n_ties;
+            run = cand_pick(run, c);
+          }
+        }
+        n_ties = warp_sum_u32(n_ties);
+        if (lane == 0 && n_ties) atomicAdd(&sh_ties, n_ties);
+        __syncthreads();  // every thread has read sh_best
+        if (tid == blockDim.x - 1) sh_best = run;  // the last chunk's run covers the tile
+      }
+      // tau after the tile, for the next one
+      if (tid == blockDim.x - 1) sh_carry = ff_add(tau_start, local);
+    }
+    cp_async_wait<0>();  // a prefetch past the stopping tile lands before the exit
+    __syncthreads();
+    if (MODE == kModeStop && !stopped) {
+      n_star = nE;
+      if (tid == 0) sh_tau_star = sh_carry;
+    }
+    if (MODE == kModeGlobal) n_star = sh_best.m;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    *gws.n_star = n_star;
+    if (ties) *ties = sh_ties;
+    if (theta_out && T) {
+      if (MODE == kModeGlobal) {
+        *theta_out = sh_best.tau / sh_best.t;
+      } else {
+        const double tau_star = static_cast<double>(sh_tau_star.hi) + sh_tau_star.lo;
+        *theta_out = tau_star / T[R + n_star];
+      }
+    }
+    if (K_out) *K_out = n_star;
+  }
+}
+
+// l_r: request r's candidates among the first n* (a prefix of its run, since
+// a does not increase with j), from the ranks of its flattened indices.
+__global__ void __launch_bounds__(kLengthThreads)
+    k_sched_lengths(int R, int gamma, SchedWs gws, int32_t* __restrict__ verify_len) {
+  pdl_wait();  // predecessor grid complete, its writes visible
+  pdl_trigger();
+  const int r = blockIdx.x * kLengthThreads + threadIdx.x;
+  if (r >= R) return;
+  const int n_star = __ldcg(gws.n_star);
+  const int32_t* rk = gws.idxB + static_cast<size_t>(r) * gamma;
+  int l = 0;
+  for (int j0 = 0; j0 < gamma; j0 += 8) {  // eight independent loads at a time
+    int32_t v[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) v[t] = j0 + t < gamma ? __ldcg(rk + j0 + t) : INT_MAX;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) l += v[t] < n_star;
+  }
+  verify_len[r] = l;
+}
+
 // Static-threshold lengths (section 4.3.3, the diagnostic baseline): l_r =
 // the number of leading draft tokens whose confidence reaches the threshold.
 // One CTA, a thread per request; the CTA sees every confidence, so its verdict
@@ -755,8 +1006,17 @@ int schedule_run(int mode, const float* confidences, const double* step_time_ms,
   {
     std::lock_guard<std::mutex> lock(g_sched_mutex);
     if (!g_sched_ready[dev]) {
-      if (cudaFuncSetAttribute(k_schedule, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSchedSmemMaxN * 24) != cudaSuccess)
+      if (cudaFuncSetAttribute(k_sched_sweep_tiled<kModeStop>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kTiledSmem) != cudaSuccess ||
+          cudaFuncSetAttribute(k_sched_sweep_tiled<kModeGlobal>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kTiledSmem) != cudaSuccess ||
+          cudaFuncSetAttribute(k_sched_sweep_tiled<kModeTopK>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kTiledSmem) != cudaSuccess ||
+          cudaFuncSetAttribute(k_sched_merge, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kMergeSmem) != cudaSuccess)
         return DSPARK_ERR_CUDA;
       if (cudaFuncSetAttribute(k_sched_rank, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kRankSmemMax) != cudaSuccess)
@@ -775,6 +1035,8 @@ int schedule_run(int mode, const float* confidences, const double* step_time_ms,
   char* p = static_cast<char*>(workspace);
   SchedWs ws;
   ws.ties_scratch = reinterpret_cast<uint32_t*>(p);
+  ws.n_cand = reinterpret_cast<uint32_t*>(p + 64);
+  ws.n_star = reinterpret_cast<int32_t*>(p + 128);
   p += 256;
   ws.keysA = reinterpret_cast<u64*>(p);
   p += DSPARK_ALIGN256(static_cast<size_t>(n) * 8);
@@ -788,7 +1050,7 @@ int schedule_run(int mode, const float* confidences, const double* step_time_ms,
   uint32_t* ties = near_tie_count ? near_tie_count : ws.ties_scratch;
   const double* T = step_time_ms;
   const size_t rank_smem = static_cast<size_t>(R) * (gamma | 1) * 8;
-  if (n <= kRankMaxN && rank_smem <= static_cast<size_t>(kRankSmemMax)) {
+  if (n < kBlockPathMinN && n <= kRankMaxN && rank_smem <= static_cast<size_t>(kRankSmemMax)) {
     // ranks over the whole GPU, then a one-CTA float-float sweep
     const int blocks = (n + 31) / 32;
     const int grid = blocks < sms ? blocks : sms;
@@ -807,12 +1069,29 @@ int schedule_run(int mode, const float* confidences, const double* step_time_ms,
                                   ties, device_status, K_in, K_out);
     if (e != cudaSuccess) return DSPARK_ERR_CUDA;
   } else {
-    const int use_smem = n <= kSchedSmemMaxN ? 1 : 0;
-    const size_t smem = use_smem ? static_cast<size_t>(n) * 24 : 0;
-    if (launch_pdl(k_schedule, 1, kSchedThreads, smem, st, confidences, T, R, gamma, verify_len,
-                   theta_best, ties, device_status, ws, use_smem, mode, K_in,
-                   K_out) != cudaSuccess)
-      return DSPARK_ERR_CUDA;
+    // sorted blocks, ranks against the other blocks, a tiled one-CTA sweep,
+    // the lengths
+    const int nb = (n + kBlockKeys - 1) / kBlockKeys;
+    cudaError_t e = launch_pdl(k_sched_blocks, nb, kBlockKeys, 0, st, confidences, R, gamma, ws,
+                               device_status);
+    if (e == cudaSuccess)
+      e = launch_pdl(k_sched_merge, nb, kBlockKeys, static_cast<size_t>(kMergeSmem), st, T, R,
+                     gamma, ws, device_status);
+    if (e == cudaSuccess) {
+      if (mode == kModeStop)
+        e = launch_pdl(k_sched_sweep_tiled<kModeStop>, 1, kRankThreads, kTiledSmem, st, T, R,
+                       gamma, ws, theta_best, ties, device_status, K_in, K_out);
+      else if (mode == kModeGlobal)
+        e = launch_pdl(k_sched_sweep_tiled<kModeGlobal>, 1, kRankThreads, kTiledSmem, st, T, R,
+                       gamma, ws, theta_best, ties, device_status, K_in, K_out);
+      else
+        e = launch_pdl(k_sched_sweep_tiled<kModeTopK>, 1, kRankThreads, kTiledSmem, st, T, R,
+                       gamma, ws, theta_best, ties, device_status, K_in, K_out);
+    }
+    if (e == cudaSuccess)
+      e = launch_pdl(k_sched_lengths, (R + kLengthThreads - 1) / kLengthThreads, kLengthThreads,
+                     0, st, R, gamma, ws, verify_len);
+    if (e != cudaSuccess) return DSPARK_ERR_CUDA;
   }
   if (cudaGetLastError() != cudaSuccess) return DSPARK_ERR_CUDA;
   return DSPARK_OK;

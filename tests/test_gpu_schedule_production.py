@@ -2,7 +2,7 @@
 capacity from the global search without the early-stopping break
 (dspark_schedule_capacity) and the dynamic top-K admission
 (dspark_schedule_topk), against the oracle. Both scheduler paths are covered:
-the rank-and-sweep kernels (up to 16,384 candidates) and the one-CTA kernel
+the rank-and-sweep kernels (up to 6,144 candidates) and the block path
 beyond."""
 import json
 import os
@@ -104,8 +104,8 @@ def test_capacity_random(dev, seed):
 
 @pytest.mark.parametrize("R,g", [(512, 16), (1024, 16), (1100, 16), (3000, 32)])
 def test_capacity_named_and_large(dev, R, g):
-    """512 x 16 and 1024 x 16 take the rank-and-sweep path (8 and 16 candidates
-    per thread); 1100 x 16 and 3000 x 32 exceed it and take the one-CTA path."""
+    """The scheduled workload's 512 x 16 and three larger batches, all on the
+    block path (more than 6,144 candidates)."""
     rng = np.random.default_rng(R + g)
     conf = workloads.make_confidences(R, g, seed=7)
     K, ref = check_capacity(conf, jagged_profile(rng, R * (g + 1) + 1), dev, no_ties=True)
