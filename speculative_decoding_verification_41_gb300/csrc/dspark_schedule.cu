@@ -43,6 +43,13 @@ namespace dspark {
 
 typedef unsigned long long u64;
 
+// Per-thread asynchronous 8-byte copy global -> shared (both addresses
+// 8-byte aligned), completing with the thread's commit groups.
+__device__ __forceinline__ void cp_async8(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+
 struct SchedWs {
   uint32_t* ties_scratch;
   uint32_t* n_cand;  // block path: the number of candidates (a > 0)
@@ -117,9 +124,9 @@ __device__ Cand block_excl_pick(const Cand& v, Cand* sh) {
 // Parallel path (up to kRankMaxN candidates): ranks over the whole GPU, then a
 // one-CTA sweep in float-float arithmetic.
 // ---------------------------------------------------------------------------
-constexpr int kRankMaxN = 16384;   // candidates of the parallel path
+constexpr int kRankMaxN = 6144;    // candidates of the rank path (above: the block path)
 constexpr int kRankThreads = 1024;
-// keys of R runs at an odd stride: at most 8192 runs of 3 slots (gamma = 2)
+// keys of R runs at an odd stride (within this for every batch of the rank path)
 constexpr int kRankSmemMax = 196608;
 
 // float -> double without the double-precision pipe (exact: both are IEEE
@@ -249,6 +256,40 @@ __global__ void __launch_bounds__(kRankThreads, 1)
   }
 }
 
+// The early-stop comparison of admission m: improve = tau(m) T(R+m-1) >
+// tau(m-1) T(R+m), tie = the two within the near-tie window. Most admissions
+// are settled in float: D = a T(R+m-1) - tau(m-1) (T(R+m) - T(R+m-1)), whose
+// distance from the float-float evaluation is at most E (the float roundings,
+// the dropped low parts, that evaluation's own error: E keeps a factor of ten
+// over their sum); beyond E from zero and from the window's edge the two agree
+// (same sign, no tie). The rest take the float-float evaluation, and values
+// outside the float range double precision.
+__device__ __forceinline__ void stop_compare(const ff& tau_prev, const ff& av, const ff& tau_m,
+                                             const ff& tp, const ff& tm, bool okv, double Tp,
+                                             double Tm, bool& improve, bool& tie) {
+  if (okv) {
+    const float dT = (tm.hi - tp.hi) + (tm.lo - tp.lo);
+    const float A = av.hi * tp.hi, B = tau_prev.hi * dT;
+    const float D = A - B;
+    const float scale = tau_prev.hi * tm.hi;
+    const float E = 4e-6f * (fabsf(A) + fabsf(B)) + 1e-12f * scale;
+    if (fabsf(D) > E + 1.0001e-9f * scale) {  // false for inf or NaN
+      improve = D > 0.f;
+      tie = false;
+      return;
+    }
+    const ff lhs = ff_mul(tau_m, tp), rhs = ff_mul(tau_prev, tm);
+    improve = ff_cmp(lhs, rhs) > 0;
+    const ff d = ff_sub(lhs, rhs);
+    tie = fabsf(d.hi) <= static_cast<float>(DSPARK_SCHED_TIE_REL) * rhs.hi;
+  } else {  // values outside the float range: double precision
+    const double A = static_cast<double>(tau_m.hi) + tau_m.lo;
+    const double Bv = static_cast<double>(tau_prev.hi) + tau_prev.lo;
+    improve = A * Tp > Bv * Tm;
+    tie = fabs(A * Tp - Bv * Tm) <= DSPARK_SCHED_TIE_REL * Bv * Tm;
+  }
+}
+
 constexpr int kSweepSmemMax = (kRankMaxN + 1) * 8 + kRankMaxN * 4;  // profile slice + lengths
 
 // Sweep over the sorted candidates (one CTA): tau(n) = R + sum of the n
@@ -280,20 +321,28 @@ __global__ void __launch_bounds__(kRankThreads, 1)
   const int c0 = min(tid * chunk, n), c1 = min(c0 + chunk, n);
   const int len = c1 - c0;
 
-  // this thread's keys in registers; the profile slice in shared memory (both
-  // loaded once, up front, so that their latencies overlap)
+  // every global load of the kernel is issued here, before any is waited
+  // for: the profile slice by asynchronous copies, this thread's sorted values
+  // and the flattened indices of its share of the order (for the lengths)
+  if (T)  // the top-K admission may run without a profile
+    for (int m = tid; m <= n; m += blockDim.x) cp_async8(&sh_T[m], T + R + m);
+  cp_async_commit();
   u64 kv[CHUNK];
 #pragma unroll
   for (int q = 0; q < CHUNK; ++q) kv[q] = q < len ? gws.keysB[c0 + q] : 0ull;
-  bool bad_t = false;
-  if (T) {  // the top-K admission may run without a profile
-    for (int m = tid; m <= n; m += blockDim.x) {
-      const double t = T[R + m];
-      const u64 b = static_cast<u64>(__double_as_longlong(t));
-      if ((b >> 63) || ((b >> 52) & 0x7FFull) == 0x7FFull || b == 0ull) bad_t = true;
-      sh_T[m] = t;
-    }
+  int32_t ids[CHUNK];
+#pragma unroll
+  for (int k = 0; k < CHUNK; ++k) {
+    const int i = tid + k * static_cast<int>(blockDim.x);
+    ids[k] = i < n ? gws.idxB[i] : 0;
   }
+  cp_async_wait<0>();
+  bool bad_t = false;
+  if (T)
+    for (int m = tid; m <= n; m += blockDim.x) {
+      const u64 b = static_cast<u64>(__double_as_longlong(sh_T[m]));
+      if ((b >> 63) || ((b >> 52) & 0x7FFull) == 0x7FFull || b == 0ull) bad_t = true;
+    }
   if (bad_t) set_status(status, DSPARK_ERR_BAD_DATA);
   if (tid == 0) {
     sh_nE = 0;
@@ -353,21 +402,12 @@ __global__ void __launch_bounds__(kRankThreads, 1)
       const int m = c0 + q + 1;
       if (q < len && m <= nE && first == INT_MAX) {
         bool okv = ok && okt;
-        const ff tau_m = ff_add(tau_prev, ff_from_bits(kv[q], okv));
+        const ff av = ff_from_bits(kv[q], okv);
+        const ff tau_m = ff_add(tau_prev, av);
         const double Tp = sh_T[m - 1], Tm = sh_T[m];
         const ff tm = ff_from_double(Tm, okv);
         bool improve, tie;
-        if (okv) {
-          const ff lhs = ff_mul(tau_m, tp), rhs = ff_mul(tau_prev, tm);
-          improve = ff_cmp(lhs, rhs) > 0;
-          const ff d = ff_sub(lhs, rhs);
-          tie = fabsf(d.hi) <= static_cast<float>(DSPARK_SCHED_TIE_REL) * rhs.hi;
-        } else {  // values outside the float range: double precision
-          const double A = static_cast<double>(tau_m.hi) + tau_m.lo;
-          const double Bv = static_cast<double>(tau_prev.hi) + tau_prev.lo;
-          improve = A * Tp > Bv * Tm;
-          tie = fabs(A * Tp - Bv * Tm) <= DSPARK_SCHED_TIE_REL * Bv * Tm;
-        }
+        stop_compare(tau_prev, av, tau_m, tp, tm, okv, Tp, Tm, improve, tie);
         if (tie) ++n_ties;
         if (!improve) first = m;
         tau_prev = tau_m;
@@ -431,10 +471,10 @@ __global__ void __launch_bounds__(kRankThreads, 1)
       if (c0 + q < n_star) t = ff_add(t, ff_from_bits(kv[q], okv));
     sh_tau_star = t;
   }
-  for (int i = tid; i < n_star; i += blockDim.x) {
-    const int id = gws.idxB[i];
-    atomicMax(&sh_ell[id / gamma], id % gamma + 1);
-  }
+#pragma unroll
+  for (int k = 0; k < CHUNK; ++k)
+    if (tid + k * static_cast<int>(blockDim.x) < n_star)
+      atomicMax(&sh_ell[ids[k] / gamma], ids[k] % gamma + 1);
   __syncthreads();
   for (int r = tid; r < R; r += blockDim.x) verify_len[r] = sh_ell[r];
   if (tid == 0) {
@@ -477,13 +517,6 @@ constexpr int kSweepTile = kTilePer * kRankThreads;      // 4,096
 // two tiles of sorted values and of the profile slice
 constexpr int kTiledSmem = 2 * kSweepTile * 8 + 2 * (kSweepTile + 1) * 8;
 constexpr int kLengthThreads = 256;
-// candidates from which the block path replaces the rank path
-constexpr int kBlockPathMinN = 6145;
-
-__device__ __forceinline__ void cp_async8(void* smem_dst, const void* gsrc) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
-               : "memory");
-}
 
 // Blocks of kBlockKeys candidates (flattened index e = r*gamma + j): CTA b
 // forms a_{r,j} for the requests overlapping [b*1024, b*1024 + 1024), left to
@@ -794,21 +827,12 @@ __global__ void __launch_bounds__(kRankThreads, 1)
           const int m = t0 + c0 + q + 1;
           if (q < len && first == INT_MAX) {
             bool okv = ok && okt;
-            const ff tau_m = ff_add(tau_prev, ff_from_bits(kv[q], okv));
+            const ff av = ff_from_bits(kv[q], okv);
+            const ff tau_m = ff_add(tau_prev, av);
             const double Tp = sh_T[c0 + q], Tm = sh_T[c0 + q + 1];
             const ff tm = ff_from_double(Tm, okv);
             bool improve, tie;
-            if (okv) {
-              const ff lhs = ff_mul(tau_m, tp), rhs = ff_mul(tau_prev, tm);
-              improve = ff_cmp(lhs, rhs) > 0;
-              const ff d = ff_sub(lhs, rhs);
-              tie = fabsf(d.hi) <= static_cast<float>(DSPARK_SCHED_TIE_REL) * rhs.hi;
-            } else {  // values outside the float range: double precision
-              const double A = static_cast<double>(tau_m.hi) + tau_m.lo;
-              const double Bv = static_cast<double>(tau_prev.hi) + tau_prev.lo;
-              improve = A * Tp > Bv * Tm;
-              tie = fabs(A * Tp - Bv * Tm) <= DSPARK_SCHED_TIE_REL * Bv * Tm;
-            }
+            stop_compare(tau_prev, av, tau_m, tp, tm, okv, Tp, Tm, improve, tie);
             if (tie) ++n_ties;
             if (!improve) first = m;
             tau_prev = tau_m;
@@ -952,24 +976,20 @@ bool sweep_smem_attr() {
   return cudaFuncSetAttribute(k_sched_sweep<4, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSweepSmemMax) == cudaSuccess &&
          cudaFuncSetAttribute(k_sched_sweep<8, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSweepSmemMax) == cudaSuccess &&
-         cudaFuncSetAttribute(k_sched_sweep<16, MODE>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSweepSmemMax) == cudaSuccess;
 }
 
 // the sweep instantiation whose per-thread chunk holds n / 1024 candidates
+// (n <= kRankMaxN <= 8 * 1024)
 template <int MODE>
 cudaError_t launch_sweep(int n, size_t smem, cudaStream_t st, const double* T, int R, int gamma,
                          const SchedWs& ws, int32_t* verify_len, double* theta, uint32_t* ties,
                          int32_t* status, const int32_t* K_in, int32_t* K_out) {
+  static_assert(kRankMaxN <= 8 * kRankThreads, "rank path larger than the sweep's chunks");
   if (n <= 4 * kRankThreads)
     return launch_pdl(k_sched_sweep<4, MODE>, 1, kRankThreads, smem, st, T, R, gamma, ws,
                       verify_len, theta, ties, status, K_in, K_out);
-  if (n <= 8 * kRankThreads)
-    return launch_pdl(k_sched_sweep<8, MODE>, 1, kRankThreads, smem, st, T, R, gamma, ws,
-                      verify_len, theta, ties, status, K_in, K_out);
-  return launch_pdl(k_sched_sweep<16, MODE>, 1, kRankThreads, smem, st, T, R, gamma, ws,
+  return launch_pdl(k_sched_sweep<8, MODE>, 1, kRankThreads, smem, st, T, R, gamma, ws,
                     verify_len, theta, ties, status, K_in, K_out);
 }
 
@@ -1050,7 +1070,7 @@ int schedule_run(int mode, const float* confidences, const double* step_time_ms,
   uint32_t* ties = near_tie_count ? near_tie_count : ws.ties_scratch;
   const double* T = step_time_ms;
   const size_t rank_smem = static_cast<size_t>(R) * (gamma | 1) * 8;
-  if (n < kBlockPathMinN && n <= kRankMaxN && rank_smem <= static_cast<size_t>(kRankSmemMax)) {
+  if (n <= kRankMaxN && rank_smem <= static_cast<size_t>(kRankSmemMax)) {
     // ranks over the whole GPU, then a one-CTA float-float sweep
     const int blocks = (n + 31) / 32;
     const int grid = blocks < sms ? blocks : sms;
