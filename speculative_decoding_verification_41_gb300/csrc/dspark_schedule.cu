@@ -185,6 +185,7 @@ __device__ bool survival_keys(const float* __restrict__ conf, int R, int gamma, 
         bad = true;
         c = 0.f;
       }
+      if (c == 0.f) c = 0.f;  // -0 is in [0, 1]; its product -0 would read as the largest key
       prod *= f2d_exact(c);
       keys[r * stride + j] = static_cast<u64>(__double_as_longlong(prod));
     }
@@ -559,6 +560,7 @@ __global__ void __launch_bounds__(kBlockKeys, 1)
         bad = true;
         c = 0.f;
       }
+      if (c == 0.f) c = 0.f;  // -0 is in [0, 1]; its product -0 would read as the largest key
       prod *= f2d_exact(c);
       const int e = r * gamma + j;
       if (e >= e0 && e < e0 + m) {

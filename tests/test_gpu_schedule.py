@@ -124,6 +124,28 @@ def test_flat_profile_admits_everything(dev):
     assert np.all(ell == 16)
 
 
+@pytest.mark.parametrize("R,g", [(37, 9), (1100, 16)])
+def test_negative_zero_confidence(dev, R, g):
+    """-0.0 lies in [0, 1]: it ends its request's candidates like +0.0 (a > 0
+    is false for a = -0), on the rank path (333 candidates) and the block path
+    (17,600)."""
+    conf = workloads.make_confidences(R, g, seed=R)
+    rng = np.random.default_rng(R)
+    rows = rng.choice(R, size=max(1, R // 10), replace=False)
+    conf[rows, rng.integers(0, g, size=rows.size)] = np.float32(-0.0)
+    assert np.signbit(conf).any()
+    n = R * (g + 1) + 1
+    N = np.arange(n, dtype=np.float64)
+    for T in (workloads.step_time_profile(n), np.full(n, 4.0), 2.0 + 1e-4 * N):
+        ell, ref = check(conf, T, dev)
+        zero_at = np.where(conf[rows] == 0, np.arange(g), g).min(axis=1)
+        assert np.all(ell[rows] <= zero_at)
+    out = binding.dspark_schedule(torch.from_numpy(conf).to(dev),
+                                  torch.from_numpy(workloads.step_time_profile(n)).to(dev))
+    torch.cuda.synchronize()
+    assert int(out["device_status"].item()) == 0
+
+
 def test_bad_confidence_sets_status(dev):
     conf = workloads.make_confidences(8, 4, seed=1)
     conf[3, 2] = np.nan

@@ -145,3 +145,23 @@ def test_judge_rejects_a_wrong_stopping_point():
     if not np.array_equal(bad, s["verify_len"]):
         with pytest.raises(AssertionError):
             judge_schedule(bad, None, p, R, g)
+
+
+def test_negative_zero_confidence_acts_as_zero():
+    """-0.0 is a confidence in [0, 1]; its survival product is -0.0, and a > 0
+    is false for it as for +0.0: the request's candidates end there. Every
+    output of both scheduler variants equals the +0.0 case's."""
+    rng = np.random.default_rng(5)
+    conf = rng.uniform(0.3, 1.0, (6, 5)).astype(np.float32)
+    N = np.arange(6 * 6 + 1, dtype=np.float64)
+    T = 2.0 + 0.05 * N
+    for r, j in [(0, 0), (2, 3), (5, 4)]:
+        neg, pos = conf.copy(), conf.copy()
+        neg[r, j], pos[r, j] = np.float32(-0.0), np.float32(0.0)
+        for stop in (True, False):
+            a, b = oracle.schedule(neg, T, early_stop=stop), oracle.schedule(pos, T, early_stop=stop)
+            assert a["verify_len"].tolist() == b["verify_len"].tolist()
+            assert a["theta_best"] == b["theta_best"] and a["n_admitted"] == b["n_admitted"]
+            assert a["verify_len"][r] <= j
+        assert oracle.schedule_path(neg, T)["order"].tolist() == \
+            oracle.schedule_path(pos, T)["order"].tolist()
