@@ -65,6 +65,8 @@ SHAPES = [
     (5, 32, 9000, torch.bfloat16, 1.0, "full", False),      # gamma = 32
     (8, 16, 10000, torch.bfloat16, 0.05, "full", False),    # cold: nearly one-hot rows
     (8, 16, 10000, torch.bfloat16, 20.0, "uniform", False), # hot: nearly flat rows
+    (7, 5, 1, torch.bfloat16, 0.9, "uniform", False),       # one token: every rate is 1
+    (7, 5, 3, torch.float32, 0.9, "uniform", True),         # three tokens, ragged
 ]
 
 

@@ -115,6 +115,23 @@ def test_single_token_vocabulary(dev):
     assert np.all(out["emitted_tokens"].cpu().numpy() == 0)
 
 
+@pytest.mark.parametrize("V,dt", [(1, torch.bfloat16), (1, torch.float32), (2, torch.bfloat16),
+                                  (3, torch.float32), (5, torch.bfloat16)])
+def test_tiny_vocabularies(dev, V, dt):
+    """Rows of 1 to 5 tokens (2 to 20 bytes: the plain-load path, one unit and
+    one resample segment per row). With one token both distributions are 1 at
+    token 0: every verified position is accepted and every emitted token is 0."""
+    vi = workloads.make_verify(7, 5, V, dt, 0.9, rho=(0.5, 0.95), verify_len="uniform",
+                               ragged=V % 2 == 1, seed=40 + V, device=dev)
+    out, ref, st = check_all(vi)
+    if V == 1:
+        ell = vi.verify_len.cpu().numpy()
+        np.testing.assert_array_equal(out["accepted_len"].cpu().numpy(), ell)
+        em = out["emitted_tokens"].cpu().numpy()
+        for r in range(vi.B):
+            assert np.all(em[r, :ell[r] + 1] == 0) and np.all(em[r, ell[r] + 1:] == -1)
+
+
 def test_empty_batch(dev):
     e = torch.empty(0, 5, dtype=torch.int32, device=dev)
     out = binding.dspark_verify(torch.zeros(1, 64, dtype=torch.bfloat16, device=dev),
