@@ -69,31 +69,75 @@ struct SchedWs {
 //                 from device memory
 enum { kModeStop = 0, kModeGlobal = 1, kModeTopK = 2 };
 
+// R as a float pair, exactly (R < 2^30: the low part is a small integer).
+__device__ __forceinline__ ff ff_of_int(int R) {
+  const float hi = static_cast<float>(R);
+  return ff{hi, static_cast<float>(R - static_cast<int>(hi))};
+}
+
+__device__ __forceinline__ double d_of(const ff& x) { return static_cast<double>(x.hi) + x.lo; }
+
+// A positive double as a float by its bits (truncated: relative error below
+// 2^-23); false outside the float's normal range.
+__device__ __forceinline__ bool f_of(double x, float& f) {
+  const u64 b = static_cast<u64>(__double_as_longlong(x));
+  const int e = static_cast<int>((b >> 52) & 0x7FF) - 1023;
+  if (e < -126 || e > 127) return false;
+  f = __uint_as_float((static_cast<uint32_t>(e + 127) << 23) |
+                      static_cast<uint32_t>((b >> 29) & 0x7FFFFFull));
+  return true;
+}
+
 // A prefix of the sorted candidates as a point of the global search:
 // Theta = tau / t with t = T(R + m); m < 0 marks "none".
 struct Cand {
-  double tau, t;
+  ff tau;
+  double t;
   int m;
 };
 
-// a precedes b in the sorted order; the first maximum of Theta wins (compared
-// by cross-multiplication: both t are positive)
+// Theta(b) > Theta(a), by cross-multiplication (both t are positive). The two
+// products are formed in float from the pairs' high parts and the t's bits
+// (each within 2^-22 of the double products); more than 4e-6 apart they
+// decide, otherwise the double products do. Inf and NaN fail the float test.
+__device__ __forceinline__ bool theta_greater(const Cand& b, const Cand& a) {
+  float ta, tb;
+  if (f_of(a.t, ta) && f_of(b.t, tb)) {
+    const float L = b.tau.hi * ta, Rr = a.tau.hi * tb;
+    if (fabsf(L - Rr) > 4e-6f * (L + Rr)) return L > Rr;
+  }
+  return d_of(b.tau) * a.t > d_of(a.tau) * b.t;
+}
+
+// |Theta(c) - Theta(run)| <= eps Theta(run), multiplied through by both t;
+// settled in float when the products are clearly apart, as above.
+__device__ __forceinline__ bool theta_tie(const Cand& c, const Cand& run) {
+  float tc, tr;
+  if (f_of(c.t, tc) && f_of(run.t, tr)) {
+    const float L = c.tau.hi * tr, Rr = run.tau.hi * tc;
+    if (fabsf(L - Rr) > 4e-6f * (L + Rr) + 1.0001e-9f * Rr) return false;
+  }
+  const double rt = d_of(run.tau);
+  return fabs(d_of(c.tau) * run.t - rt * c.t) <= DSPARK_SCHED_TIE_REL * rt * c.t;
+}
+
+// a precedes b in the sorted order; the first maximum of Theta wins
 __device__ __forceinline__ Cand cand_pick(const Cand& a, const Cand& b) {
   if (b.m < 0) return a;
   if (a.m < 0) return b;
-  return b.tau * a.t > a.tau * b.t ? b : a;
+  return theta_greater(b, a) ? b : a;
 }
 
 __device__ __forceinline__ Cand shfl_up_cand(const Cand& v, int o) {
-  return Cand{__shfl_up_sync(0xFFFFFFFFu, v.tau, o), __shfl_up_sync(0xFFFFFFFFu, v.t, o),
-              __shfl_up_sync(0xFFFFFFFFu, v.m, o)};
+  return Cand{ff{__shfl_up_sync(0xFFFFFFFFu, v.tau.hi, o), __shfl_up_sync(0xFFFFFFFFu, v.tau.lo, o)},
+              __shfl_up_sync(0xFFFFFFFFu, v.t, o), __shfl_up_sync(0xFFFFFFFFu, v.m, o)};
 }
 
 // Exclusive scan of v over the block in thread order under cand_pick (sh: 32
 // slots of shared memory). Every thread must call it.
 __device__ Cand block_excl_pick(const Cand& v, Cand* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const Cand none{0.0, 1.0, -1};
+  const Cand none{ff{0.f, 0.f}, 1.0, -1};
   Cand incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -349,7 +393,7 @@ __global__ void __launch_bounds__(kRankThreads, 1)
     sh_nE = 0;
     sh_break = INT_MAX;
     sh_ties = 0;
-    sh_tau_star = ff{static_cast<float>(R), 0.f};
+    sh_tau_star = ff_of_int(R);
   }
   for (int r = tid; r < R; r += blockDim.x) sh_ell[r] = 0;
 
@@ -387,7 +431,7 @@ __global__ void __launch_bounds__(kRankThreads, 1)
   }
   __syncthreads();
   const int nE = sh_nE;
-  ff tau_start = ff_add(ff{static_cast<float>(R), 0.f}, ex);
+  ff tau_start = ff_add(ff_of_int(R), ex);
   if (warp > 0) tau_start = ff_add(tau_start, sh_w[warp - 1]);
 
   int n_star;
@@ -424,7 +468,7 @@ __global__ void __launch_bounds__(kRankThreads, 1)
   } else if constexpr (MODE == kModeGlobal) {
     // the best admission of this chunk, then the running best before every
     // position (first maximum; position 0, nothing admitted, leads)
-    Cand loc{0.0, 1.0, -1};
+    Cand loc{ff{0.f, 0.f}, 1.0, -1};
     ff tau_m = tau_start;
 #pragma unroll
     for (int q = 0; q < CHUNK; ++q) {
@@ -432,10 +476,10 @@ __global__ void __launch_bounds__(kRankThreads, 1)
       if (q < len && m <= nE) {
         bool okv = true;
         tau_m = ff_add(tau_m, ff_from_bits(kv[q], okv));
-        loc = cand_pick(loc, Cand{static_cast<double>(tau_m.hi) + tau_m.lo, sh_T[m], m});
+        loc = cand_pick(loc, Cand{tau_m, sh_T[m], m});
       }
     }
-    Cand run = cand_pick(Cand{static_cast<double>(R), sh_T[0], 0}, block_excl_pick(loc, sh_cand));
+    Cand run = cand_pick(Cand{ff_of_int(R), sh_T[0], 0}, block_excl_pick(loc, sh_cand));
     unsigned n_ties = 0;
     tau_m = tau_start;
 #pragma unroll
@@ -444,9 +488,8 @@ __global__ void __launch_bounds__(kRankThreads, 1)
       if (q < len && m <= nE) {
         bool okv = true;
         tau_m = ff_add(tau_m, ff_from_bits(kv[q], okv));
-        const Cand c{static_cast<double>(tau_m.hi) + tau_m.lo, sh_T[m], m};
-        // |Theta(m) - Theta_best| <= eps Theta_best, multiplied through by both T
-        if (fabs(c.tau * run.t - run.tau * c.t) <= DSPARK_SCHED_TIE_REL * run.tau * c.t) ++n_ties;
+        const Cand c{tau_m, sh_T[m], m};
+        if (theta_tie(c, run)) ++n_ties;  // |Theta(m) - Theta_best| <= eps Theta_best
         run = cand_pick(run, c);
       }
     }
@@ -733,9 +776,9 @@ __global__ void __launch_bounds__(kRankThreads, 1)
   if (tid == 0) {
     sh_break = INT_MAX;
     sh_ties = 0;
-    sh_carry = ff{static_cast<float>(R), 0.f};
-    sh_tau_star = ff{static_cast<float>(R), 0.f};
-    if (MODE == kModeGlobal) sh_best = Cand{static_cast<double>(R), T[R], 0};
+    sh_carry = ff_of_int(R);
+    sh_tau_star = ff_of_int(R);
+    if (MODE == kModeGlobal) sh_best = Cand{ff_of_int(R), T[R], 0};
   }
   // tile t0's values and profile slice T(R + t0 + i), i = 0..len, into buffer p
   auto fetch = [&](int t0, int p) {
@@ -862,15 +905,14 @@ __global__ void __launch_bounds__(kRankThreads, 1)
           }
         }
       } else {  // kModeGlobal
-        Cand loc{0.0, 1.0, -1};
+        Cand loc{ff{0.f, 0.f}, 1.0, -1};
         ff tau_m = tau_start;
 #pragma unroll
         for (int q = 0; q < kTilePer; ++q) {
           if (q < len) {
             bool okv = true;
             tau_m = ff_add(tau_m, ff_from_bits(kv[q], okv));
-            loc = cand_pick(loc, Cand{static_cast<double>(tau_m.hi) + tau_m.lo, sh_T[c0 + q + 1],
-                                      t0 + c0 + q + 1});
+            loc = cand_pick(loc, Cand{tau_m, sh_T[c0 + q + 1], t0 + c0 + q + 1});
           }
         }
         Cand run = cand_pick(sh_best, block_excl_pick(loc, sh_cand));
@@ -881,10 +923,8 @@ __global__ void __launch_bounds__(kRankThreads, 1)
           if (q < len) {
             bool okv = true;
             tau_m = ff_add(tau_m, ff_from_bits(kv[q], okv));
-            const Cand c{static_cast<double>(tau_m.hi) + tau_m.lo, sh_T[c0 + q + 1],
-                         t0 + c0 + q + 1};
-            if (fabs(c.tau * run.t - run.tau * c.t) <= DSPARK_SCHED_TIE_REL * run.tau * c.t)
-              ++n_ties;
+            const Cand c{tau_m, sh_T[c0 + q + 1], t0 + c0 + q + 1};
+            if (theta_tie(c, run)) ++n_ties;
             run = cand_pick(run, c);
           }
         }
@@ -910,7 +950,7 @@ __global__ void __launch_bounds__(kRankThreads, 1)
     if (ties) *ties = sh_ties;
     if (theta_out && T) {
       if (MODE == kModeGlobal) {
-        *theta_out = sh_best.tau / sh_best.t;
+        *theta_out = d_of(sh_best.tau) / sh_best.t;
       } else {
         const double tau_star = static_cast<double>(sh_tau_star.hi) + sh_tau_star.lo;
         *theta_out = tau_star / T[R + n_star];
