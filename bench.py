@@ -883,10 +883,13 @@ def drafter_measure(args, dev, stream, rank, ws):
                      "tensor_tflops": flops / (t_step * 1e-3) / 1e12},
         # the product path, the whole block as one launch: the same bytes per
         # position (W2 counted once) over the call time, serial chain included
-        "block": {"kernel": "k_draft_block", "algorithmic_bytes": alg * g,
+        # the one cooperative launch: k_draft_pair for two request tiles
+        # (128 < B <= 256), k_draft_block for one
+        "block": {"kernel": "k_draft_pair" if 128 < sh["B"] <= 256 else "k_draft_block",
+                  "algorithmic_bytes": alg * g,
                   "achieved": alg * g / (t_call * 1e-3) / 1e9, "unit": "GB/s",
                   "tensor_tflops": flops * g / (t_call * 1e-3) / 1e12},
-        "gpu_launches_per_call": 1,  # k_draft_block (cooperative), after one 2 KB memset
+        "gpu_launches_per_call": 1,  # one cooperative launch, after one memset
         "gpu_launches_per_call_timed_path": 1 + 2 * g,
         "cpu_baseline": None,
     }

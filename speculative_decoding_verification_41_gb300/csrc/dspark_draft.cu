@@ -21,6 +21,14 @@
 //                 draw of softmax(L_k / T) in ascending token order. It then
 //                 copies W1[x_k] into G for the next position.
 //
+// dspark_draft_markov runs the whole block in one cooperative launch where the
+// grid fits on the GPU at once: k_draft_pair for two request tiles
+// (128 < B <= 256: the streaming CTAs serve both tiles and the draws run on
+// CTAs of their own, so one tile's draws and next G overlap the other tile's
+// streaming), k_draft_block otherwise (the CTAs of a request tile stream it,
+// meet at a barrier, draw); larger grids, and the timed entry point, take the
+// two kernels per position above.
+//
 // W2 is stored transposed, w2t[v][j] = W2[j][v], so both operands are K-major.
 // The tile is 128 requests x 128 tokens. With G in tensor memory (where the
 // MMA reads it without touching shared memory), a ring of 8 W2 chunks keeps two
@@ -252,6 +260,7 @@ struct DraftPickArgs {
   int32_t* tokens;           // [B][gamma]
   int32_t* status;
   unsigned long long* ready;  // k_draft_block: [B], (k + 1) << 32 | x_k once drawn
+  bool relaxed_flag = false;  // the flag's reader needs only x_k (k_draft_pair)
 };
 
 constexpr int kPickWarps = 4;   // one request per warp
@@ -372,9 +381,16 @@ __device__ __forceinline__ void publish_token(const DraftPickArgs& a, int b, int
                          lane * 128;
       asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
     }
-    if (lane == 0 && a.k + 1 < a.gamma)
-      st_release_gpu64(&a.ready[b], (static_cast<unsigned long long>(a.k + 1) << 32) |
-                                        static_cast<uint32_t>(y));
+    if (lane == 0 && a.k + 1 < a.gamma) {
+      const unsigned long long f =
+          (static_cast<unsigned long long>(a.k + 1) << 32) | static_cast<uint32_t>(y);
+      // k_draft_pair's reader takes only the token from the flag (W1 is an
+      // input): no ordering needed; k_draft_block's readers rely on a release
+      if (a.relaxed_flag)
+        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(&a.ready[b]), "l"(f) : "memory");
+      else
+        st_release_gpu64(&a.ready[b], f);
+    }
   } else if (a.k + 1 < a.gamma) {
     copy_row(a.W1, a.G, y, b, a.r, lane);
   }
@@ -523,6 +539,7 @@ __device__ __forceinline__ void mass_add(int32_t& R, ff& S, int32_t R2, ff S2) {
 // and draw_in_tile finishes. Float pairs and exact powers of two throughout,
 // as in draw_request; only the grouping of the sums differs.
 constexpr int kRangesHeld = kMaxBlockCtas / 32;  // ranges per lane at most
+template <int kRec>  // records per range (one per epilogue group, or one combined)
 __device__ __forceinline__ void draw_ranges(const DraftPickArgs& a, int b, int lane,
                                             const DraftPartial* parts, int per_m) {
   const int per = (per_m + 31) / 32;
@@ -536,9 +553,11 @@ __device__ __forceinline__ void draw_ranges(const DraftPickArgs& a, int b, int l
     rR[i] = INT_MIN;
     rS[i] = ff{0.f, 0.f};
     if (p0 + i < p1) {
-      const DraftPartial q0 = ld_part(parts + 2 * (p0 + i)), q1 = ld_part(parts + 2 * (p0 + i) + 1);
-      mass_add(rR[i], rS[i], q0.R, ff{q0.hi, q0.lo});
-      mass_add(rR[i], rS[i], q1.R, ff{q1.hi, q1.lo});
+#pragma unroll
+      for (int q = 0; q < kRec; ++q) {
+        const DraftPartial d = ld_part(parts + kRec * (p0 + i) + q);
+        mass_add(rR[i], rS[i], d.R, ff{d.hi, d.lo});
+      }
       mass_add(Rl, Sl, rR[i], rS[i]);
     }
   }
@@ -1016,7 +1035,7 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
       for (int i = ew * a.per_m + p; i < kDM; i += kDEpiWarps * a.per_m) {
         const int rq = m_tile * kDM + i;
         if (rq >= a.B) break;
-        draw_ranges(pa, rq, lane, parts_k + static_cast<size_t>(rq) * a.per_m * 2, a.per_m);
+        draw_ranges<2>(pa, rq, lane, parts_k + static_cast<size_t>(rq) * a.per_m * 2, a.per_m);
       }
     }
     if (leader) bulk_wait<0>();
@@ -1043,6 +1062,454 @@ __global__ void __launch_bounds__(kDThreads, 1)
     k_draft_block(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapU,
                   const __grid_constant__ CUtensorMap mapL, const DraftBlockArgs ba) {
   draft_tiles<true>(mapW, mapU, mapL, ba);
+}
+
+// ---------------------------------------------------------------------------
+// k_draft_pair: the whole block for two request tiles (128 < B <= 256) in one
+// cooperative launch: most CTAs stream both request tiles, a few only draw
+// ---------------------------------------------------------------------------
+// In k_draft_block the CTAs of a request tile stream that tile's vocabulary
+// ranges, then wait at the tile's barrier, draw and load the next G while the
+// memory system idles. Here each streaming CTA owns one contiguous vocabulary
+// range for both request tiles and alternates: position k's tiles of request
+// tile 0, then those of request tile 1 (walking the range backwards, so that
+// it starts on the W2 tiles just read), then position k + 1's of tile 0, ...
+// A request tile's end of a position runs beside the other tile's streaming:
+// the epilogue leaves its range masses (one record per request and CTA) behind
+// and streams on; a release warp publishes the CTA's tag for (tile, position)
+// once the rows, statistics and records are in memory. The draws run on CTAs
+// of their own (kPDrawCtas of them, one warp per request of a tile), which
+// read the tags of every range and then draw; on the streaming SMs the draws'
+// chains of dependent loads would compete with the streams. The streaming
+// CTAs' four G warps wait for the tile's tokens and write its next
+// G = W1[x_k] into tensor memory. No CTA waits at a grid-wide barrier. Tensor
+// memory: two f32 accumulators of 128 columns, then G of request tile 0 and of
+// request tile 1 (r / 2 columns each): 512 columns at r = 256.
+constexpr int kPStages = 7;     // W2 ring (the eighth stage's room holds the range masses)
+constexpr int kPGWarps = 4;     // G loaders: one per lane quarter of tensor memory
+constexpr int kPWarpU = 2 + kDEpiWarps;      // the U producer's warp
+constexpr int kPWarpG = kPWarpU + 1;         // the G warps' first
+constexpr int kPWarpRel = kPWarpG + kPGWarps;  // the release warp
+// draw CTAs beside the streaming ones: with 16 warps each, 8 give one warp per
+// request of a tile (measured on 256 x 16 x 129,280: 0.69 ms per block with 8,
+// 0.76 with 4 or 6, 0.72-0.73 with 10 or 16)
+constexpr int kPDrawCtas = 8;
+constexpr int kPThreads = (kPWarpRel + 1) * 32;
+constexpr uint32_t kPOffU = kPStages * kBoxW;
+constexpr uint32_t kPOffPart = kPOffU + kDSlots * 2 * kBoxU;  // [request tile][group][row]
+constexpr uint32_t kPOffBar = kPOffPart + 2 * 2 * kDM * sizeof(DraftPartial);
+constexpr uint32_t kPairSmem = kPOffBar + 512 + 1024;
+static_assert(kPairSmem <= 232448, "shared memory of k_draft_pair");
+static_assert(kColG + 2 * (DSPARK_DRAFT_MAX_RANK / 2) <= kTmemCols, "tensor memory of k_draft_pair");
+static_assert(2 * kMaxBlockCtas * 4 <= kTileSyncBytes, "tags of k_draft_pair");
+
+struct PairBars {
+  uint64_t a_full[2];  // G of request tile g in tensor memory (one arrival per G warp)
+  uint64_t w_full[kPStages], w_empty[kPStages];
+  uint64_t u_full[kDSlots], u_empty[kDSlots];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t st_ready[2];  // a group's rows are in shared memory, ready to store
+  uint64_t mma_done;
+  uint64_t epi_done[2];  // the epilogue finished request tile g's tiles of a position
+  uint32_t tmem_base;
+};
+static_assert(sizeof(PairBars) <= 512, "barrier block of k_draft_pair");
+
+// The eight epilogue warps of the CTA (256 threads) meet: named barrier 1.
+__device__ __forceinline__ void epi_warps_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kDEpiWarps * 32) : "memory");
+}
+
+// G of request tile g into tensor memory, rows of this warp's lane quarter
+// (request g * 128 + 32 * quarter + lane): W1[x] for the token x the row's
+// request drew at position k - 1 (the anchor at k = 0), zero past the batch.
+// Returns false if a wait gave up.
+__device__ __forceinline__ bool pair_load_g(const DraftBlockArgs& ba, int g, int k, uint32_t tmem,
+                                            int quarter, int lane) {
+  const DraftStepArgs& a = ba.s;
+  const int b = g * kDM + quarter * 32 + lane;
+  const bool row_ok = b < a.B;
+  int x = 0;
+  bool r_ok = true;
+  if (row_ok) {
+    if (k == 0) {
+      x = ba.anchors[b];
+      if (x < 0 || x >= a.V) {
+        set_status(a.status, DSPARK_ERR_BAD_DATA);
+        x = 0;
+      }
+    } else {
+      // the flag carries the token; W1 is an input, so a relaxed read suffices
+      WaitClock clock;
+      unsigned long long f;
+      for (;;) {
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(f) : "l"(&ba.ready[b]) : "memory");
+        if ((f >> 32) >= static_cast<unsigned>(k)) break;
+        if (clock.expired()) {
+          r_ok = false;
+          break;
+        }
+        __nanosleep(32);
+      }
+      x = static_cast<int>(static_cast<uint32_t>(f));
+    }
+  }
+  if (!__all_sync(0xFFFFFFFFu, r_ok)) {
+    set_status(a.status, DSPARK_ERR_TIMEOUT);
+    return false;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(ba.p.W1 + static_cast<size_t>(x) * a.r);
+  const int KC = a.r / kDK;
+  for (int c = 0; c < KC; ++c) {  // 64 elements (32 columns) at a time
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 v = row_ok ? __ldg(src + c * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+      w[4 * i] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+    __syncwarp();
+    tmem_st32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kColG +
+                  static_cast<uint32_t>(g) * (DSPARK_DRAFT_MAX_RANK / 2) + c * 32,
+              w);
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  return true;
+}
+
+// Every CTA's tag of request tile g has reached k + 1: the rows, statistics
+// and range records of (g, k) are in memory. Each lane reads the tags of the
+// ranges it reads in draw_ranges, all at once with relaxed loads (one round
+// trip per try, not one per tag), and once every tag is there one fence makes
+// them acquires; the warp then meets, so the loads of every lane come after.
+// Returns false if the wait gave up.
+constexpr int kTagsHeld = kMaxBlockCtas / 32;
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool pair_wait_tags(const uint32_t* tags, int P, int k, int lane) {
+  const int per = (P + 31) / 32;
+  const int p0 = min(lane * per, P), p1 = min(p0 + per, P);
+  WaitClock clock;
+  for (;;) {
+    uint32_t v[kTagsHeld];
+#pragma unroll
+    for (int q = 0; q < kTagsHeld; ++q) v[q] = p0 + q < p1 ? ld_relaxed_gpu(&tags[p0 + q]) : ~0u;
+    bool mine = true;
+#pragma unroll
+    for (int q = 0; q < kTagsHeld; ++q) mine = mine && v[q] >= static_cast<uint32_t>(k + 1);
+    if (__all_sync(0xFFFFFFFFu, mine)) break;
+    if (__any_sync(0xFFFFFFFFu, clock.expired())) return false;
+    __nanosleep(32);
+  }
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  __syncwarp();
+  return true;
+}
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    k_draft_pair(const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapU,
+                 const __grid_constant__ CUtensorMap mapL, const DraftBlockArgs ba) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  PairBars* bars = reinterpret_cast<PairBars*>(smem + kPOffBar);
+  DraftPartial* part = reinterpret_cast<DraftPartial*>(smem + kPOffPart);
+  const DraftStepArgs& a = ba.s;
+  const uint32_t sbase = smem_addr(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = a.per_m;  // streaming CTAs: vocabulary ranges; the rest draw
+  const int p = blockIdx.x;
+  if (p >= P) {
+    // ---------------- draw CTA: one warp per request of each (tile, position) ----------------
+    // (no tensor memory, barriers or shared memory: it reads the tags, the
+    // range records and statistics, and the rows of the tile it picks)
+    const int n_draw_warps = (static_cast<int>(gridDim.x) - P) * (kPThreads / 32);
+    const int wid = (p - P) * (kPThreads / 32) + warp;
+    const size_t n_req = static_cast<size_t>(a.n_m) * kDM;
+    bool ok = true;
+    for (int k = 0; k < a.gamma && ok; ++k)
+      for (int g = 0; g < 2 && ok; ++g) {
+        DraftPickArgs pa = ba.p;
+        pa.k = k;
+        pa.stats = (k & 1) ? ba.stats1 : a.stats;
+        pa.ready = ba.ready;
+        pa.relaxed_flag = true;
+        for (int i = wid; i < kDM && ok; i += n_draw_warps) {
+          const int rq = g * kDM + i;
+          if (rq >= a.B) break;
+          ok = pair_wait_tags(ba.tile_sync + g * kMaxBlockCtas, P, k, lane);
+          if (!ok) {
+            if (lane == 0) set_status(a.status, DSPARK_ERR_TIMEOUT);
+            break;
+          }
+          draw_ranges<1>(pa, rq, lane, ba.parts + (static_cast<size_t>(k & 1) * n_req + rq) * P,
+                         P);
+        }
+      }
+    return;
+  }
+  const int lo = range_begin(p, a.n_tiles, P), hi = range_begin(p + 1, a.n_tiles, P);
+  const int n_local = hi - lo;
+  const int KC = a.r / kDK;
+  const int gamma = a.gamma;
+  const size_t n_req = static_cast<size_t>(a.n_m) * kDM;
+  uint32_t* const tags = ba.tile_sync;  // [2][kMaxBlockCtas]: (tile, CTA) -> position + 1
+  // request tile g's t-th vocabulary tile of this range: tile 0 forwards, tile
+  // 1 backwards (so each starts on the W2 tiles the other read last)
+  auto tile_of = [&](int g, int t) { return g ? hi - 1 - t : lo + t; };
+  // tile index tg over (position, request tile, t): its position and request tile
+  auto pos_of = [&](int tg) { return tg / (2 * n_local); };
+  auto rt_of = [&](int tg) { return (tg / n_local) & 1; };
+
+  if (threadIdx.x == 0) {
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&bars->a_full[g], kPGWarps);
+      mbar_init(&bars->epi_done[g], kDEpiWarps);
+    }
+    for (int s = 0; s < kPStages; ++s) {
+      mbar_init(&bars->w_full[s], 1);
+      mbar_init(&bars->w_empty[s], 1);
+    }
+    for (int s = 0; s < kDSlots; ++s) {
+      mbar_init(&bars->u_full[s], 1);
+      mbar_init(&bars->u_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->acc_full[i], 1);
+      mbar_init(&bars->acc_empty[i], 4);
+      mbar_init(&bars->st_ready[i], 4);
+    }
+    mbar_init(&bars->mma_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const int total_tiles = gamma * 2 * n_local;
+
+  if (warp == 0) {
+    // ---------------- W2 producer: the chunks of every tile, in order ----------------
+    if (lane == 0) {
+      tma_prefetch_map(&mapW);
+      const uint64_t pol_keep = policy_evict_last();
+      const int total = total_tiles * KC;
+      bool ok = true;
+      int nq = 0;
+      for (int q = 0; q < total; ++q) {
+        const int tg = q / KC, c = q % KC, s = q % kPStages;
+        if (q >= kPStages) {
+          ok = wait_or_flag(&bars->w_empty[s], ((q / kPStages) - 1) & 1, a.status);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(&bars->w_full[s], kBoxW);
+        tma_load_2d(smem + s * kBoxW, &mapW, c * kDK, tile_of(rt_of(tg), tg % n_local) * kDN,
+                    &bars->w_full[s], pol_keep);
+        nq = q + 1;
+      }
+      if (!ok)
+        for (int q = nq - kPStages > 0 ? nq - kPStages : 0; q < nq; ++q)
+          mbar_wait(&bars->w_full[q % kPStages], (q / kPStages) & 1);
+    }
+  } else if (warp == kPWarpU) {
+    // ---------------- U producer: every tile, in order ----------------
+    if (lane == 0) {
+      tma_prefetch_map(&mapU);
+      const uint64_t pol_stream = policy_evict_first();
+      bool ok = true;
+      int nu = 0;
+      for (int tg = 0; tg < total_tiles; ++tg) {
+        const int slot = tg % kDSlots;
+        if (tg >= kDSlots) {
+          ok = wait_or_flag(&bars->u_empty[slot], ((tg / kDSlots) - 1) & 1, a.status);
+          if (!ok) break;
+        }
+        const int g = rt_of(tg);
+        const int v0 = tile_of(g, tg % n_local) * kDN;
+        uint8_t* dst = smem + kPOffU + slot * 2 * kBoxU;
+        mbar_arrive_expect_tx(&bars->u_full[slot], 2 * kBoxU);
+        tma_load_3d(dst, &mapU, v0, pos_of(tg), g * kDM, &bars->u_full[slot], pol_stream);
+        tma_load_3d(dst + kBoxU, &mapU, v0 + kDK, pos_of(tg), g * kDM, &bars->u_full[slot],
+                    pol_stream);
+        nu = tg + 1;
+      }
+      if (!ok)
+        for (int t = nu - kDSlots > 0 ? nu - kDSlots : 0; t < nu; ++t)
+          mbar_wait(&bars->u_full[t % kDSlots], (t / kDSlots) & 1);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = true;
+      for (int j = 0; j < gamma && ok; ++j)
+        for (int g = 0; g < 2 && ok; ++g) {
+          ok = wait_or_flag(&bars->a_full[g], j & 1, a.status);  // G of (g, j) in tensor memory
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a_col = tmem + kColG + static_cast<uint32_t>(g) * (DSPARK_DRAFT_MAX_RANK / 2);
+          for (int t = 0; t < n_local && ok; ++t) {
+            const int tg = (j * 2 + g) * n_local + t;
+            const int acc = tg & 1;
+            if (tg >= 2) {
+              ok = wait_or_flag(&bars->acc_empty[acc], ((tg >> 1) - 1) & 1, a.status);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            const uint32_t d = tmem + acc * kDN;
+            for (int c = 0; c < KC && ok; ++c) {
+              const int q = tg * KC + c, s = q % kPStages;
+              ok = wait_or_flag(&bars->w_full[s], (q / kPStages) & 1, a.status);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t w_base = sbase + s * kBoxW;
+#pragma unroll
+              for (int kk = 0; kk < kDK / 16; ++kk)
+                tc_mma_ts(d, a_col + c * (kDK / 2) + kk * 8, sdesc_sw128(w_base + 32 * kk), kIdesc,
+                          (c | kk) != 0);
+              tc_commit(&bars->w_empty[s]);
+            }
+            if (ok) tc_commit(&bars->acc_full[acc]);
+          }
+        }
+      tc_commit(&bars->mma_done);
+      wait_or_flag(&bars->mma_done, 0, a.status);
+    }
+    __syncwarp();
+  } else if (warp < kPWarpU) {
+    // ---------------- epilogue: every tile, in order ----------------
+    const int ew = warp - 2;  // 0..7
+    const int grp = ew >> 2;
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;
+    const bool leader = (warp == 2 + 4 * grp) && lane == 0;
+    const uint64_t pol_out = policy_evict_first();
+    int jg = 0;  // tiles this group has finished
+    bool ok = true;
+    for (int j = 0; j < gamma && ok; ++j) {
+      const int k = j;
+      DraftStat* st_k = (k & 1) ? ba.stats1 : a.stats;
+      for (int g = 0; g < 2 && ok; ++g) {
+        const int b = g * kDM + m;
+        const bool row_ok = b < a.B;
+        int32_t Rp = INT_MIN;
+        ff Sp{0.f, 0.f};
+        for (int t = 0; t < n_local; ++t) {
+          const int tg = (j * 2 + g) * n_local + t;
+          if ((tg & 1) != grp) continue;
+          const int n = tile_of(g, t);
+          const int v0 = n * kDN;
+          const int slot = tg % kDSlots;
+          const uint32_t ubase = sbase + kPOffU + slot * 2 * kBoxU;
+          bool w_ok = wait_or_flag(&bars->acc_full[grp], (tg >> 1) & 1, a.status);
+          w_ok = w_ok && wait_or_flag(&bars->u_full[slot], (tg / kDSlots) & 1, a.status);
+          if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * kDN;
+          int32_t R;
+          float total;
+          bool inf_seen = false;
+          if (v0 + kDN <= a.V)
+            epi_tile<true>(taddr, ubase, m, v0, a.V, a.ep, R, total, inf_seen,
+                           &bars->acc_empty[grp], lane);
+          else
+            epi_tile<false>(taddr, ubase, m, v0, a.V, a.ep, R, total, inf_seen,
+                            &bars->acc_empty[grp], lane);
+          const bool bad = inf_seen || total != total;
+          if (row_ok) {
+            if (bad) set_status(a.status, DSPARK_ERR_BAD_DATA);
+            st_k[static_cast<size_t>(b) * a.n_tiles + n] =
+                DraftStat{bad ? 0.f : total, bad ? INT_MIN : R};
+            if (!bad && total > 0.f) mass_add(Rp, Sp, R, ff{total, 0.f});
+          }
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->st_ready[grp]);
+          if (leader && wait_or_flag(&bars->st_ready[grp], jg & 1, a.status)) {
+            tma_store_3d(&mapL, smem + kPOffU + slot * 2 * kBoxU, v0, k, g * kDM, pol_out);
+            if (v0 + kDK < a.V)
+              tma_store_3d(&mapL, smem + kPOffU + slot * 2 * kBoxU + kBoxU, v0 + kDK, k, g * kDM,
+                           pol_out);
+            bulk_commit();
+            bulk_wait_read<0>();
+            mbar_arrive(&bars->u_empty[slot]);
+          }
+          ++jg;
+          __syncwarp();
+        }
+        if (!ok) break;
+        // the row's mass over the range: group 1 hands its share over through
+        // shared memory, group 0 writes the record; the rows of (g, k) are
+        // stored before the release warp publishes the CTA's tag
+        if (grp == 1) part[g * kDM + m] = DraftPartial{Sp.hi, Sp.lo, Rp, 0};
+        if (leader) {
+          bulk_wait<0>();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        epi_warps_sync();
+        if (grp == 0 && row_ok) {
+          const DraftPartial o = part[g * kDM + m];
+          mass_add(Rp, Sp, o.R, ff{o.hi, o.lo});
+          ba.parts[(static_cast<size_t>(k & 1) * n_req + b) * P + p] =
+              DraftPartial{Sp.hi, Sp.lo, Rp, 0};
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->epi_done[g]);
+      }
+    }
+    if (leader) bulk_wait<0>();
+  } else if (warp == kPWarpRel) {
+    // ---------------- release warp: publishes the CTA's tag of (g, k) ----------------
+    if (lane == 0) {
+      bool ok = true;
+      for (int j = 0; j < gamma && ok; ++j)
+        for (int g = 0; g < 2 && ok; ++g) {
+          ok = wait_or_flag(&bars->epi_done[g], j & 1, a.status);
+          if (!ok) break;
+          // a release at GPU scope: the epilogue's rows, statistics and records,
+          // which this thread saw through epi_done, are visible before the tag
+          st_release_gpu(&tags[g * kMaxBlockCtas + p], static_cast<uint32_t>(j + 1));
+        }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- G warps: each request tile's next G ----------------
+    const int quarter = warp & 3;
+    bool ok = true;
+    for (int g = 0; g < 2 && ok; ++g) {  // G of position 0: W1 at the anchors
+      ok = pair_load_g(ba, g, 0, tmem, quarter, lane);
+      if (ok && lane == 0) mbar_arrive(&bars->a_full[g]);
+    }
+    for (int j = 0; j + 1 < gamma && ok; ++j)
+      for (int g = 0; g < 2 && ok; ++g) {
+        // G of (g, j + 1), once this CTA's MMAs of (g, j) have completed (its
+        // epilogue finished with their accumulators) and the tile's tokens x_j
+        // are drawn (pair_load_g waits for them)
+        ok = __all_sync(0xFFFFFFFFu, wait_or_flag(&bars->epi_done[g], j & 1, a.status));
+        ok = ok && pair_load_g(ba, g, j + 1, tmem, quarter, lane);
+        if (ok && lane == 0) mbar_arrive(&bars->a_full[g]);
+      }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1093,7 +1560,9 @@ int draft_setup(int& sms, bool& coop) {
     if (cudaFuncSetAttribute(k_draft_step, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kDraftSmem)) != cudaSuccess ||
         cudaFuncSetAttribute(k_draft_block, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kDraftSmem)) != cudaSuccess)
+                             static_cast<int>(kDraftSmem)) != cudaSuccess ||
+        cudaFuncSetAttribute(k_draft_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPairSmem)) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     int coop = 0;
     if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
@@ -1190,6 +1659,44 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
   const uint16_t* W1 = static_cast<const uint16_t*>(w1);
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return DSPARK_ERR_CUDA;
   const int grid = n_m * per_m;
+  if (!ev && coop && n_m == 2 && sms > 2 * kPDrawCtas) {
+    // two request tiles: the streaming CTAs serve both, and each tile's draws
+    // (on kPDrawCtas CTAs of their own) and next G overlap the other tile's
+    // streaming
+    const int grid_all = sms < kMaxBlockCtas ? sms : kMaxBlockCtas;
+    const int P = grid_all - kPDrawCtas < n_tiles ? grid_all - kPDrawCtas : n_tiles;
+    if (cudaMemsetAsync(sync, 0,
+                        256 + DSPARK_ALIGN256(static_cast<size_t>(B) * 8) + kTileSyncBytes,
+                        stream) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    DraftBlockArgs ba{};
+    ba.s = DraftStepArgs{B, Vi, r, gamma, 0, n_tiles, n_m, P, ep, stats, device_status};
+    ba.p = DraftPickArgs{B,     Vi,       r, gamma, 0,  n_tiles, ep, stats,
+                         static_cast<const uint16_t*>(draft_logits), uniforms, W1, G,
+                         draft_tokens, device_status, nullptr};
+    ba.k_begin = 0;
+    ba.k_end = gamma;
+    ba.G = nullptr;
+    ba.stats1 = stats1;
+    ba.anchors = anchors;
+    ba.sync = sync;
+    ba.ready = ready;
+    ba.parts = parts;
+    ba.tile_sync = tile_sync;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = P + kPDrawCtas;
+    cfg.blockDim = kPThreads;
+    cfg.dynamicSmemBytes = kPairSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_draft_pair, mapW, mapU, mapL, ba) == cudaSuccess)
+      return DSPARK_OK;
+    (void)cudaGetLastError();  // not resident as one grid: the other paths
+  }
   if (!ev && coop && grid <= sms && grid <= kMaxBlockCtas) {
     // the whole block in one cooperative launch (every CTA resident, one per SM)
     if (cudaMemsetAsync(sync, 0,
