@@ -881,10 +881,10 @@ def drafter_measure(args, dev, stream, rank, ws):
                      "kernel": "k_draft_step (median CUDA-event interval around each of the 16 "
                                "launches, dspark_draft_markov_timed)",
                      "tensor_tflops": flops / (t_step * 1e-3) / 1e12},
-        # the product path, the whole block as one launch: the same bytes per
-        # position (W2 counted once) over the call time, serial chain included
-        # the one cooperative launch: k_draft_pair for two request tiles
-        # (128 < B <= 256), k_draft_block for one
+        # the product path, the whole block as one cooperative launch
+        # (k_draft_pair for two request tiles, 128 < B <= 256; k_draft_block
+        # for one): the same bytes per position (W2 counted once) over the
+        # call time, the chain between positions included
         "block": {"kernel": "k_draft_pair" if 128 < sh["B"] <= 256 else "k_draft_block",
                   "algorithmic_bytes": alg * g,
                   "achieved": alg * g / (t_call * 1e-3) / 1e9, "unit": "GB/s",
