@@ -538,49 +538,45 @@ __device__ __forceinline__ void mass_add(int32_t& R, ff& S, int32_t R2, ff S2) {
 // as in draw_request), that range's tiles are scanned to the crossing tile,
 // and draw_in_tile finishes. Float pairs and exact powers of two throughout,
 // as in draw_request; only the grouping of the sums differs.
-//
-// kWaitTags (the draw CTAs of k_draft_pair): the warp first waits for the
-// tags of every range. Each lane polls only its own ranges' tags (relaxed
-// loads, no warp-wide vote per try) and makes them acquires with a fence; the
-// warp then meets, so every lane's loads of records, statistics and rows come
-// after every lane's acquire. Returns false if a wait gave up (the token is
-// then not published). Measured on 256 x 16 x 129,280 against a warp-wide
-// vote per try: 0.692 against 0.704 ms per block; reading each lane's records
-// before the warp meets made it 0.726 ms, and also copying the lanes' tile
-// statistics to shared memory there 1.17 ms.
+
 constexpr int kRangesHeld = kMaxBlockCtas / 32;  // ranges per lane at most
 __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-template <int kRec, bool kWaitTags = false>  // records per range (one per epilogue group, or one combined)
-__device__ __forceinline__ bool draw_ranges(const DraftPickArgs& a, int b, int lane,
-                                            const DraftPartial* parts, int per_m,
-                                            const uint32_t* tags = nullptr, int k = 0) {
+// One warp waits until the tags of all P ranges (tile_sync words of one
+// request tile) have reached k + 1: each lane polls its own ranges' tags
+// (relaxed loads, no warp-wide vote per try) and makes them acquires with a
+// fence, then the warp meets. Returns false if the wait gave up.
+__device__ __forceinline__ bool wait_range_tags(const uint32_t* tags, int P, int k, int lane) {
+  const int per = (P + 31) / 32;
+  const int p0 = min(lane * per, P), p1 = min(p0 + per, P);
+  WaitClock clock;
+  bool gave_up = false;
+  for (;;) {
+    bool mine = true;
+#pragma unroll
+    for (int i = 0; i < kRangesHeld; ++i)
+      if (p0 + i < p1) mine = mine && ld_relaxed_gpu(tags + p0 + i) >= static_cast<uint32_t>(k + 1);
+    if (mine) break;
+    if (clock.expired()) {
+      gave_up = true;
+      break;
+    }
+    __nanosleep(32);
+  }
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  __syncwarp();
+  return !__any_sync(0xFFFFFFFFu, gave_up);
+}
+
+template <int kRec>  // records per range (one per epilogue group, or one combined)
+__device__ __forceinline__ void draw_ranges(const DraftPickArgs& a, int b, int lane,
+                                            const DraftPartial* parts, int per_m) {
   const int per = (per_m + 31) / 32;
   const int p0 = min(lane * per, per_m), p1 = min(p0 + per, per_m);
   const float u = a.uniforms[static_cast<size_t>(b) * a.gamma + a.k];
-  if constexpr (kWaitTags) {
-    WaitClock clock;
-    bool gave_up = false;
-    for (;;) {
-      bool mine = true;
-#pragma unroll
-      for (int i = 0; i < kRangesHeld; ++i) {
-        if (p0 + i < p1) mine = mine && ld_relaxed_gpu(tags + p0 + i) >= static_cast<uint32_t>(k + 1);
-      }
-      if (mine) break;
-      if (clock.expired()) {
-        gave_up = true;
-        break;
-      }
-      __nanosleep(32);
-    }
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    __syncwarp();  // every lane's later loads come after every lane's acquire
-    if (__any_sync(0xFFFFFFFFu, gave_up)) return false;
-  }
   int32_t rR[kRangesHeld];
   ff rS[kRangesHeld];
   int32_t Rl = INT_MIN;
@@ -605,7 +601,7 @@ __device__ __forceinline__ bool draw_ranges(const DraftPickArgs& a, int b, int l
   if (Rmax == INT_MIN || !(u >= 0.f && u < 1.f)) {
     if (lane == 0) set_status(a.status, DSPARK_ERR_BAD_DATA);
     publish_token(a, b, y, lane);
-    return true;
+    return;
   }
   // level 1: the ranges
   const ff S = Rl == INT_MIN ? ff{0.f, 0.f} : ff_scale(Sl, pow2_nonpos(Rl - Rmax));
@@ -645,7 +641,7 @@ __device__ __forceinline__ bool draw_ranges(const DraftPickArgs& a, int b, int l
   if (ps < 0) {  // no mass where the scan put the cut: the masses and the scan disagree
     if (lane == 0) set_status(a.status, DSPARK_ERR_BAD_DATA);
     publish_token(a, b, y, lane);
-    return true;
+    return;
   }
   // level 2: the tiles of range ps, in order
   const DraftStat* st = a.stats + static_cast<size_t>(b) * a.n_tiles;
@@ -681,7 +677,6 @@ __device__ __forceinline__ bool draw_ranges(const DraftPickArgs& a, int b, int l
   }
   if (g >= 0) y = draw_in_tile<true>(a, b, g, s_before, target, Rmax, lane);
   publish_token(a, b, y, lane);
-  return true;
 }
 
 __global__ void __launch_bounds__(kPickWarps * 32) k_draft_pick(const DraftPickArgs a) {
@@ -1238,25 +1233,32 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int n_draw_warps = (static_cast<int>(gridDim.x) - P) * (kPThreads / 32);
     const int wid = (p - P) * (kPThreads / 32) + warp;
     const size_t n_req = static_cast<size_t>(a.n_m) * kDM;
-    bool ok = true;
-    for (int k = 0; k < a.gamma && ok; ++k)
-      for (int g = 0; g < 2 && ok; ++g) {
-        DraftPickArgs pa = ba.p;
-        pa.k = k;
-        pa.stats = (k & 1) ? ba.stats1 : a.stats;
-        pa.ready = ba.ready;
-        pa.relaxed_flag = true;
-        for (int i = wid; i < kDM && ok; i += n_draw_warps) {
-          const int rq = g * kDM + i;
-          if (rq >= a.B) break;
-          const DraftPartial* parts = ba.parts + (static_cast<size_t>(k & 1) * n_req + rq) * P;
-          ok = draw_ranges<1, true>(pa, rq, lane, parts, P, ba.tile_sync + g * kMaxBlockCtas, k);
-          if (!ok) {
-            if (lane == 0) set_status(a.status, DSPARK_ERR_TIMEOUT);
-            break;
-          }
-        }
+    // warp 0 waits for the tags of (tile, position) and takes the acquire;
+    // the CTA's barrier then orders every warp's loads after it (one poller
+    // per CTA: every warp starts together, and 16 times fewer polls)
+    __shared__ int sh_gave_up[2];  // by parity: rewritten two barriers later
+    for (int it = 0; it < 2 * a.gamma; ++it) {
+      const int k = it >> 1, g = it & 1;
+      if (warp == 0) {
+        const bool got = wait_range_tags(ba.tile_sync + g * kMaxBlockCtas, P, k, lane);
+        if (lane == 0) sh_gave_up[it & 1] = got ? 0 : 1;
       }
+      __syncthreads();
+      if (sh_gave_up[it & 1]) {
+        if (threadIdx.x == 0) set_status(a.status, DSPARK_ERR_TIMEOUT);
+        break;
+      }
+      DraftPickArgs pa = ba.p;
+      pa.k = k;
+      pa.stats = (k & 1) ? ba.stats1 : a.stats;
+      pa.ready = ba.ready;
+      pa.relaxed_flag = true;
+      for (int i = wid; i < kDM; i += n_draw_warps) {
+        const int rq = g * kDM + i;
+        if (rq >= a.B) break;
+        draw_ranges<1>(pa, rq, lane, ba.parts + (static_cast<size_t>(k & 1) * n_req + rq) * P, P);
+      }
+    }
     return;
   }
   const int lo = range_begin(p, a.n_tiles, P), hi = range_begin(p + 1, a.n_tiles, P);
