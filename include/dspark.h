@@ -104,13 +104,14 @@ typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
 #define DSPARK_DRAFT_MAX_RANK 256
 /* Workspace of dspark_draft_markov, in bytes: the gathered embedding rows
    W1[x_{k-1}] of the batch, two buffers of one statistic per (request, tile),
-   the grid-barrier words, one ready flag per request, one barrier per request
-   tile (4 KiB) and (2 MiB) the single launch's per-range masses: two position
-   parities x 256 CTAs at most x 128 requests x 2 records of 16 bytes. */
+   the grid-barrier words, one ready flag per request (each on a 128-byte line
+   of its own), one barrier per request tile (4 KiB) and (2 MiB) the single
+   launch's per-range masses: two position parities x 256 CTAs at most x 128
+   requests x 2 records of 16 bytes. */
 #define DSPARK_DRAFT_WS_BYTES(B, r, V)                                        \
   (DSPARK_ALIGN256((size_t)(B) * (size_t)(r) * 2u) +                          \
    2u * DSPARK_ALIGN256((size_t)(B) * DSPARK_CEILDIV((V), DSPARK_DRAFT_TILE) * 8u) + \
-   256u + DSPARK_ALIGN256((size_t)(B) * 8u) + 4096u + ((size_t)2u << 20))
+   256u + DSPARK_ALIGN256((size_t)(B) * 128u) + 4096u + ((size_t)2u << 20))
 
 /* Workspace of dspark_schedule, in bytes: two (key, index) buffers for the
    sort, per-request lengths and a header. */

@@ -77,7 +77,7 @@ def acceptance_workspace_bytes(B: int, gamma: int, V: int) -> int:
 def draft_workspace_bytes(B: int, r: int, V: int) -> int:
     """Python statement of DSPARK_DRAFT_WS_BYTES (include/dspark.h)."""
     return (_a256(B * r * 2) + 2 * _a256(B * _cdiv(V, _CONSTS["DSPARK_DRAFT_TILE"]) * 8) + 256
-            + _a256(B * 8) + 4096 + (2 << 20))
+            + _a256(B * 128) + 4096 + (2 << 20))
 
 
 def schedule_workspace_bytes(R: int, gamma: int) -> int:

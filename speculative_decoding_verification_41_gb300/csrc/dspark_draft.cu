@@ -70,6 +70,13 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_bf16_f32(kDM, kDN);
 static_assert(kDN == 128 && kDK == 64, "epilogue and statistics assume 128-token tiles");
 static_assert(kColG + DSPARK_DRAFT_MAX_RANK / 2 <= kTmemCols, "tensor memory columns");
+
+// A request's token flag sits alone on a 128-byte line (16 words): every
+// streaming CTA polls the flags, and packed 16 to a line their reads all land
+// on a few L2 slices, which cost the block up to a fifth of its time
+// depending on where the workspace happened to start.
+constexpr int kReadyStride = 16;
+
 static_assert(kDraftSmem <= 232448, "shared memory of k_draft_step");
 // more than half of an SM's 228 KB: one CTA per SM (the single launch maps CTAs by SM id)
 static_assert(kDraftSmem > 233472 / 2, "one drafter CTA per SM");
@@ -387,9 +394,9 @@ __device__ __forceinline__ void publish_token(const DraftPickArgs& a, int b, int
       // k_draft_pair's reader takes only the token from the flag (W1 is an
       // input): no ordering needed; k_draft_block's readers rely on a release
       if (a.relaxed_flag)
-        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(&a.ready[b]), "l"(f) : "memory");
+        asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(&a.ready[b * kReadyStride]), "l"(f) : "memory");
       else
-        st_release_gpu64(&a.ready[b], f);
+        st_release_gpu64(&a.ready[b * kReadyStride], f);
     }
   } else if (a.k + 1 < a.gamma) {
     copy_row(a.W1, a.G, y, b, a.r, lane);
@@ -945,7 +952,7 @@ __device__ __forceinline__ void draft_tiles(const CUtensorMap& mapW, const CUten
           } else {
             WaitClock clock;
             unsigned long long f;
-            while (((f = ld_acquire_gpu64(&ba.ready[b])) >> 32) < static_cast<unsigned>(k)) {
+            while (((f = ld_acquire_gpu64(&ba.ready[b * kReadyStride])) >> 32) < static_cast<unsigned>(k)) {
               if (clock.expired()) {
                 r_ok = false;
                 break;
@@ -1175,7 +1182,7 @@ __device__ __forceinline__ bool pair_load_g(const DraftBlockArgs& ba, int g, int
       WaitClock clock;
       unsigned long long f;
       for (;;) {
-        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(f) : "l"(&ba.ready[b]) : "memory");
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(f) : "l"(&ba.ready[b * kReadyStride]) : "memory");
         if ((f >> 32) >= static_cast<unsigned>(k)) break;
         if (clock.expired()) {
           r_ok = false;
@@ -1641,7 +1648,7 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
   unsigned long long* ready =
       reinterpret_cast<unsigned long long*>(sync + 64);  // 256 bytes after the barrier words
   uint32_t* tile_sync = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(ready) +
-                                                     DSPARK_ALIGN256(static_cast<size_t>(B) * 8));
+                                                     DSPARK_ALIGN256(static_cast<size_t>(B) * 8 * kReadyStride));
   DraftPartial* parts =
       reinterpret_cast<DraftPartial*>(reinterpret_cast<char*>(tile_sync) + kTileSyncBytes);
 
@@ -1672,7 +1679,7 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
     const int grid_all = sms < kMaxBlockCtas ? sms : kMaxBlockCtas;
     const int P = grid_all - kPDrawCtas < n_tiles ? grid_all - kPDrawCtas : n_tiles;
     if (cudaMemsetAsync(sync, 0,
-                        256 + DSPARK_ALIGN256(static_cast<size_t>(B) * 8) + kTileSyncBytes,
+                        256 + DSPARK_ALIGN256(static_cast<size_t>(B) * 8 * kReadyStride) + kTileSyncBytes,
                         stream) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     DraftBlockArgs ba{};
@@ -1706,7 +1713,7 @@ int draft_entry(const void* base_logits, const void* w1, const void* w2t, const 
   if (!ev && coop && grid <= sms && grid <= kMaxBlockCtas) {
     // the whole block in one cooperative launch (every CTA resident, one per SM)
     if (cudaMemsetAsync(sync, 0,
-                        256 + DSPARK_ALIGN256(static_cast<size_t>(B) * 8) + kTileSyncBytes,
+                        256 + DSPARK_ALIGN256(static_cast<size_t>(B) * 8 * kReadyStride) + kTileSyncBytes,
                         stream) != cudaSuccess)
       return DSPARK_ERR_CUDA;
     DraftBlockArgs ba{};
