@@ -829,15 +829,19 @@ def drafter_measure(args, dev, stream, rank, ws):
     torch.cuda.synchronize(dev)
     if int(o["device_status"].item()) != 0:
         raise SystemExit("drafter device status not OK during warm-up")
+    # calls issued back to back with an event pair around each, one
+    # synchronisation at the end (as the verification steps are timed): the
+    # host stays ahead of the GPU, so an interval holds the call's device work,
+    # not the host's time to submit it to an idle GPU
     n = max(5, min(args.steps, 20))
-    ms = []
-    for _ in range(n):
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a0, a1 in evs:
         a0.record(stream)
         call()
         a1.record(stream)
-        torch.cuda.synchronize(dev)
-        ms.append(a0.elapsed_time(a1))
+    torch.cuda.synchronize(dev)
+    ms = [a0.elapsed_time(a1) for a0, a1 in evs]
     # a soak of back-to-back calls with the clocks sampled during it
     clocks = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else
                           int(os.environ.get("LOCAL_RANK", "0")))

@@ -1204,20 +1204,33 @@ __device__ __forceinline__ bool pair_load_g(const DraftBlockArgs& ba, int g, int
   }
   const uint4* src = reinterpret_cast<const uint4*>(ba.p.W1 + static_cast<size_t>(x) * a.r);
   const int KC = a.r / kDK;
-  for (int c = 0; c < KC; ++c) {  // 64 elements (32 columns) at a time
-    uint32_t w[32];
+  const uint32_t t0 = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kColG +
+                      static_cast<uint32_t>(g) * (DSPARK_DRAFT_MAX_RANK / 2);
+  // two 64-element chunks (32 columns each) per round: both chunks' loads are
+  // in flight before the first store to tensor memory (a store is ordered
+  // after every earlier load of the warp)
+  for (int c = 0; c < KC; c += 2) {
+    const bool two = c + 1 < KC;
+    uint32_t w0[32], w1[32];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint4 v = row_ok ? __ldg(src + c * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
-      w[4 * i] = v.x;
-      w[4 * i + 1] = v.y;
-      w[4 * i + 2] = v.z;
-      w[4 * i + 3] = v.w;
+      w0[4 * i] = v.x;
+      w0[4 * i + 1] = v.y;
+      w0[4 * i + 2] = v.z;
+      w0[4 * i + 3] = v.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 v = row_ok && two ? __ldg(src + (c + 1) * 8 + i) : make_uint4(0u, 0u, 0u, 0u);
+      w1[4 * i] = v.x;
+      w1[4 * i + 1] = v.y;
+      w1[4 * i + 2] = v.z;
+      w1[4 * i + 3] = v.w;
     }
     __syncwarp();
-    tmem_st32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + kColG +
-                  static_cast<uint32_t>(g) * (DSPARK_DRAFT_MAX_RANK / 2) + c * 32,
-              w);
+    tmem_st32(t0 + c * 32, w0);
+    if (two) tmem_st32(t0 + (c + 1) * 32, w1);
   }
   tmem_wait_st();
   tc_fence_before();
