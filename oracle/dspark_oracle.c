@@ -471,7 +471,7 @@ int oracle_schedule(const float* confidences, const double* step_time,
 
 /*
  * The greedy admission path of Algorithm 1 [P-3.2.2, P2-Alg1], written out in
- * full for a comparison that has to judge another implementation's stopping
+ * full for a comparison that has to check another implementation's stopping
  * point: the candidates of E in the loop's order and Theta after each
  * admission, with no break.
  *   order[i]  : flattened index r*gamma + (j-1) of the (i+1)-th candidate

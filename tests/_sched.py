@@ -55,8 +55,8 @@ def lengths_of_prefix(order, n, R, gamma):
     return ell
 
 
-def judge_schedule(ell, theta, path, R, gamma, early_stop=True):
-    """Judge another implementation's scheduler output against the oracle's
+def assess_schedule(ell, theta, path, R, gamma, early_stop=True):
+    """Assess another implementation's scheduler output against the oracle's
     admission path (oracle.schedule_path). Every request's length must be the
     one its admitted count n = sum(l) gives along the oracle's order; n itself
     must be where the oracle's rule stops, except where the comparison that

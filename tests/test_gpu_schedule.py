@@ -12,7 +12,7 @@ import oracle
 from speculative_decoding_verification_41_gb300 import binding, workloads
 from speculative_decoding_verification_41_gb300 import build as cuda_build
 from tests._gpu import PROB_RTOL_QUALITY, compare, oracle_on_requests
-from tests._sched import judge_schedule
+from tests._sched import assess_schedule
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -43,7 +43,7 @@ def check(conf, T, dev, no_ties=False):
     ell, theta, ties = gpu_schedule(conf, T, dev)
     ref = oracle.schedule(conf, T, early_stop=True)
     R, g = conf.shape
-    excused = judge_schedule(ell, theta, oracle.schedule_path(conf, T), R, g, early_stop=True)
+    excused = assess_schedule(ell, theta, oracle.schedule_path(conf, T), R, g, early_stop=True)
     if ref["near_ties"] == 0 or no_ties:
         assert ref["near_ties"] == 0 and excused == 0
         np.testing.assert_array_equal(ell, ref["verify_len"])

@@ -3,7 +3,7 @@ candidates, ranks against the other blocks, a sweep over tiles of 8,192
 positions), which takes the batches whose candidates exceed what the rank
 path holds in shared memory. Against the oracle (DSpark paper section 3.2.2,
 Algorithm 1; section 5.2 for the capacity and the top-K admission): every
-request's length judged along the oracle's admission path, Theta, and the
+request's length checked along the oracle's admission path, Theta, and the
 stopping points that fall on a tile's first and last positions."""
 import numpy as np
 import pytest
@@ -12,7 +12,7 @@ import torch
 import oracle
 from speculative_decoding_verification_41_gb300 import binding, workloads
 from speculative_decoding_verification_41_gb300 import build as cuda_build
-from tests._sched import judge_schedule
+from tests._sched import assess_schedule
 
 pytestmark = pytest.mark.gpu
 TILE = 8192  # positions per tile of the block path's sweep
@@ -40,7 +40,7 @@ def check_stop(conf, T, dev, no_ties=False):
     ell, theta, _ = run_stop(conf, T, dev)
     ref = oracle.schedule(conf, T, early_stop=True)
     R, g = conf.shape
-    excused = judge_schedule(ell, theta, oracle.schedule_path(conf, T), R, g, early_stop=True)
+    excused = assess_schedule(ell, theta, oracle.schedule_path(conf, T), R, g, early_stop=True)
     if ref["near_ties"] == 0 or no_ties:
         assert ref["near_ties"] == 0 and excused == 0
         np.testing.assert_array_equal(ell, ref["verify_len"])
@@ -56,7 +56,7 @@ def check_capacity(conf, T, dev):
     assert K == int(ell.sum())
     ref = oracle.schedule(conf, T, early_stop=False)
     R, g = conf.shape
-    excused = judge_schedule(ell, theta, oracle.schedule_path(conf, T), R, g, early_stop=False)
+    excused = assess_schedule(ell, theta, oracle.schedule_path(conf, T), R, g, early_stop=False)
     if ref["near_ties"] == 0:
         assert excused == 0 and K == ref["n_admitted"]
         np.testing.assert_array_equal(ell, ref["verify_len"])

@@ -14,7 +14,7 @@ import torch
 import oracle
 from speculative_decoding_verification_41_gb300 import binding, workloads
 from speculative_decoding_verification_41_gb300 import build as cuda_build
-from tests._sched import judge_schedule
+from tests._sched import assess_schedule
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -69,7 +69,7 @@ def check_capacity(conf, T, dev, no_ties=False):
     ref = oracle.schedule(conf, T, early_stop=False)
     R, g = conf.shape
     assert K == int(ell.sum())
-    excused = judge_schedule(ell, theta, oracle.schedule_path(conf, T), R, g, early_stop=False)
+    excused = assess_schedule(ell, theta, oracle.schedule_path(conf, T), R, g, early_stop=False)
     if ref["near_ties"] == 0 or no_ties:
         assert ref["near_ties"] == 0 and excused == 0
         assert K == ref["n_admitted"]

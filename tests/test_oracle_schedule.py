@@ -102,7 +102,7 @@ def test_admission_path_matches_independent_statement(seed):
     (numpy stable sort of the survival products) and Theta recomputed from the
     objective's definition at every prefix; the early-stop and global-search
     results sit on that path where their rules put them."""
-    from tests._sched import judge_schedule, lengths_of_prefix
+    from tests._sched import assess_schedule, lengths_of_prefix
     rng = np.random.default_rng(300 + seed)
     R, g = int(rng.integers(1, 7)), int(rng.integers(1, 6))
     conf = _confidences(rng, R, g)
@@ -117,14 +117,14 @@ def test_admission_path_matches_independent_statement(seed):
         assert abs(p["theta"][n] - theta_of(ell, conf, T)) <= 1e-12 * p["theta"][n]
     for es in (True, False):
         s = oracle.schedule(conf, T, early_stop=es)
-        assert judge_schedule(s["verify_len"], s["theta_best"], p, R, g, early_stop=es) == 0
+        assert assess_schedule(s["verify_len"], s["theta_best"], p, R, g, early_stop=es) == 0
         assert p["theta"][s["n_admitted"]] == s["theta_best"]
 
 
-def test_judge_rejects_a_wrong_stopping_point():
+def test_assess_rejects_a_wrong_stopping_point():
     """The comparison the GPU tests use refuses a length vector one admission
     short of or past the oracle's, and one that is not a prefix of its order."""
-    from tests._sched import judge_schedule, lengths_of_prefix
+    from tests._sched import assess_schedule, lengths_of_prefix
     rng = np.random.default_rng(5)
     R, g = 6, 4
     conf = _confidences(rng, R, g)
@@ -136,7 +136,7 @@ def test_judge_rejects_a_wrong_stopping_point():
     assert 0 < n < len(p["order"])
     for m in (n - 1, n + 1):
         with pytest.raises(AssertionError):
-            judge_schedule(lengths_of_prefix(p["order"], m, R, g), None, p, R, g)
+            assess_schedule(lengths_of_prefix(p["order"], m, R, g), None, p, R, g)
     bad = s["verify_len"].copy()
     r = int(np.argmax(bad))
     bad[r] -= 1
@@ -144,7 +144,7 @@ def test_judge_rejects_a_wrong_stopping_point():
     bad[other] += 1
     if not np.array_equal(bad, s["verify_len"]):
         with pytest.raises(AssertionError):
-            judge_schedule(bad, None, p, R, g)
+            assess_schedule(bad, None, p, R, g)
 
 
 def test_negative_zero_confidence_acts_as_zero():
