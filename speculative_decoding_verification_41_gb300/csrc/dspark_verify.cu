@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verif
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t carry;
   __shared__ int32_t sh_start[1025];  // this chunk's row starts (and the chunk's end)
+  __shared__ long long sh_tb[1024], sh_db[1024];  // this chunk's first target and draft rows
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     *status = DSPARK_OK;
@@ -98,6 +99,10 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verif
     const int r = base + tid;
     int cnt = 0;
     if (r < B) {
+      // the request's first rows, kept for the row list below (no dependent
+      // load per request there)
+      sh_tb[tid] = toff ? toff[r] : static_cast<long long>(r) * (gamma + 1);
+      sh_db[tid] = doff ? doff[r] : static_cast<long long>(r) * gamma;
       const int ell = verify_len[r];
       bool ok = ell >= 0 && ell <= gamma;
       if (ok && toff) {
@@ -149,8 +154,7 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verif
       const int start = sh_start[q], end = sh_start[q + 1];
       if (end == start) continue;  // invalid request: nothing to read
       const int ell = (end - start - 1) / 2;
-      const long long tb = toff ? toff[rq] : (long long)rq * (gamma + 1);
-      const long long db = doff ? doff[rq] : (long long)rq * gamma;
+      const long long tb = sh_tb[q], db = sh_db[q];
       for (int i = lane; i < end - start; i += 32)
         ws.row_list[start + i] = i <= ell ? (tb + i) << 1 : ((db + i - ell - 1) << 1) | 1;
     }
