@@ -59,6 +59,8 @@ SMALL = [
     (8, 16, 10000, torch.bfloat16, 0.05, "full", False),     # cold: nearly one-hot rows
     (8, 16, 10000, torch.bfloat16, 20.0, "uniform", False),  # hot: nearly flat rows
     (6, 8, 7000, torch.float32, 0.05, "uniform", True),      # cold fp32, ragged
+    (1500, 4, 1024, torch.bfloat16, 1.0, "uniform", True),   # B > 1024: the planner's 2nd chunk
+    (1100, 2, 512, torch.float32, 0.8, "uniform", False),    # the same, dense
 ]
 
 
