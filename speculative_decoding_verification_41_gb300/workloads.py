@@ -113,11 +113,17 @@ class VerifyInputs:
     draft_tokens: torch.Tensor      # [B, gamma] int32
     verify_len: torch.Tensor        # [B] int32
     uniforms: torch.Tensor          # [B, gamma+1] float32
-    temperature: float
+    temperature: float              # a binary32 value (see __post_init__)
     target_row_off: Optional[torch.Tensor] = None  # [B+1] int64
     draft_row_off: Optional[torch.Tensor] = None   # [B+1] int64
     name: str = ""
     meta: dict = field(default_factory=dict)
+
+    def __post_init__(self):
+        # the verification call takes the temperature as a binary32 value:
+        # the value kept here is that one, so that every consumer (the call,
+        # the oracle) is handed the same temperature
+        self.temperature = float(np.float32(self.temperature))
 
     @property
     def B(self) -> int:
