@@ -1,4 +1,5 @@
-"""dspark_verify on seeded random shapes against the CPU oracle.
+"""dspark_verify (and dspark_acceptance) on seeded random shapes against the
+CPU oracle.
 
 Each case draws, from its own generator:
 - the batch size, the block length gamma (1..32) and the vocabulary (8..6,000).
@@ -65,3 +66,14 @@ def test_random_shapes(dev, seed):
     ref = oracle_on_requests(vi, idx)
     st = compare(out, ref, vi, idx)
     assert st["prob_max_rel_err"] <= PROB_RTOL_QUALITY, (B, g, V, dt, T, ragged, st)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes_acceptance(dev, seed):
+    """dspark_acceptance (every verified position's sum_v min(p_t, p_d)) on
+    the same random shapes, within the probability tolerance of the oracle."""
+    from tests.test_gpu_acceptance import check as check_acceptance
+    B, g, V, dt, T, rho, ell, ragged = draw_case(100 + seed)
+    vi = workloads.make_verify(B, g, V, dt, T, rho=rho, verify_len=ell, ragged=ragged,
+                               seed=seed + 5, device=dev)
+    check_acceptance(vi)
