@@ -346,8 +346,11 @@ class MarkovDraftInputs:
     w2t: torch.Tensor
     anchors: torch.Tensor
     uniforms: torch.Tensor
-    temperature: float
+    temperature: float              # a binary32 value, as the drafter's call takes it
     name: str = ""
+
+    def __post_init__(self):
+        self.temperature = float(np.float32(self.temperature))
 
     @property
     def B(self) -> int:
