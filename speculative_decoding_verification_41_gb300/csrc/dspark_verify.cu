@@ -147,10 +147,9 @@ __global__ void __launch_bounds__(1024) k_plan(const int32_t* __restrict__ verif
     }
     __syncthreads();
     // the chunk's row list: one warp per request, lanes over its rows
-    // (coalesced stores), the starts from shared memory
+    // (coalesced stores), the starts and first rows from shared memory
     const int nb = B - base < 1024 ? B - base : 1024;
     for (int q = warp; q < nb; q += 32) {
-      const int rq = base + q;
       const int start = sh_start[q], end = sh_start[q + 1];
       if (end == start) continue;  // invalid request: nothing to read
       const int ell = (end - start - 1) / 2;
